@@ -1,0 +1,189 @@
+"""GB300 (sm_103a) fp16 GEMM  D = A·Bᵀ  — Python binding of the C ABI.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library ``_build/libgemm_f16.so`` (see ``include/gemm_f16.h``). PyTorch only
+supplies device memory and streams. There is no fallback: if the library
+cannot be built or loaded, every call raises.
+
+    import torch, blackwell_tensor_core_02_gb300 as g
+    A = torch.randn(4096, 4096, device="cuda", dtype=torch.float16)
+    B = torch.randn(4096, 4096, device="cuda", dtype=torch.float16)   # N×K
+    D = g.gemm_f16_nt(A, B)                                          # M×N = A @ B.T
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "GemmError", "Options", "load", "gemm_f16_nt", "gemm_f16_nt_ptr", "gemm_f16_nt_supported",
+    "gemm_f16_nt_host", "last_device_status", "status_string", "schedule", "cta_origin", "pipeline_trace", "STATUS",
+]
+
+STATUS = {
+    0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED_SHAPE", -3: "GEMM_ERR_MISALIGNED",
+    -4: "GEMM_ERR_NO_DEVICE", -5: "GEMM_ERR_ARCH", -6: "GEMM_ERR_LAUNCH", -7: "GEMM_ERR_DEVICE_TIMEOUT",
+    -8: "GEMM_ERR_CUDA",
+}
+
+
+class GemmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+class Options(ctypes.Structure):
+    """Mirror of ``gemm_f16_options`` (zero fields mean defaults)."""
+    _fields_ = [("cta_group", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
+                ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib: ctypes.CDLL | None = None
+
+
+def load() -> ctypes.CDLL:
+    """Build (if stale) and load the CUDA library; raise if that is impossible."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        i64p, i32p = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+        lib.gemm_f16_nt.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+        lib.gemm_f16_nt.restype = ctypes.c_int
+        lib.gemm_f16_nt_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+        lib.gemm_f16_nt_ex.restype = ctypes.c_int
+        lib.gemm_f16_nt_supported.argtypes = [i64, i64, i64]
+        lib.gemm_f16_nt_supported.restype = ctypes.c_int
+        lib.gemm_f16_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+        lib.gemm_f16_last_device_status.restype = ctypes.c_int
+        lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
+        lib.gemm_f16_status_string.restype = ctypes.c_char_p
+        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i32, i32, i64, i64, i64, i64p, i64p]
+        lib.gemm_f16_nt_schedule.restype = ctypes.c_int
+        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i64, i64, i32, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
+        lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
+        lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().gemm_f16_status_string(int(code)).decode()
+
+
+def gemm_f16_nt_supported(M: int, N: int, K: int) -> bool:
+    return bool(load().gemm_f16_nt_supported(M, N, K))
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def gemm_f16_nt_ptr(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, stream: int | None = 0,
+                    options: Options | None = None) -> int:
+    """Raw C-ABI call with device pointers; returns the status code (no raise)."""
+    lib = load()
+    if options is None:
+        return lib.gemm_f16_nt(A_ptr, B_ptr, D_ptr, M, N, K, stream)
+    return lib.gemm_f16_nt_ex(A_ptr, B_ptr, D_ptr, M, N, K, stream, ctypes.byref(options))
+
+
+def gemm_f16_nt(A, B, D=None, *, stream=None, options: Options | None = None):
+    """D = A·Bᵀ for fp16 CUDA tensors A (M×K) and B (N×K); returns D (M×N)."""
+    import torch
+
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("A and B must be torch.float16")
+    if A.dim() != 2 or B.dim() != 2 or A.shape[1] != B.shape[1]:
+        raise ValueError(f"expected A (M×K) and B (N×K), got {tuple(A.shape)} and {tuple(B.shape)}")
+    if not (A.is_cuda and B.is_cuda) or not (A.is_contiguous() and B.is_contiguous()):
+        raise ValueError("A and B must be contiguous CUDA tensors")
+    M, K = A.shape
+    N = B.shape[0]
+    if D is None:
+        D = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    elif D.dtype != torch.float16 or tuple(D.shape) != (M, N) or not D.is_contiguous() or not D.is_cuda:
+        raise ValueError("D must be a contiguous fp16 CUDA tensor of shape (M, N)")
+    with torch.cuda.device(A.device):
+        rc = gemm_f16_nt_ptr(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _stream_handle(stream), options)
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_nt")
+    return D
+
+
+def gemm_f16_nt_host(A_host, B_host, D_host=None, *, device=None, stream=None, A_dev=None, B_dev=None,
+                     D_dev=None):
+    """End-to-end call on HOST fp16 tensors: copy A, B in, run the GEMM, copy D out.
+
+    Pass pinned host tensors for asynchronous copies and (optionally) reusable
+    device buffers. Returns the host D after the stream has finished.
+    """
+    import torch
+
+    dev = torch.device(device or "cuda")
+    s = stream or torch.cuda.current_stream(dev)
+    M, K = A_host.shape
+    N = B_host.shape[0]
+    with torch.cuda.stream(s):
+        A_dev = A_dev if A_dev is not None else torch.empty((M, K), dtype=torch.float16, device=dev)
+        B_dev = B_dev if B_dev is not None else torch.empty((N, K), dtype=torch.float16, device=dev)
+        D_dev = D_dev if D_dev is not None else torch.empty((M, N), dtype=torch.float16, device=dev)
+        if D_host is None:
+            D_host = torch.empty((M, N), dtype=torch.float16, pin_memory=True)
+        A_dev.copy_(A_host, non_blocking=True)
+        B_dev.copy_(B_host, non_blocking=True)
+        gemm_f16_nt(A_dev, B_dev, D_dev, stream=s)
+        D_host.copy_(D_dev, non_blocking=True)
+    s.synchronize()
+    return D_host
+
+
+def last_device_status(stream=None) -> tuple[int, int]:
+    """(status, info) of the device status word, after synchronising `stream`; clears it."""
+    info = ctypes.c_uint64(0)
+    rc = load().gemm_f16_last_device_status(_stream_handle(stream), ctypes.byref(info))
+    return rc, info.value
+
+
+def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
+             it: int):
+    """The scheduler's iter-th tile (m_idx, n_idx) of one cluster, or None when it has no more."""
+    m, n = ctypes.c_int64(), ctypes.c_int64()
+    rc = load().gemm_f16_nt_schedule(M, N, cta_group, raster_group, num_clusters, cluster_id, it,
+                                     ctypes.byref(m), ctypes.byref(n))
+    if rc < 0:
+        raise GemmError(rc, "gemm_f16_nt_schedule")
+    return (m.value, n.value) if rc == 1 else None
+
+
+def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int) -> dict:
+    """Rows/columns CTA `rank` of tile (m_idx, n_idx) loads and writes (see the C header)."""
+    out = [ctypes.c_int64() for _ in range(4)]
+    rc = load().gemm_f16_nt_cta_origin(cta_group, m_idx, n_idx, rank, *[ctypes.byref(o) for o in out])
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_nt_cta_origin")
+    return dict(zip(("a_row", "b_row", "d_row", "d_col"), (o.value for o in out)))
+
+
+def pipeline_trace(depth: int, initial_phase: int, steps: int) -> list[tuple[int, int]]:
+    """The (stage, phase) a ring's PipelineState shows before each of `steps` advances."""
+    st = (ctypes.c_int32 * max(steps, 1))()
+    ph = (ctypes.c_int32 * max(steps, 1))()
+    rc = load().gemm_f16_pipeline_trace(depth, initial_phase, steps, st, ph)
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_pipeline_trace")
+    return [(st[i], ph[i]) for i in range(steps)]

@@ -1,0 +1,319 @@
+// gemm_f16.cu -- host side of the C ABI declared in include/gemm_f16.h:
+// argument validation, TMA tensor-map encoding, per-device launch caches and
+// the cluster launch of the persistent kernel.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_f16.h"
+#include "gemm_kernel.cuh"
+#include "schedule.h"
+
+namespace gemm_f16 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kDefaultTimeoutNs = 4000000000LL;
+constexpr int32_t kDefaultRasterGroup = 8;
+constexpr int64_t kDimLimit = (int64_t(1) << 31) - 1;
+
+struct DeviceInfo {
+    bool ready = false;
+    int status = GEMM_OK;
+    int sm_count = 0;
+    int max_clusters[3] = {0, 0, 0};  // co-resident clusters for cta_group 1 and 2
+};
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+template <int CG>
+cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(Cfg<CG>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG>::SMEM_ALLOC;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cfg;
+}
+
+template <int CG>
+int prepare_kernel(int *max_clusters) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<CG>::SMEM_ALLOC);
+    if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config<CG>(dim3(CG, 1, 1), nullptr, attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG>, &cfg);
+    if (e != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
+    *max_clusters = n;
+    return GEMM_OK;
+}
+
+// Per-device set-up, once: architecture check, SM count, kernel attributes,
+// co-resident cluster counts, and the driver's tensor-map encoder.
+int device_setup(int *dev_out, DeviceInfo **info_out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo &d = g_devices[dev];
+    if (!d.ready) {
+        d.ready = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            d.status = GEMM_ERR_NO_DEVICE;
+        } else if (major != 10 || minor != 3) {
+            d.status = GEMM_ERR_ARCH;
+        } else {
+            d.status = prepare_kernel<1>(&d.max_clusters[1]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<2>(&d.max_clusters[2]);
+        }
+        if (d.status == GEMM_OK && g_encode == nullptr) {
+            void *fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                d.status = GEMM_ERR_CUDA;
+            } else {
+                g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+            }
+        }
+        cudaGetLastError();
+    }
+    *dev_out = dev;
+    *info_out = &d;
+    return d.status;
+}
+
+// Row-major fp16 matrix rows x cols, tiles of box_rows x 64 columns, 128-byte
+// swizzle, zero fill past the edges.
+int encode_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, uint32_t box_rows) {
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {64u, box_rows};
+    cuuint32_t estride[2] = {1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void *>(ptr), gdim, gstride, box,
+                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+bool shape_ok(int64_t M, int64_t N, int64_t K) {
+    return M >= 0 && N >= 0 && K >= 0 && M <= kDimLimit && N <= kDimLimit && K <= kDimLimit && N % 8 == 0 &&
+           K % 8 == 0;
+}
+
+template <int CG>
+int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+           const DeviceInfo &dev, int32_t max_clusters, int32_t raster_group, int64_t timeout_ns,
+           uint32_t debug_flags) {
+    using C = Cfg<CG>;
+    CUtensorMap tmA, tmB, tmD;
+    if (encode_map(&tmA, A, M, K, C::BLOCK_M) != GEMM_OK || encode_map(&tmB, B, N, K, C::B_ROWS) != GEMM_OK ||
+        encode_map(&tmD, D, M, N, 32) != GEMM_OK) {
+        return GEMM_ERR_CUDA;
+    }
+    Params p;
+    p.M = static_cast<int32_t>(M);
+    p.N = static_cast<int32_t>(N);
+    p.K = static_cast<int32_t>(K);
+    p.num_m_tiles = static_cast<int32_t>((M + C::TILE_M - 1) / C::TILE_M);
+    p.num_n_tiles = static_cast<int32_t>((N + C::BLOCK_N - 1) / C::BLOCK_N);
+    p.k_tiles = static_cast<int32_t>((K + C::BLOCK_K - 1) / C::BLOCK_K);
+    const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
+    if (tiles > kDimLimit) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    p.num_tiles = static_cast<int32_t>(tiles);
+    p.raster_group = raster_group;
+    p.debug_flags = debug_flags;
+    p.timeout_ns = static_cast<uint64_t>(timeout_ns);
+    int64_t clusters = dev.max_clusters[CG];
+    if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
+    if (clusters > tiles) clusters = tiles;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config<CG>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG>, tmA, tmB, tmD, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_LAUNCH;
+    }
+    return GEMM_OK;
+}
+
+int zero_fill(void *D, int64_t M, int64_t N, cudaStream_t stream) {
+    const int64_t elems = M * N;
+    const int64_t n16 = elems / 8;
+    const int64_t ntail = elems - n16 * 8;
+    uint16_t *tail = reinterpret_cast<uint16_t *>(D) + n16 * 8;
+    int64_t blocks = (n16 + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > 65535) blocks = 65535;
+    zero_fill_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(reinterpret_cast<uint4 *>(D), n16, tail,
+                                                                         ntail);
+    if (cudaGetLastError() != cudaSuccess) return GEMM_ERR_LAUNCH;
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gemm_f16
+
+using namespace gemm_f16;
+
+extern "C" {
+
+int gemm_f16_nt_supported(int64_t M, int64_t N, int64_t K) { return shape_ok(M, N, K) ? 1 : 0; }
+
+int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
+                   const gemm_f16_options *opts) {
+    int32_t cta_group = 2, max_clusters = 0, raster_group = kDefaultRasterGroup;
+    int64_t timeout_ns = kDefaultTimeoutNs;
+    uint32_t debug_flags = 0;
+    if (opts) {
+        if (opts->cta_group != 0) cta_group = opts->cta_group;
+        if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
+            (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
+            return GEMM_ERR_INVALID_ARG;
+        }
+        debug_flags = static_cast<uint32_t>(opts->debug_flags);
+        max_clusters = opts->max_clusters;
+        if (opts->raster_group != 0) raster_group = opts->raster_group;
+        if (opts->timeout_ns != 0) timeout_ns = opts->timeout_ns;
+    }
+    if (cta_group != 1 && cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return GEMM_OK;  // empty product: nothing to write
+    if (!D || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(D) & 15u) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) ||
+                                                             (reinterpret_cast<uintptr_t>(B) & 15u)))) {
+        return GEMM_ERR_MISALIGNED;
+    }
+    int dev = -1;
+    DeviceInfo *info = nullptr;
+    const int st = device_setup(&dev, &info);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_fill(D, M, N, s);
+    if (cta_group == 2) return launch<2>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags);
+    return launch<1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags);
+}
+
+int gemm_f16_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream) {
+    return gemm_f16_nt_ex(A, B, D, M, N, K, stream, nullptr);
+}
+
+int gemm_f16_last_device_status(void *stream, uint64_t *info) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    int status = 0;
+    unsigned long long where = 0;
+    const int zero = 0;
+    const unsigned long long zero64 = 0;
+    if (cudaMemcpyFromSymbol(&status, g_status, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyFromSymbol(&where, g_info, sizeof(where)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_info, &zero64, sizeof(zero64)) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (info) *info = where;
+    return status;
+}
+
+const char *gemm_f16_status_string(int status) {
+    switch (status) {
+        case GEMM_OK: return "GEMM_OK";
+        case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: null pointer, negative size or bad option";
+        case GEMM_ERR_UNSUPPORTED_SHAPE:
+            return "GEMM_ERR_UNSUPPORTED_SHAPE: N and K must be multiples of 8 and below 2^31";
+        case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: A, B and D must be 16-byte aligned";
+        case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no usable CUDA device";
+        case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: the current device is not sm_103 (GB300)";
+        case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
+        case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a wait inside the kernel ran out";
+        case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime or driver error";
+        default: return "unknown gemm_f16 status";
+    }
+}
+
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster_group, int64_t num_clusters,
+                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx) {
+    if (cta_group == 0) cta_group = 2;
+    if (raster_group == 0) raster_group = kDefaultRasterGroup;
+    if ((cta_group != 1 && cta_group != 2) || raster_group < 0 || M <= 0 || N <= 0 || M > kDimLimit ||
+        N > kDimLimit || num_clusters <= 0 || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !m_idx ||
+        !n_idx) {
+        return GEMM_ERR_INVALID_ARG;
+    }
+    const int64_t tile_m = 128 * cta_group, tile_n = 256;
+    const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
+    const int64_t tiles = num_m * num_n;
+    if (tiles > kDimLimit) return GEMM_ERR_INVALID_ARG;
+    const int64_t t = cluster_id + iter * num_clusters;
+    if (t >= tiles) return 0;
+    const TileCoord c = tile_of(static_cast<int32_t>(t), static_cast<int32_t>(num_m), static_cast<int32_t>(num_n),
+                                raster_group);
+    *m_idx = c.m_idx;
+    *n_idx = c.n_idx;
+    return 1;
+}
+
+int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int32_t rank, int64_t *a_row,
+                           int64_t *b_row, int64_t *d_row, int64_t *d_col) {
+    if (cta_group == 0) cta_group = 2;
+    if ((cta_group != 1 && cta_group != 2) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
+        m_idx * 128 * cta_group > kDimLimit || n_idx * 256 > kDimLimit || !a_row || !b_row || !d_row || !d_col) {
+        return GEMM_ERR_INVALID_ARG;
+    }
+    TileCoord tc;
+    tc.m_idx = static_cast<int32_t>(m_idx);
+    tc.n_idx = static_cast<int32_t>(n_idx);
+    const CtaOrigin o = cta_origin(tc, cta_group, rank);
+    *a_row = o.a_row;
+    *b_row = o.b_row;
+    *d_row = o.d_row;
+    *d_col = o.d_col;
+    return GEMM_OK;
+}
+
+int gemm_f16_pipeline_trace(int32_t depth, int32_t initial_phase, int32_t steps, int32_t *stage_out,
+                            int32_t *phase_out) {
+    if (depth < 1 || depth > 16 || (initial_phase != 0 && initial_phase != 1) || steps < 0 ||
+        (steps > 0 && (!stage_out || !phase_out))) {
+        return GEMM_ERR_INVALID_ARG;
+    }
+    PipelineState ring(depth, static_cast<uint32_t>(initial_phase));
+    for (int32_t i = 0; i < steps; ++i) {
+        stage_out[i] = ring.stage;
+        phase_out[i] = static_cast<int32_t>(ring.phase);
+        ring.advance();
+    }
+    return GEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,380 @@
+// gemm_kernel.cuh -- the persistent, warp-specialized sm_103a GEMM kernel.
+//
+// D (M x N, fp16) = A (M x K, fp16) * B (N x K, fp16)^T, fp32 accumulation in
+// tensor memory, one round to fp16 at writeback.
+//
+// The data path is the pages' fixed hop chain ("GEMM I -- the tiled
+// baseline", "The one invariant"): GMEM -TMA-> swizzled SMEM -tcgen05.mma->
+// TMEM (fp32) -tcgen05.ld-> registers -cast-> SMEM -TMA-> GMEM.
+//
+// Roles (one CTA = 6 warps, "GEMM III", Step 7; TIRx notes V7 "Warp Roles"):
+//   warp 0     TMA producer: one elected lane fills the SMEM ring.
+//   warp 1     TMEM allocator; in the leader CTA also the MMA issuer (one
+//              elected lane issues every tcgen05.mma, "GEMM I", "Why one
+//              elected thread issues the MMA").
+//   warps 2-5  epilogue: each warp owns one 32-lane quarter of TMEM (warp w
+//              may only touch lanes 32*(w%4) .. +31), i.e. 32 rows of the tile.
+//
+// Two producer-consumer rings ("GEMM III", "Four barriers"; TIRx notes V7):
+//   SMEM ring:  empty[s] (mma2tma) -> TMA -> full[s] (tma2mma) -> MMA -> empty[s]
+//   TMEM ring:  tmem_empty[a] (ld2mma) -> MMA -> tmem_full[a] (mma2ld) -> epilogue
+// The TMEM ring has two accumulator buffers, so the epilogue of tile i runs
+// while the MMA issuer already accumulates tile i+1 into the other buffer.
+//
+// CTA pair (CG = 2; "GEMM III", Step 8; TIRx notes V8): a 2-CTA cluster owns a
+// 256 x 256 tile.  CTA r loads A rows m_base + 128r and B rows n_base + 128r
+// into its own SMEM; the leader (rank 0) alone issues cta_group::2 MMAs of
+// M = 256, N = 256 that read both CTAs' SMEM and write each CTA's own TMEM
+// ([A_r B_0^T | A_r B_1^T]).  Both CTAs' TMA bytes complete on the leader's
+// full[s]; the MMA commits arrive on empty[s] / tmem_full[a] of both CTAs
+// (cta_mask 0b11); tmem_empty[a] on the leader counts the epilogue warps of
+// both CTAs.
+//
+// Every wait is bounded: after `timeout_ns` the waiting role records an error
+// in the device status word, raises the CTA's abort flag and falls through to
+// teardown, so a protocol error ends the kernel instead of hanging the GPU.
+#pragma once
+
+#include <stdint.h>
+
+#include "ptx.cuh"
+#include "schedule.h"
+
+namespace gemm_f16 {
+
+__device__ int g_status;              // first error code of any CTA (0 = none)
+__device__ unsigned long long g_info; // where it happened (role, CTA, tile seq)
+
+enum : int { kStatusTimeout = -7 };
+enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+
+template <int CG>
+struct Cfg {
+    static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
+    static constexpr int BLOCK_M = 128;                 // rows of D per CTA
+    static constexpr int BLOCK_N = 256;                 // columns of D per tile (MMA N)
+    static constexpr int BLOCK_K = 64;                  // one 128-byte swizzle row of fp16
+    static constexpr int TILE_M = BLOCK_M * CG;         // rows of D per tile (MMA M)
+    static constexpr int UMMA_K = 16;                   // K of one tcgen05.mma kind::f16
+    static constexpr int B_ROWS = BLOCK_N / CG;         // rows of B each CTA loads
+    static constexpr int A_STAGE = BLOCK_M * BLOCK_K * 2;
+    static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
+    static constexpr int STAGES = CG == 2 ? 6 : 4;
+    static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;  // per stage, on the leader
+    static constexpr int ACC_BUFS = 2;
+    static constexpr int TMEM_COLS = ACC_BUFS * BLOCK_N;            // 512: all of TMEM
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_N = 64;                    // columns per epilogue chunk
+    static constexpr int EPI_CHUNKS = BLOCK_N / EPI_N;
+    static constexpr int EPI_BUFS = 2;
+    static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
+    static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+    // Shared-memory layout (offsets from a 1024-byte aligned base; identical
+    // in both CTAs of a pair, which the pair MMA relies on).
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_D = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_BAR = OFF_D + EPI_WARPS * EPI_BUFS * EPI_BUF;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;  // + drain
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;         // tmem base, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
+    static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;            // alignment slack
+    static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KiB per-block shared memory limit");
+    static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0 && EPI_BUF % 1024 == 0, "1 KiB swizzle atoms");
+};
+
+struct Params {
+    int32_t M, N, K;
+    int32_t num_m_tiles, num_n_tiles, k_tiles, num_tiles;
+    int32_t raster_group;
+    uint32_t debug_flags;
+    uint64_t timeout_ns;
+};
+
+enum : uint32_t { kDebugProducerPhase0 = 1u };
+
+// Instruction descriptor of tcgen05.mma kind::f16 (PTX ISA): D fp32 [4,6)=1,
+// A and B fp16 [7,10)=[10,13)=0, both K-major [15]=[16]=0, N>>3 at [17,23),
+// M>>4 at [24,29).
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void record_failure(uint32_t role, uint32_t seq) {
+    if (atomicCAS(&g_status, 0, kStatusTimeout) == 0) {
+        g_info = (static_cast<unsigned long long>(role) << 56) |
+                 (static_cast<unsigned long long>(blockIdx.x & 0xFFFFFFu) << 32) | seq;
+    }
+}
+
+// Bounded wait by one thread.  Returns false if the wait ran out (the failure
+// is recorded and the CTA's abort flag raised) or if another role of this CTA
+// already aborted.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             uint64_t timeout_ns, uint32_t role, uint32_t seq) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                record_failure(role, seq);
+                return false;
+            }
+        }
+    }
+}
+
+template <int CG>
+__global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
+    gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmD, const Params p) {
+    using C = Cfg<CG>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
+    const int lane = static_cast<int>(threadIdx.x) % 32;
+    const uint32_t rank = CG == 2 ? ptx::cluster_ctarank() : 0u;
+    const bool leader = rank == 0;
+    const int cluster = static_cast<int>(blockIdx.x) / CG;
+    const int num_clusters = static_cast<int>(gridDim.x) / CG;
+
+    const uint32_t sA = base + C::OFF_A;
+    const uint32_t sB = base + C::OFF_B;
+    const uint32_t sD = base + C::OFF_D;
+    const uint32_t bar_full = base + C::OFF_BAR;              // [STAGES]
+    const uint32_t bar_empty = bar_full + 8 * C::STAGES;      // [STAGES]
+    const uint32_t bar_tfull = bar_empty + 8 * C::STAGES;     // [ACC_BUFS]
+    const uint32_t bar_tempty = bar_tfull + 8 * C::ACC_BUFS;  // [ACC_BUFS]
+    const uint32_t bar_drain = bar_tempty + 8 * C::ACC_BUFS;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    // ---- prologue: barriers, TMEM, tensor-map prefetch (once per persistent CTA)
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmD);
+        for (int s = 0; s < C::STAGES; ++s) {
+            ptx::mbar_init(bar_full + 8 * s, 1);
+            ptx::mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int a = 0; a < C::ACC_BUFS; ++a) {
+            ptx::mbar_init(bar_tfull + 8 * a, 1);
+            ptx::mbar_init(bar_tempty + 8 * a, C::EPI_WARPS * CG);
+        }
+        ptx::mbar_init(bar_drain, 1);
+        *abort_flag = 0;
+        ptx::fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc<CG>(ptx::smem_u32(tmem_slot), C::TMEM_COLS);
+        ptx::tmem_relinquish<CG>();
+    }
+    ptx::tcgen05_fence_before();
+    if constexpr (CG == 2) {
+        ptx::cluster_sync();
+    } else {
+        __syncthreads();
+    }
+    ptx::tcgen05_fence_after();
+    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    if (warp == 0) {
+        // ---------------------------------------------------- TMA producer
+        if (ptx::elect_one()) {
+            // The producer end starts one phase ahead of the consumer end
+            // ("GEMM III", "The subtlest bug: opposite initial phases").  The
+            // debug flag starts it at phase 0 instead, which blocks every role;
+            // only the tests of the timeout path set it.
+            PipelineState ring(C::STAGES, (p.debug_flags & kDebugProducerPhase0) ? 0u : 1u);
+            uint32_t seq = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < p.num_tiles; t += num_clusters, ++seq) {
+                const CtaOrigin o =
+                    cta_origin(tile_of(t, p.num_m_tiles, p.num_n_tiles, p.raster_group), CG, static_cast<int32_t>(rank));
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
+                                      kRoleProducer, seq)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t full = bar_full + 8 * ring.stage;
+                    if (leader) ptx::mbar_arrive_expect_tx(full, C::TX_BYTES);
+                    const int32_t k0 = kt * C::BLOCK_K;
+                    if constexpr (CG == 2) {
+                        const uint32_t full_leader = ptx::mapa(full, 0);
+                        ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE, &tmA, full_leader, k0, o.a_row);
+                        ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, &tmB, full_leader, k0, o.b_row);
+                    } else {
+                        ptx::tma_load_2d(sA + ring.stage * C::A_STAGE, &tmA, full, k0, o.a_row);
+                        ptx::tma_load_2d(sB + ring.stage * C::B_STAGE, &tmB, full, k0, o.b_row);
+                    }
+                    ring.advance();
+                }
+            }
+            if (!ok) {
+                // Give loads already in flight time to land before teardown.
+                const uint64_t t0 = ptx::globaltimer_ns();
+                while (ptx::globaltimer_ns() - t0 < 20000) ptx::nanosleep(1000);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (leader && ptx::elect_one()) {
+            constexpr uint32_t idesc = idesc_f16_f32(C::TILE_M, C::BLOCK_N);
+            constexpr uint16_t pair_mask = CG == 2 ? 0x3 : 0x1;
+            PipelineState ring(C::STAGES, 0u);
+            PipelineState acc(C::ACC_BUFS, 1u);
+            uint32_t seq = 0;
+            bool ok = true;
+            for (int t = cluster; ok && t < p.num_tiles; t += num_clusters, ++seq) {
+                if (!wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
+                                  seq)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tcgen05_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * C::BLOCK_N);
+                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                    if (!wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
+                                      seq)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tcgen05_fence_after();
+                    const uint64_t a_desc = ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE);
+                    const uint64_t b_desc = ptx::smem_desc_k_sw128(sB + ring.stage * C::B_STAGE);
+#pragma unroll
+                    for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
+                        // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
+                        const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
+                        ptx::mma_f16<CG>(d_tmem, a_desc + koff, b_desc + koff, idesc, (kt | k) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit<CG>(bar_empty + 8 * ring.stage, pair_mask);  // stage free, both CTAs
+                    ring.advance();
+                }
+                if (!ok) break;
+                ptx::mma_commit<CG>(bar_tfull + 8 * acc.stage, pair_mask);  // accumulator ready, both CTAs
+                acc.advance();
+            }
+            // Wait for every MMA issued so far before TMEM can be released.
+            ptx::mma_commit<CG>(bar_drain, 0x1);
+            wait_bounded(bar_drain, 0, abort_flag, p.timeout_ns, kRoleMma, 0xFFFFFFFFu);
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------- epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 = rows of this warp
+        const uint32_t stage_base = sD + static_cast<uint32_t>(quarter * C::EPI_BUFS * C::EPI_BUF);
+        PipelineState acc(C::ACC_BUFS, 0u);
+        uint32_t buf = 0;
+        uint32_t seq = 0;
+        for (int t = cluster; t < p.num_tiles; t += num_clusters, ++seq) {
+            const CtaOrigin o =
+                cta_origin(tile_of(t, p.num_m_tiles, p.num_n_tiles, p.raster_group), CG, static_cast<int32_t>(rank));
+            const int32_t row0 = o.d_row + quarter * 32;
+            const int32_t col0 = o.d_col;
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_bounded(bar_tfull + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleEpilogue,
+                                  seq);
+            }
+            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!ok) break;
+            ptx::tcgen05_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(acc.stage * C::BLOCK_N);
+#pragma unroll 1
+            for (int c = 0; c < C::EPI_CHUNKS; ++c) {
+                uint32_t lo[32], hi[32];
+                ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N, lo);
+                ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
+                ptx::tmem_wait_ld();
+                if (c == C::EPI_CHUNKS - 1) {
+                    // The whole accumulator of this warp is in registers: hand
+                    // the TMEM buffer back (TIRx notes V7, "Writeback Flow").
+                    ptx::tcgen05_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (CG == 2) {
+                            ptx::mbar_arrive_cluster(ptx::mapa(bar_tempty + 8 * acc.stage, 0));
+                        } else {
+                            ptx::mbar_arrive(bar_tempty + 8 * acc.stage);
+                        }
+                    }
+                }
+                // fp32 -> fp16, round to nearest even, packed two per word.
+                uint32_t h[32];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const __half2 v = __floats2half2_rn(__uint_as_float(lo[2 * j]), __uint_as_float(lo[2 * j + 1]));
+                    h[j] = *reinterpret_cast<const uint32_t *>(&v);
+                }
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const __half2 v = __floats2half2_rn(__uint_as_float(hi[2 * j]), __uint_as_float(hi[2 * j + 1]));
+                    h[16 + j] = *reinterpret_cast<const uint32_t *>(&v);
+                }
+                // The store issued from this buffer two chunks ago must have
+                // finished reading it.
+                if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
+                __syncwarp();
+                // Row `lane` of the 32 x 64 staging tile, in the 128-byte
+                // swizzle the D tensor map expects: 16-byte unit j of row r
+                // sits at unit j ^ (r % 8).
+                const uint32_t row_addr = stage_base + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
+                    ptx::st_shared_v4(row_addr + unit * 16u, h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                }
+                ptx::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    const int32_t col = col0 + c * C::EPI_N;
+                    if (row0 < p.M && col < p.N) {
+                        ptx::tma_store_2d(&tmD, stage_base + buf * C::EPI_BUF, col, row0);
+                    }
+                    ptx::bulk_commit_group();
+                }
+                buf ^= 1u;
+            }
+            acc.advance();
+        }
+        if (lane == 0) ptx::bulk_wait_group<0>();
+        __syncwarp();
+    }
+
+    // ---- teardown: both CTAs done with TMEM and with each other's SMEM
+    ptx::tcgen05_fence_before();
+    if constexpr (CG == 2) {
+        ptx::cluster_sync();
+    } else {
+        __syncthreads();
+    }
+    if (warp == 1) {
+        ptx::tcgen05_fence_after();
+        ptx::tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// D = 0 for an empty contraction (K == 0): every output element is the sum of
+// no products.
+__global__ void zero_fill_kernel(uint4 *D, int64_t n16, uint16_t *tail, int64_t ntail) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n16; i += stride) {
+        D[i] = make_uint4(0, 0, 0, 0);
+    }
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < ntail; i += stride) {
+        tail[i] = 0;
+    }
+}
+
+}  // namespace gemm_f16

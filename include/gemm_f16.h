@@ -1,0 +1,159 @@
+/*
+ * gemm_f16.h -- C ABI of a GB300 (sm_103a) fp16 GEMM:  D = A * B^T
+ *
+ * The operation ("GEMM I -- the tiled baseline", section "The problem we are
+ * solving"; "TIRx GEMM detailed technical notes", V8 "Operand Partition"):
+ *
+ *     A is M x K, B is N x K, D is M x N, all row-major, dense, IEEE binary16.
+ *     D[m][n] = fp16( sum_{k<K} A[m][k] * B[n][k] )
+ *
+ * B is stored N x K on purpose: a row-band of B is a column-band of B^T, so
+ * both operands stream as K-major row-bands.  Products and the running sum are
+ * fp32 on the tensor cores (tcgen05, accumulator in tensor memory); the sum is
+ * rounded to fp16 once, round-to-nearest-even, at writeback (Step 1, "round
+ * once, at the end").
+ *
+ * Conventions shared by every call below:
+ *   - Pointers named A, B, D are DEVICE pointers owned by the caller.  The
+ *     library never frees, keeps or reallocates them and allocates no device
+ *     memory per call.  D must not overlap A or B.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Compute calls are asynchronous: they validate, enqueue one
+ *     kernel on `stream` and return; D is ready when the stream reaches that
+ *     point.
+ *   - Errors are negative gemm_status_t values.  An argument error is reported
+ *     before anything is enqueued and leaves D untouched.  A failure inside a
+ *     running kernel (a bounded wait that ran out) is reported by
+ *     gemm_f16_last_device_status(), never by a hang or a trap.
+ *   - Calls on different streams may run concurrently from several host
+ *     threads.  The device status word is one per device, last writer wins.
+ */
+#ifndef GEMM_F16_H
+#define GEMM_F16_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gemm_status {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad option  */
+    GEMM_ERR_UNSUPPORTED_SHAPE = -2, /* see gemm_f16_nt_supported()             */
+    GEMM_ERR_MISALIGNED = -3,        /* A, B or D not 16-byte aligned           */
+    GEMM_ERR_NO_DEVICE = -4,         /* no CUDA device / driver usable          */
+    GEMM_ERR_ARCH = -5,              /* current device is not sm_103 (GB300)    */
+    GEMM_ERR_LAUNCH = -6,            /* the kernel launch itself failed         */
+    GEMM_ERR_DEVICE_TIMEOUT = -7,    /* a bounded wait inside the kernel ran out */
+    GEMM_ERR_CUDA = -8               /* another CUDA runtime/driver error        */
+} gemm_status_t;
+
+/*
+ * Options for gemm_f16_nt_ex().  Zero-initialise and set what you need; every
+ * zero field means "the default".
+ *   cta_group     2 (default): a 2-CTA cluster issues one cta_group::2 MMA
+ *                 over a 256 x 256 tile per CTA pair ("GEMM III -- warp
+ *                 specialization & clusters to SOTA", Step 8; TIRx notes V8).
+ *                 1: each CTA computes a 128 x 256 tile alone (Step 7 / V7).
+ *   max_clusters  cap on the persistent grid, in clusters (CTA pairs for
+ *                 cta_group 2); 0 = as many as are co-resident on the device.
+ *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes
+ *                 V6 "l2_group_size = 8"); 0 = 8.
+ *   debug_flags   test hook, 0 in normal use.  1 starts the producer end of
+ *                 the SMEM ring at phase 0 instead of 1 -- the pages' "subtlest
+ *                 bug" ("GEMM III", "opposite initial phases") -- so that every
+ *                 wait runs out; it exists to test the timeout path, which
+ *                 must end the kernel with GEMM_ERR_DEVICE_TIMEOUT, not hang.
+ *                 Other bits: GEMM_ERR_INVALID_ARG.
+ *   timeout_ns    limit of every wait inside the kernel; 0 = 4 s.
+ */
+typedef struct gemm_f16_options {
+    int32_t cta_group;
+    int32_t max_clusters;
+    int32_t raster_group;
+    int32_t debug_flags;
+    int64_t timeout_ns;
+} gemm_f16_options;
+
+/*
+ * 1 if gemm_f16_nt() accepts this shape, 0 if not.  Pure host logic, no CUDA
+ * call.  Accepted: M >= 0, N >= 0, K >= 0, N % 8 == 0 and K % 8 == 0 (rows of
+ * B and D are then whole 16-byte units, as the tensor-memory-accelerator copy
+ * engine requires), and M, N, K < 2^31.  M, N and K need not be multiples of
+ * the tile: edge tiles read zeros past the ends of A and B and write only the
+ * in-range part of D.  M == 0 or N == 0 is an empty product (nothing is
+ * launched); K == 0 writes D = 0.
+ */
+int gemm_f16_nt_supported(int64_t M, int64_t N, int64_t K);
+
+/*
+ * D = A * B^T (see the top of this file) with the default options.
+ * Returns GEMM_OK once the kernel is enqueued on `stream`; GEMM_ERR_INVALID_ARG
+ * for a null A/B/D with a non-empty product or negative sizes;
+ * GEMM_ERR_UNSUPPORTED_SHAPE; GEMM_ERR_MISALIGNED; GEMM_ERR_NO_DEVICE;
+ * GEMM_ERR_ARCH; GEMM_ERR_LAUNCH.
+ */
+int gemm_f16_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream);
+
+/* As gemm_f16_nt(), with options (NULL = defaults); GEMM_ERR_INVALID_ARG for
+ * an option out of range. */
+int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
+                   const gemm_f16_options *opts);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's status
+ * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a wait inside a kernel ran out
+ * (the kernel then skipped its remaining work and exited; D is incomplete).
+ * If `info` is not NULL it receives where the first failure happened:
+ * bits 56-63 role (1 producer, 2 MMA issuer, 3 epilogue), 32-55 CTA index,
+ * 0-31 the tile's sequence number in that CTA.  Returns GEMM_ERR_CUDA if the
+ * synchronisation itself reports an error.
+ */
+int gemm_f16_last_device_status(void *stream, uint64_t *info);
+
+/* A static, human-readable name for a gemm_status_t value. */
+const char *gemm_f16_status_string(int status);
+
+/*
+ * The persistent tile scheduler, as a pure host query (no CUDA call).  The
+ * output is cut into tiles of (128 * cta_group) rows x 256 columns; cluster
+ * `cluster_id` of `num_clusters` takes tiles cluster_id, cluster_id +
+ * num_clusters, ... in a grouped order: groups of `raster_group` M-tiles, M
+ * fastest inside a group, then N, then the next group (TIRx notes V6, "Better
+ * L2 Locality").  Returns 1 and the tile's (m_idx, n_idx) if that cluster has
+ * an iter-th tile, 0 if it has not, GEMM_ERR_INVALID_ARG for bad arguments.
+ */
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster_group, int64_t num_clusters,
+                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx);
+
+/*
+ * Where CTA `rank` of tile (m_idx, n_idx) reads and writes, as a pure host
+ * query (no CUDA call); the kernel uses the same function.  TIRx notes V8,
+ * "Operand Partition" and "Output Ownership": with m_base = m_idx * 128 *
+ * cta_group and n_base = n_idx * 256, the CTA loads A rows a_row = m_base +
+ * 128 * rank (128 rows) and B rows b_row = n_base + (256 / cta_group) * rank
+ * (256 / cta_group rows), and writes D rows d_row = a_row (128 rows) over the
+ * 256 columns starting at d_col = n_base ("Epilogue Column Address": no rank
+ * term).  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not 0/1/2, rank
+ * out of range, negative or too large indices, null outputs).
+ */
+int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int32_t rank, int64_t *a_row,
+                           int64_t *b_row, int64_t *d_row, int64_t *d_col);
+
+/*
+ * The stage/phase bookkeeping of one SMEM or TMEM ring, run on the host with
+ * the same code the kernel runs ("GEMM III", "Four barriers = two
+ * producer-consumer rings": PipelineState(depth, phase) with .stage, .phase
+ * and .advance(); TIRx notes V5 "Barrier Phase Tracking").  Writes the
+ * (stage, phase) seen before each of `steps` advances.  Returns GEMM_OK, or
+ * GEMM_ERR_INVALID_ARG (depth outside 1..16, phase not 0/1, null outputs).
+ */
+int gemm_f16_pipeline_trace(int32_t depth, int32_t initial_phase, int32_t steps, int32_t *stage_out,
+                            int32_t *phase_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_F16_H */

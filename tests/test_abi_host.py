@@ -1,0 +1,199 @@
+"""Host-side tests of the C ABI (no GPU needed, no compute call is made).
+
+* the library builds for sm_103a, loads, and exports every entry point that
+  include/gemm_f16.h declares;
+* argument validation returns its codes before any CUDA work;
+* the scheduler, the per-CTA origin and the ring bookkeeping — the same code
+  the kernel runs — against the pages' worked examples (tests/golden) and
+  against exhaustive properties (bijection, ownership).
+"""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import blackwell_tensor_core_02_gb300 as g
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, NO_DEVICE = 0, -1, -2, -3, -4
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return rows
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "gemm_f16.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_f16_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    lib = g.load()
+    names = declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), f"{name} declared in include/gemm_f16.h but not exported"
+
+
+def test_supported_shapes():
+    ok = [(128, 128, 64), (4096, 4096, 4096), (8192, 28672, 4096), (1, 8, 8), (0, 8, 8), (5, 0, 0),
+          (129, 264, 520), (2 ** 31 - 1, 8, 8)]
+    bad = [(128, 12, 64), (128, 128, 60), (-1, 8, 8), (8, 8, -8), (2 ** 31, 8, 8), (8, 2 ** 31, 8)]
+    for s in ok:
+        assert g.gemm_f16_nt_supported(*s), s
+    for s in bad:
+        assert not g.gemm_f16_nt_supported(*s), s
+
+
+def test_argument_errors_are_returned_before_any_launch():
+    lib = g.load()
+    a, b, d = 0x10000, 0x20000, 0x30000  # never dereferenced: every case fails validation first
+    assert lib.gemm_f16_nt(a, b, d, -1, 8, 8, None) == INVALID
+    assert lib.gemm_f16_nt(a, b, d, 128, 12, 64, None) == UNSUPPORTED
+    assert lib.gemm_f16_nt(a, b, d, 128, 128, 60, None) == UNSUPPORTED
+    assert lib.gemm_f16_nt(None, b, d, 128, 128, 64, None) == INVALID
+    assert lib.gemm_f16_nt(a, None, d, 128, 128, 64, None) == INVALID
+    assert lib.gemm_f16_nt(a, b, None, 128, 128, 64, None) == INVALID
+    assert lib.gemm_f16_nt(a + 2, b, d, 128, 128, 64, None) == MISALIGNED
+    assert lib.gemm_f16_nt(a, b + 8, d, 128, 128, 64, None) == MISALIGNED
+    assert lib.gemm_f16_nt(a, b, d + 4, 128, 128, 64, None) == MISALIGNED
+    # empty products are accepted and launch nothing, even with null operands
+    assert lib.gemm_f16_nt(None, None, None, 0, 128, 64, None) == OK
+    assert lib.gemm_f16_nt(None, None, None, 128, 0, 64, None) == OK
+    for bad in (g.Options(cta_group=3), g.Options(max_clusters=-1), g.Options(raster_group=-2),
+                g.Options(debug_flags=2), g.Options(timeout_ns=-5)):
+        assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
+
+
+def test_no_device_reported_without_gpu():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful on a machine without a GPU (the pointers here are fake)")
+    lib = g.load()
+    assert lib.gemm_f16_nt(0x10000, 0x20000, 0x30000, 128, 128, 64, None) == NO_DEVICE
+
+
+def test_status_strings():
+    for code, name in g.STATUS.items():
+        assert g.status_string(code).startswith(name)
+    assert "unknown" in g.status_string(12345)
+
+
+@pytest.mark.parametrize("M,N,cg,group,clusters", [
+    (4096, 4096, 2, 8, 74), (4096, 4096, 2, 8, 76), (8192, 28672, 2, 8, 76), (4096, 4096, 1, 8, 148),
+    (300, 520, 2, 8, 3), (1, 8, 1, 1, 1), (2560, 1280, 2, 3, 7), (1000, 7000, 1, 5, 13), (128, 128, 2, 8, 1),
+])
+def test_schedule_is_a_bijection(M, N, cg, group, clusters):
+    num_m = -(-M // (128 * cg))
+    num_n = -(-N // 256)
+    seen = {}
+    for c in range(clusters):
+        it = 0
+        while True:
+            t = g.schedule(M, N, cg, group, clusters, c, it)
+            if t is None:
+                break
+            assert 0 <= t[0] < num_m and 0 <= t[1] < num_n
+            assert t not in seen, f"tile {t} assigned twice"
+            seen[t] = (c, it)
+            it += 1
+        # cluster c has exactly the tiles c, c + P, c + 2P, ...
+        assert it == len(range(c, num_m * num_n, clusters))
+    assert len(seen) == num_m * num_n
+
+
+def test_schedule_grouped_order():
+    # 16 x 16 tiles, groups of 8 M-tiles: M fastest inside a group, then N.
+    order = [g.schedule(4096, 4096, 2, 8, 1, 0, i) for i in range(256)]
+    assert order[:9] == [(m, 0) for m in range(8)] + [(0, 1)]
+    assert order[127] == (7, 15) and order[128] == (8, 0) and order[255] == (15, 15)
+
+
+def test_cta_origin_matches_the_pages_operand_partition():
+    for m_idx, n_idx, cbx, a_row, b_row, d_row, d_col in _golden_rows("v8_operand_partition.txt"):
+        got = g.cta_origin(2, m_idx, n_idx, cbx)
+        assert got == dict(a_row=a_row, b_row=b_row, d_row=d_row, d_col=d_col)
+
+
+def test_cta_origin_ownership_covers_each_output_once():
+    # Over all tiles and both CTAs, the written 128-row x 256-column blocks tile D exactly once.
+    for cg in (1, 2):
+        M, N = 1024, 768
+        cover = np.zeros((M // 128, N // 256), dtype=int)
+        for m_idx in range(M // (128 * cg)):
+            for n_idx in range(N // 256):
+                for r in range(cg):
+                    o = g.cta_origin(cg, m_idx, n_idx, r)
+                    assert o["d_row"] == o["a_row"] and o["d_col"] == n_idx * 256
+                    cover[o["d_row"] // 128, o["d_col"] // 256] += 1
+                    # the B slice loaded by this CTA lies inside the tile's 256 output columns
+                    assert n_idx * 256 <= o["b_row"] < (n_idx + 1) * 256
+        assert np.all(cover == 1)
+    with pytest.raises(g.GemmError):
+        g.cta_origin(2, 0, 0, 2)
+
+
+def test_pipeline_state_matches_the_pages_table():
+    want = [(s, p) for _, s, p in _golden_rows("v5_stage_phase_depth2.txt")]
+    assert g.pipeline_trace(2, 0, 4) == want
+    # the producer end runs the same sequence one phase apart
+    assert g.pipeline_trace(2, 1, 4) == [(s, 1 - p) for s, p in want]
+    # deeper rings: the phase flips exactly when the stage wraps
+    tr = g.pipeline_trace(6, 0, 20)
+    for i, (s, p) in enumerate(tr):
+        assert s == i % 6 and p == (i // 6) % 2
+    with pytest.raises(g.GemmError):
+        g.pipeline_trace(0, 0, 1)
+
+
+def _simulate_ring(depth, producer_phase, steps, seed):
+    """Model one SMEM ring with parity barriers, driven by the library's PipelineState traces.
+
+    try_wait(bar, p) passes when the barrier's phase bit differs from p
+    ("GEMM I", the phase-flip table).  A fill completes full[s]'s phase; a
+    consume completes empty[s]'s phase.  Returns the consumed sequence, or None
+    on deadlock.
+    """
+    prod = g.pipeline_trace(depth, producer_phase, steps)
+    cons = g.pipeline_trace(depth, 0, steps)
+    full, empty = [0] * depth, [0] * depth
+    slot = [None] * depth
+    i = j = 0
+    out = []
+    rng = random.Random(seed)
+    while j < steps:
+        can_p = i < steps and empty[prod[i][0]] != prod[i][1]
+        can_c = full[cons[j][0]] != cons[j][1]
+        if not (can_p or can_c):
+            return None
+        if can_p and (not can_c or rng.random() < 0.5):
+            s = prod[i][0]
+            slot[s] = i
+            full[s] ^= 1
+            i += 1
+        else:
+            s = cons[j][0]
+            out.append(slot[s])
+            empty[s] ^= 1
+            j += 1
+    return out
+
+
+def test_opposite_initial_phases_model():
+    for depth in (1, 2, 4, 6):
+        for seed in range(20):
+            assert _simulate_ring(depth, 1, 50, seed) == list(range(50))
+    # the pages' "subtlest bug": both ends at phase 0 deadlock on the fresh barrier
+    assert _simulate_ring(4, 0, 50, 0) is None

@@ -1,0 +1,185 @@
+"""GPU parity: the sm_103a kernel, called through the C ABI, against the CPU oracle.
+
+Bar (per element, floating point): |gpu − oracle| ≤ 2⁻⁹·|oracle| + 1e-3, with
+the oracle the fp64 sum rounded once to fp16.  Cases with one product per
+output (identity operands) must match bit for bit.
+
+Small and medium shapes are compared in full; the three large workloads
+(4096³, 8192³, 8192×28672×4096) are compared, in the launch configuration the
+benchmark times, on whole sampled rows and columns (tile borders included)
+plus random points, all computed one by one by the oracle.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 2.0 ** -9
+ATOL = 1e-3
+SENTINEL = 0x7E00  # an fp16 NaN no finite result can equal
+
+
+def to_dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def run(g, A, B, options=None):
+    D = g.gemm_f16_nt(to_dev(A), to_dev(B), options=options)
+    status, info = g.last_device_status()
+    assert status == 0, f"device status {g.status_string(status)} info={info:#x}"
+    return D.cpu().numpy()
+
+
+def assert_close(gpu_f16, ref_bits, what=""):
+    got = np.asarray(gpu_f16, dtype=np.float16).astype(np.float64)
+    ref = np.asarray(ref_bits).view(np.float16).astype(np.float64)
+    assert got.shape == ref.shape
+    err = np.abs(got - ref)
+    ok = err <= RTOL * np.abs(ref) + ATOL
+    if not ok.all():
+        bad = np.argwhere(~ok)
+        i = tuple(bad[0])
+        raise AssertionError(f"{what}: {len(bad)} of {ok.size} outside tolerance; first at {i}: "
+                             f"gpu={got[i]!r} oracle={ref[i]!r}")
+
+
+def opts(g, cta_group=0, max_clusters=0):
+    return g.Options(cta_group=cta_group, max_clusters=max_clusters)
+
+
+# ----------------------------------------------------------- full compares --
+
+@pytest.mark.parametrize("cg", [2, 1])
+@pytest.mark.parametrize("name", ["single_tile_128x128x64", "ktile_grid_256x256x512"])
+def test_small_workloads_full(gpu_lib, name, cg):
+    w = si.WORKLOADS[name]
+    A, B = w.operands()
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg)), oracle.gemm_f16_nt(A, B), f"{name} cg={cg}")
+
+
+@pytest.mark.parametrize("cg", [2, 1])
+def test_identity_operands_are_exact(gpu_lib, cg):
+    # One product per output element: the result is exact, so bit equality.
+    # A = I (M = K = 384, 1.5 cluster tiles) gives D = Bᵀ; B = I gives D = A.
+    rng = np.random.default_rng(21)
+    K = 384
+    B = rng.uniform(-2, 2, size=(520, K)).astype(np.float16)
+    D = run(gpu_lib, np.eye(K, dtype=np.float16), B, opts(gpu_lib, cg))
+    assert np.array_equal(D.view(np.uint16), np.ascontiguousarray(B.T).view(np.uint16))
+    A = rng.uniform(-2, 2, size=(200, K)).astype(np.float16)
+    D = run(gpu_lib, A, np.eye(K, dtype=np.float16), opts(gpu_lib, cg))
+    assert np.array_equal(D.view(np.uint16), A.view(np.uint16))
+
+
+RAGGED = [(1, 8, 8), (200, 136, 72), (129, 264, 520), (383, 1032, 1000), (1000, 8, 64), (640, 776, 8)]
+
+
+@pytest.mark.parametrize("cg", [2, 1])
+@pytest.mark.parametrize("M,N,K", RAGGED)
+def test_ragged_shapes_full(gpu_lib, M, N, K, cg):
+    w = si.custom(M, N, K, seed=M * 7 + N * 3 + K)
+    A, B = w.operands()
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg)), oracle.gemm_f16_nt(A, B), f"{M}x{N}x{K} cg={cg}")
+
+
+@pytest.mark.parametrize("cg,clusters", [(2, 1), (2, 3), (1, 1), (1, 5)])
+def test_few_persistent_clusters_run_many_tiles(gpu_lib, cg, clusters):
+    # 1024 x 1024 x 320: 16 (cg 2) or 32 (cg 1) tiles, so each persistent CTA
+    # runs several tiles and both rings wrap many times across tiles.
+    w = si.custom(1024, 1024, 320, seed=77)
+    A, B = w.operands()
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg, clusters)), oracle.gemm_f16_nt(A, B),
+                 f"cg={cg} clusters={clusters}")
+
+
+def test_guard_bands_and_full_overwrite(gpu_lib):
+    # D sits inside a larger buffer filled with a NaN sentinel: every element of
+    # D must be written, and nothing before or after it.
+    M, N, K = 300, 520, 200
+    w = si.custom(M, N, K, seed=5)
+    A, B = w.operands()
+    guard = 32768
+    buf = torch.full((guard + M * N + guard,), SENTINEL, dtype=torch.int16, device="cuda").view(torch.float16)
+    D = buf[guard:guard + M * N].view(M, N)
+    gpu_lib.gemm_f16_nt(to_dev(A), to_dev(B), D)
+    status, _ = gpu_lib.last_device_status()
+    assert status == 0
+    host = buf.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.all(host[:guard] == SENTINEL) and np.all(host[guard + M * N:] == SENTINEL)
+    assert not np.any(host[guard:guard + M * N] == SENTINEL)
+    assert_close(host[guard:guard + M * N].view(np.float16).reshape(M, N), oracle.gemm_f16_nt(A, B), "guarded")
+
+
+def test_degenerate_shapes(gpu_lib):
+    # K = 0: every output is the empty sum, +0.
+    D = torch.full((130, 264), 7.0, dtype=torch.float16, device="cuda")
+    A = torch.empty((130, 0), dtype=torch.float16, device="cuda")
+    B = torch.empty((264, 0), dtype=torch.float16, device="cuda")
+    gpu_lib.gemm_f16_nt(A, B, D)
+    assert gpu_lib.last_device_status()[0] == 0
+    assert torch.count_nonzero(D).item() == 0
+    # M = 0 or N = 0: nothing to compute, nothing launched.
+    E = gpu_lib.gemm_f16_nt(torch.empty((0, 64), dtype=torch.float16, device="cuda"),
+                            torch.ones((8, 64), dtype=torch.float16, device="cuda"))
+    assert tuple(E.shape) == (0, 8)
+
+
+def test_argument_errors_on_device(gpu_lib):
+    A = torch.ones((128, 64), dtype=torch.float16, device="cuda")
+    B = torch.ones((128, 64), dtype=torch.float16, device="cuda")
+    D = torch.zeros((128 * 128 + 8,), dtype=torch.float16, device="cuda")
+    rc = gpu_lib.gemm_f16_nt_ptr(A.data_ptr(), B.data_ptr(), D.data_ptr() + 2, 128, 128, 64,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == -3
+    rc = gpu_lib.gemm_f16_nt_ptr(A.data_ptr(), B.data_ptr(), D.data_ptr(), 128, 12, 64,
+                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == -2
+    assert torch.count_nonzero(D).item() == 0
+
+
+def test_repeated_calls_and_streams(gpu_lib):
+    w = si.WORKLOADS["ktile_grid_256x256x512"]
+    A, B = w.operands()
+    ref = oracle.gemm_f16_nt(A, B)
+    dA, dB = to_dev(A), to_dev(B)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(5):
+            outs.append(gpu_lib.gemm_f16_nt(dA, dB, stream=s))
+    s.synchronize()
+    assert gpu_lib.last_device_status(s)[0] == 0
+    for o in outs:
+        assert_close(o.cpu().numpy(), ref, "repeat")
+
+
+# ------------------------------------------------ full-size, sampled compares --
+
+def _sample_indices(n, tile, count, rng):
+    """Tile-border indices (every 4th border, both sides), the two ends, and `count` random ones."""
+    idx = {0, n - 1}
+    for b in range(tile, n, tile * 4):
+        idx.update({b - 1, b})
+    idx.update(rng.choice(n, size=min(n, count), replace=False).tolist())
+    return np.array(sorted(idx))
+
+
+@pytest.mark.parametrize("name", ["square_4096", "square_8192", "mlp_proj_8192x28672x4096"])
+def test_full_size_workloads_sampled(gpu_lib, name):
+    w = si.WORKLOADS[name]
+    A, B = w.operands()
+    D = run(gpu_lib, A, B)  # default options: the launch configuration the benchmark times
+    rng = np.random.default_rng(w.seed + 100)
+    rows = _sample_indices(w.M, 128, 40, rng)
+    cols = _sample_indices(w.N, 256, 40, rng)
+    assert_close(D[rows, :], oracle.gemm_f16_nt(A[rows], B), f"{name} rows")
+    assert_close(D[:, cols], oracle.gemm_f16_nt(A, B[cols]), f"{name} cols")
+    pr = rng.integers(0, w.M, size=20000)
+    pc = rng.integers(0, w.N, size=20000)
+    assert_close(D[pr, pc], oracle.gemm_f16_nt_points(A, B, pr, pc), f"{name} points")
+    assert np.isfinite(D.astype(np.float32)).all()
