@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Benchmark of the sm_103a fp16 GEMM D = A·Bᵀ on the 4096³ headline workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one GEMM over one input set (the whole hot path: one kernel launch).
+Prints ONE JSON line (rank 0).  For N > 1 run under torchrun: every rank runs
+its own replica on its own GPU (the GEMM has no exchange step), so the scaling
+is weak and the value is the total over ranks.
+
+Timing: W untimed warm-up steps, then K steps between a barrier +
+synchronize on both sides, measured with CUDA events on the stream the kernel
+is launched on.  Inputs and outputs rotate over 4 device copies (384 MiB, above
+the 129 MB L2), so every step reads A and B from HBM.  nvidia-smi clocks and
+throttle reasons are sampled while the timed region runs.
+
+``--impl reference`` times the CPU oracle (plain C, fp64 accumulation) as it
+stands on this machine's host cores, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "GEMM TFLOP/s at M=N=K=4096 fp16→fp32 acc; % of GB300 dense fp16 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = si.HEADLINE
+ROTATE = 4
+NOMINAL_PEAK_TFLOPS = 2250.0          # GB300 dense fp16/bf16 tensor, nominal
+FALLBACK_PEAK_TFLOPS = 1900.0         # one earlier cuBLAS bf16 measurement on a GB300
+KERNEL_NAME = "gemm_f16_nt_kernel<2>"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_gemm_f16_nt_kernel_square_4096.json")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources: the ncu traffic figure is only valid for the kernel it was taken on."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "blackwell_tensor_core_02_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)) or None, \
+            "measured: MEASURED_PEAKS.json bf16_tflops (cuBLAS bf16 burst); fp16 runs at the bf16 rate"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_PEAK_TFLOPS, None, "fallback: 1.9 PFLOP/s bf16 burst from an earlier GB300 measurement"
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, or None if absent or stale."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None, "no ncu summary committed"
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None, "kernel changed since the ncu capture"
+    return int(d["dram_bytes_per_launch"]), d.get("command", "")
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (time-stamped on arrival) while the benchmark runs."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.samples: list[tuple[float, list[str]]] = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.strip().split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [p for t, p in self.samples if t0 <= t <= t1]
+        note = "samples inside the timed region"
+        if not inside:
+            after = [p for t, p in self.samples if t >= t0][:1]
+            inside, note = after, "timed region shorter than the sampling interval: first sample after its start"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[4 + i].lower().startswith("active")})
+        power = [num(p[2]) for p in inside if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][1]),
+                "reasons": reasons, "power_w_max": max(power) if power else None, "samples": len(inside),
+                "note": note}
+
+
+# ------------------------------------------------------------- CPU oracle --
+
+def oracle_rows_tflops(A, B, rows: int, threads: int):
+    """The oracle as it stands on `rows` full rows of D; returns (TFLOP/s, seconds)."""
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt(A[:rows], B, threads=threads)
+    dt = time.perf_counter() - t0
+    return 2.0 * rows * B.shape[0] * A.shape[1] / dt / 1e12, dt
+
+
+def cpu_baseline(A, B, target_s: float = 12.0) -> dict:
+    threads = os.cpu_count() or 1
+    _, dt1 = oracle_rows_tflops(A, B, 4, threads)  # calibration (also builds the oracle)
+    rows = int(max(4, min(A.shape[0], 4 * target_s / max(dt1, 1e-6))))
+    rows = max(threads, (rows // threads) * threads) if rows >= threads else rows
+    rows = min(rows, A.shape[0])
+    v, dt = oracle_rows_tflops(A, B, rows, threads)
+    return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of D for {WORKLOAD} ({rows}x{B.shape[0]} outputs, K={A.shape[1]}), "
+                      f"{dt:.1f} s on {threads} host threads"}
+
+
+def run_reference(args) -> None:
+    """--impl reference: the oracle timed on the host cores, each step a bounded sample."""
+    import oracle
+
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = si.WORKLOADS[WORKLOAD]
+    A, B = w.operands()
+    threads = os.cpu_count() or 1
+    oracle.build()
+    # size each step so that warm-up + timed steps take about a minute in total
+    rng = np.random.default_rng(0)
+    calib = 2048
+    t0 = time.perf_counter()
+    oracle.gemm_f16_nt_points(A, B, rng.integers(0, w.M, calib), rng.integers(0, w.N, calib), threads=threads)
+    per_point = (time.perf_counter() - t0) / calib
+    budget = 60.0 / max(1, args.steps + args.warmup)
+    points = int(min(1 << 20, max(threads, budget / per_point)))
+    samples = [(rng.integers(0, w.M, points), rng.integers(0, w.N, points)) for _ in range(2)]
+    for i in range(args.warmup):
+        oracle.gemm_f16_nt_points(A, B, *samples[i % 2], threads=threads)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        oracle.gemm_f16_nt_points(A, B, *samples[i % 2], threads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * points * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = f"{points} random output points of {WORKLOAD} per step (K={w.K} each), oracle on {threads} host threads"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm --
+
+def run_ours(args) -> None:
+    import torch
+
+    import blackwell_tensor_core_02_gb300 as g
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    g.load()
+    w = si.WORKLOADS[WORKLOAD]
+    A, B = w.operands()
+    flop = float(w.flop)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+    As, Bs, Ds = [], [], []
+    with torch.cuda.stream(stream):
+        a0 = torch.from_numpy(A).to(dev)
+        b0 = torch.from_numpy(B).to(dev)
+        for _ in range(ROTATE):
+            As.append(a0.clone())
+            Bs.append(b0.clone())
+            Ds.append(torch.empty((w.M, w.N), dtype=torch.float16, device=dev))
+        del a0, b0
+    stream.synchronize()
+
+    def step(i):
+        j = i % ROTATE
+        rc = g.gemm_f16_nt_ptr(As[j].data_ptr(), Bs[j].data_ptr(), Ds[j].data_ptr(), w.M, w.N, w.K, sh)
+        if rc != 0:
+            raise g.GemmError(rc, "gemm_f16_nt")
+
+    # correctness guard on the timed configuration: a few sampled outputs vs the oracle
+    step(0)
+    status, info = g.last_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {g.status_string(status)} info={info:#x}")
+    if rank == 0:
+        import oracle
+
+        rng = np.random.default_rng(1)
+        pr, pc = rng.integers(0, w.M, 512), rng.integers(0, w.N, 512)
+        ref = oracle.gemm_f16_nt_points(A, B, pr, pc).view(np.float16).astype(np.float64)
+        got = Ds[0].cpu().numpy()[pr, pc].astype(np.float64)
+        if not np.all(np.abs(got - ref) <= 2.0 ** -9 * np.abs(ref) + 1e-3):
+            raise RuntimeError("bench correctness guard failed against the oracle")
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    for i in range(args.warmup):
+        step(i)
+    barrier()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    ev1.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    status, info = g.last_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {g.status_string(status)} info={info:#x}")
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    if sampler:
+        sampler.stop()
+
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flop * args.steps / (elapsed_ms * 1e-3) / 1e12
+    per_gpu_tflops = flop / (ms_per_step * 1e-3) / 1e12
+
+    # cuBLAS (torch.matmul) on the same rotation, as a reference point
+    cublas = None
+    if not args.no_cublas:
+        torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup):
+                torch.matmul(As[i % ROTATE], Bs[i % ROTATE].t(), out=Ds[i % ROTATE])
+            c0 = torch.cuda.Event(enable_timing=True)
+            c1 = torch.cuda.Event(enable_timing=True)
+            c0.record(stream)
+            for i in range(args.steps):
+                torch.matmul(As[i % ROTATE], Bs[i % ROTATE].t(), out=Ds[i % ROTATE])
+            c1.record(stream)
+        c1.synchronize()
+        cms = c0.elapsed_time(c1) / args.steps
+        cublas = {"value": flop / (cms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": cms,
+                  "what": "torch.matmul(A, B.T) (cuBLAS), fp16 reduced-precision reduction off, same rotation"}
+
+    # end to end through the public API with host buffers: H2D of A and B from
+    # pinned memory, the GEMM, D2H of D, every step
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    Ah = torch.from_numpy(A).pin_memory()
+    Bh = torch.from_numpy(B).pin_memory()
+    Dh = torch.empty((w.M, w.N), dtype=torch.float16).pin_memory()
+    for i in range(min(3, args.warmup) or 1):
+        g.gemm_f16_nt_host(Ah, Bh, Dh, device=dev, stream=stream, A_dev=As[0], B_dev=Bs[0], D_dev=Ds[0])
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        j = i % ROTATE
+        g.gemm_f16_nt_host(Ah, Bh, Dh, device=dev, stream=stream, A_dev=As[j], B_dev=Bs[j], D_dev=Ds[j])
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * flop * e2e_steps / (e2e_ms * 1e-3) / 1e12
+
+    if rank == 0:
+        peak, peak_sustained, peak_src = measured_peak()
+        traffic, traffic_src = ncu_traffic()
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
+                       "inputs": "fp16 uniform[-1,1], splitmix64 seed 2; fp32 accumulation, fp16 output",
+                       "l2": f"inputs larger than L2: A, B, D rotate over {ROTATE} device copies "
+                             f"({ROTATE * w.min_bytes / 2 ** 20:.0f} MiB)",
+                       "cta_group": 2, "tile": "256x256 per CTA pair", "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "tensor", "achieved": per_gpu_tflops, "peak": peak, "unit": UNIT,
+                         "frac": per_gpu_tflops / peak, "traffic": traffic, "kernel": KERNEL_NAME,
+                         "peak_source": peak_src,
+                         "frac_of_sustained": (per_gpu_tflops / peak_sustained) if peak_sustained else None,
+                         "frac_of_nominal_2250": per_gpu_tflops / NOMINAL_PEAK_TFLOPS,
+                         "traffic_source": traffic_src,
+                         "algorithmic_flop_per_launch": flop,
+                         "algorithmic_bytes_per_launch": w.min_bytes},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * (w.M * w.K + w.N * w.K),
+                    "d2h_bytes_per_step": 2 * w.M * w.N, "steps": e2e_steps,
+                    "what": "gemm_f16_nt_host: pinned host A, B -> device, GEMM, D -> pinned host, per step"},
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+            "cublas_reference": cublas,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(A, B)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cublas", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

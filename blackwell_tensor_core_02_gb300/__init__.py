@@ -65,9 +65,9 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_last_device_status.restype = ctypes.c_int
         lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
         lib.gemm_f16_status_string.restype = ctypes.c_char_p
-        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i32, i32, i64, i64, i64, i64p, i64p]
+        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i32, i32, i64, i64, i64, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_schedule.restype = ctypes.c_int
-        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i64, i64, i32, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
         lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
         lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
@@ -161,19 +161,20 @@ def last_device_status(stream=None) -> tuple[int, int]:
 
 def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
              it: int):
-    """The scheduler's iter-th tile (m_idx, n_idx) of one cluster, or None when it has no more."""
-    m, n = ctypes.c_int64(), ctypes.c_int64()
+    """The iter-th work item (m_idx, n_idx, n_off, n_len) of one cluster, or None when it has no more."""
+    out = [ctypes.c_int64() for _ in range(4)]
     rc = load().gemm_f16_nt_schedule(M, N, cta_group, raster_group, num_clusters, cluster_id, it,
-                                     ctypes.byref(m), ctypes.byref(n))
+                                     *[ctypes.byref(o) for o in out])
     if rc < 0:
         raise GemmError(rc, "gemm_f16_nt_schedule")
-    return (m.value, n.value) if rc == 1 else None
+    return tuple(o.value for o in out) if rc == 1 else None
 
 
-def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int) -> dict:
-    """Rows/columns CTA `rank` of tile (m_idx, n_idx) loads and writes (see the C header)."""
+def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int, n_off: int = 0, n_len: int = 256) -> dict:
+    """Rows/columns CTA `rank` of a work item loads and writes (see the C header)."""
     out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_cta_origin(cta_group, m_idx, n_idx, rank, *[ctypes.byref(o) for o in out])
+    rc = load().gemm_f16_nt_cta_origin(cta_group, m_idx, n_idx, n_off, n_len, rank,
+                                       *[ctypes.byref(o) for o in out])
     if rc != 0:
         raise GemmError(rc, "gemm_f16_nt_cta_origin")
     return dict(zip(("a_row", "b_row", "d_row", "d_col"), (o.value for o in out)))

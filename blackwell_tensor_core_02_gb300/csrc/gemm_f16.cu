@@ -126,9 +126,9 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
            const DeviceInfo &dev, int32_t max_clusters, int32_t raster_group, int64_t timeout_ns,
            uint32_t debug_flags) {
     using C = Cfg<CG>;
-    CUtensorMap tmA, tmB, tmD;
+    CUtensorMap tmA, tmB, tmBh, tmD;
     if (encode_map(&tmA, A, M, K, C::BLOCK_M) != GEMM_OK || encode_map(&tmB, B, N, K, C::B_ROWS) != GEMM_OK ||
-        encode_map(&tmD, D, M, N, 32) != GEMM_OK) {
+        encode_map(&tmBh, B, N, K, C::B_ROWS / 2) != GEMM_OK || encode_map(&tmD, D, M, N, 32) != GEMM_OK) {
         return GEMM_ERR_CUDA;
     }
     Params p;
@@ -146,10 +146,12 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     p.timeout_ns = static_cast<uint64_t>(timeout_ns);
     int64_t clusters = dev.max_clusters[CG];
     if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
-    if (clusters > tiles) clusters = tiles;
+    p.split_from = split_point(p.num_tiles, static_cast<int32_t>(clusters));
+    p.num_items = p.num_tiles + (p.num_tiles - p.split_from);
+    if (clusters > p.num_items) clusters = p.num_items;
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = launch_config<CG>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG>, tmA, tmB, tmD, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG>, tmA, tmB, tmBh, tmD, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -262,38 +264,46 @@ const char *gemm_f16_status_string(int status) {
 }
 
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster_group, int64_t num_clusters,
-                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx) {
+                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx, int64_t *n_off,
+                         int64_t *n_len) {
     if (cta_group == 0) cta_group = 2;
     if (raster_group == 0) raster_group = kDefaultRasterGroup;
     if ((cta_group != 1 && cta_group != 2) || raster_group < 0 || M <= 0 || N <= 0 || M > kDimLimit ||
-        N > kDimLimit || num_clusters <= 0 || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !m_idx ||
-        !n_idx) {
+        N > kDimLimit || num_clusters <= 0 || num_clusters > kDimLimit || cluster_id < 0 ||
+        cluster_id >= num_clusters || iter < 0 || !m_idx || !n_idx || !n_off || !n_len) {
         return GEMM_ERR_INVALID_ARG;
     }
     const int64_t tile_m = 128 * cta_group, tile_n = 256;
     const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
     const int64_t tiles = num_m * num_n;
-    if (tiles > kDimLimit) return GEMM_ERR_INVALID_ARG;
-    const int64_t t = cluster_id + iter * num_clusters;
-    if (t >= tiles) return 0;
-    const TileCoord c = tile_of(static_cast<int32_t>(t), static_cast<int32_t>(num_m), static_cast<int32_t>(num_n),
-                                raster_group);
-    *m_idx = c.m_idx;
-    *n_idx = c.n_idx;
+    if (tiles > kDimLimit / 2) return GEMM_ERR_INVALID_ARG;
+    const int32_t split_from = split_point(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters));
+    const int64_t items = tiles + (tiles - split_from);
+    const int64_t item = cluster_id + iter * num_clusters;
+    if (item >= items) return 0;
+    const WorkItem w = work_of(static_cast<int32_t>(item), static_cast<int32_t>(num_m),
+                               static_cast<int32_t>(num_n), raster_group, split_from);
+    *m_idx = w.m_idx;
+    *n_idx = w.n_idx;
+    *n_off = w.n_off;
+    *n_len = w.n_len;
     return 1;
 }
 
-int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int32_t rank, int64_t *a_row,
-                           int64_t *b_row, int64_t *d_row, int64_t *d_col) {
+int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int64_t n_off, int64_t n_len,
+                           int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row, int64_t *d_col) {
     if (cta_group == 0) cta_group = 2;
     if ((cta_group != 1 && cta_group != 2) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
-        m_idx * 128 * cta_group > kDimLimit || n_idx * 256 > kDimLimit || !a_row || !b_row || !d_row || !d_col) {
+        m_idx * 128 * cta_group > kDimLimit || n_idx * 256 > kDimLimit || !(n_len == 256 || n_len == 128) ||
+        !(n_off == 0 || (n_len == 128 && n_off == 128)) || !a_row || !b_row || !d_row || !d_col) {
         return GEMM_ERR_INVALID_ARG;
     }
-    TileCoord tc;
-    tc.m_idx = static_cast<int32_t>(m_idx);
-    tc.n_idx = static_cast<int32_t>(n_idx);
-    const CtaOrigin o = cta_origin(tc, cta_group, rank);
+    WorkItem w;
+    w.m_idx = static_cast<int32_t>(m_idx);
+    w.n_idx = static_cast<int32_t>(n_idx);
+    w.n_off = static_cast<int32_t>(n_off);
+    w.n_len = static_cast<int32_t>(n_len);
+    const CtaOrigin o = cta_origin(w, cta_group, rank);
     *a_row = o.a_row;
     *b_row = o.b_row;
     *d_row = o.d_row;

@@ -60,7 +60,8 @@ struct Cfg {
     static constexpr int A_STAGE = BLOCK_M * BLOCK_K * 2;
     static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
     static constexpr int STAGES = CG == 2 ? 6 : 4;
-    static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;  // per stage, on the leader
+    static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
+    static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = 2;
     static constexpr int TMEM_COLS = ACC_BUFS * BLOCK_N;            // 512: all of TMEM
     static constexpr int EPI_WARPS = 4;
@@ -86,6 +87,7 @@ struct Cfg {
 struct Params {
     int32_t M, N, K;
     int32_t num_m_tiles, num_n_tiles, k_tiles, num_tiles;
+    int32_t num_items, split_from;  // work items; items from split_from on are half tiles
     int32_t raster_group;
     uint32_t debug_flags;
     uint64_t timeout_ns;
@@ -130,7 +132,8 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
 template <int CG>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmD, const Params p) {
+                       const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
+                       const Params p) {
     using C = Cfg<CG>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -159,6 +162,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tmA);
         ptx::prefetch_tensormap(&tmB);
+        ptx::prefetch_tensormap(&tmBh);
         ptx::prefetch_tensormap(&tmD);
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
@@ -195,9 +199,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             PipelineState ring(C::STAGES, (p.debug_flags & kDebugProducerPhase0) ? 0u : 1u);
             uint32_t seq = 0;
             bool ok = true;
-            for (int t = cluster; ok && t < p.num_tiles; t += num_clusters, ++seq) {
-                const CtaOrigin o =
-                    cta_origin(tile_of(t, p.num_m_tiles, p.num_n_tiles, p.raster_group), CG, static_cast<int32_t>(rank));
+            for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
+                const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from);
+                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank));
+                const bool half = w.n_len < C::BLOCK_N;
+                const CUtensorMap *mapB = half ? &tmBh : &tmB;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
                                       kRoleProducer, seq)) {
@@ -205,15 +211,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                         break;
                     }
                     const uint32_t full = bar_full + 8 * ring.stage;
-                    if (leader) ptx::mbar_arrive_expect_tx(full, C::TX_BYTES);
+                    if (leader) ptx::mbar_arrive_expect_tx(full, half ? C::TX_HALF : C::TX_BYTES);
                     const int32_t k0 = kt * C::BLOCK_K;
                     if constexpr (CG == 2) {
                         const uint32_t full_leader = ptx::mapa(full, 0);
                         ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE, &tmA, full_leader, k0, o.a_row);
-                        ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, &tmB, full_leader, k0, o.b_row);
+                        ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, mapB, full_leader, k0, o.b_row);
                     } else {
                         ptx::tma_load_2d(sA + ring.stage * C::A_STAGE, &tmA, full, k0, o.a_row);
-                        ptx::tma_load_2d(sB + ring.stage * C::B_STAGE, &tmB, full, k0, o.b_row);
+                        ptx::tma_load_2d(sB + ring.stage * C::B_STAGE, mapB, full, k0, o.b_row);
                     }
                     ring.advance();
                 }
@@ -228,13 +234,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (leader && ptx::elect_one()) {
-            constexpr uint32_t idesc = idesc_f16_f32(C::TILE_M, C::BLOCK_N);
+            constexpr uint32_t idesc_full = idesc_f16_f32(C::TILE_M, C::BLOCK_N);
+            constexpr uint32_t idesc_half = idesc_f16_f32(C::TILE_M, C::BLOCK_N / 2);
             constexpr uint16_t pair_mask = CG == 2 ? 0x3 : 0x1;
             PipelineState ring(C::STAGES, 0u);
             PipelineState acc(C::ACC_BUFS, 1u);
             uint32_t seq = 0;
             bool ok = true;
-            for (int t = cluster; ok && t < p.num_tiles; t += num_clusters, ++seq) {
+            for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
+                const uint32_t idesc = item >= p.split_from ? idesc_half : idesc_full;
                 if (!wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
                                   seq)) {
                     ok = false;
@@ -276,9 +284,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         PipelineState acc(C::ACC_BUFS, 0u);
         uint32_t buf = 0;
         uint32_t seq = 0;
-        for (int t = cluster; t < p.num_tiles; t += num_clusters, ++seq) {
-            const CtaOrigin o =
-                cta_origin(tile_of(t, p.num_m_tiles, p.num_n_tiles, p.raster_group), CG, static_cast<int32_t>(rank));
+        for (int item = cluster; item < p.num_items; item += num_clusters, ++seq) {
+            const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from);
+            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank));
+            const int chunks = w.n_len / C::EPI_N;
             const int32_t row0 = o.d_row + quarter * 32;
             const int32_t col0 = o.d_col;
             bool ok = true;
@@ -292,12 +301,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(acc.stage * C::BLOCK_N);
 #pragma unroll 1
-            for (int c = 0; c < C::EPI_CHUNKS; ++c) {
+            for (int c = 0; c < chunks; ++c) {
                 uint32_t lo[32], hi[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N, lo);
                 ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
                 ptx::tmem_wait_ld();
-                if (c == C::EPI_CHUNKS - 1) {
+                if (c == chunks - 1) {
                     // The whole accumulator of this warp is in registers: hand
                     // the TMEM buffer back (TIRx notes V7, "Writeback Flow").
                     ptx::tcgen05_fence_before();

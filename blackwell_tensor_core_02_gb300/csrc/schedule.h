@@ -57,12 +57,55 @@ GEMM_HD TileCoord tile_of(int32_t t, int32_t num_m, int32_t num_n, int32_t group
     return c;
 }
 
-// Where one CTA of a tile reads and writes (TIRx notes V8, "Operand
-// Partition", "Output Ownership", "Epilogue Column Address").  A tile is
-// (128 * cg) rows x 256 columns of D.  CTA `rank` of the pair loads A rows
-// a_row .. +128 and B rows b_row .. +256/cg, and writes D rows d_row .. +128
-// over all 256 columns from d_col: the rank selects the A rows and the output
-// rows, and only the slice of B it loads, never the output columns.
+// One unit of work of a persistent cluster: a whole tile, or one half of a
+// tile split along N.  Splitting the tiles of a last, partly filled wave in
+// two lets twice as many clusters share that wave, so the tail lasts half a
+// tile instead of a whole one (the pages' persistent scheduler, TIRx notes
+// V6, leaves the last wave partly idle: 1024 tiles over 148 CTAs is 6.9
+// tiles each).
+struct WorkItem {
+    int32_t m_idx;
+    int32_t n_idx;
+    int32_t n_off;  // 0, or 128 for the second half of a split tile
+    int32_t n_len;  // 256, or 128 for a half tile
+};
+
+// Items [0, split_from) are whole tiles t = item in grouped order; items from
+// split_from on are the two halves of tiles split_from, split_from + 1, ...
+GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t group, int32_t split_from) {
+    int32_t t = item;
+    int32_t half = -1;
+    if (item >= split_from) {
+        const int32_t r = item - split_from;
+        t = split_from + r / 2;
+        half = r % 2;
+    }
+    const TileCoord c = tile_of(t, num_m, num_n, group);
+    WorkItem w;
+    w.m_idx = c.m_idx;
+    w.n_idx = c.n_idx;
+    w.n_off = half < 0 ? 0 : 128 * half;
+    w.n_len = half < 0 ? 256 : 128;
+    return w;
+}
+
+// Tiles [split_from, num_tiles) are split in two when that fits the last
+// wave: with num_tiles = q * clusters + r and 0 < 2r <= clusters, the r tiles
+// of the last wave become 2r half tiles, one per cluster.  Returns split_from
+// (num_tiles when nothing is split); the item count is then
+// num_tiles + (num_tiles - split_from).
+GEMM_HD int32_t split_point(int32_t num_tiles, int32_t clusters) {
+    const int32_t r = num_tiles % clusters;
+    if (r == 0 || 2 * r > clusters) return num_tiles;
+    return num_tiles - r;
+}
+
+// Where one CTA of a work item reads and writes (TIRx notes V8, "Operand
+// Partition", "Output Ownership", "Epilogue Column Address").  An item covers
+// (128 * cg) rows x n_len columns of D.  CTA `rank` of the pair loads A rows
+// a_row .. +128 and B rows b_row .. +n_len/cg, and writes D rows d_row .. +128
+// over all n_len columns from d_col: the rank selects the A rows and the
+// output rows, and only the slice of B it loads, never the output columns.
 struct CtaOrigin {
     int32_t a_row;
     int32_t b_row;
@@ -70,12 +113,12 @@ struct CtaOrigin {
     int32_t d_col;
 };
 
-GEMM_HD CtaOrigin cta_origin(TileCoord tc, int32_t cg, int32_t rank) {
+GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank) {
     CtaOrigin o;
-    const int32_t m_base = tc.m_idx * 128 * cg;
-    const int32_t n_base = tc.n_idx * 256;
+    const int32_t m_base = w.m_idx * 128 * cg;
+    const int32_t n_base = w.n_idx * 256 + w.n_off;
     o.a_row = m_base + rank * 128;
-    o.b_row = n_base + rank * (256 / cg);
+    o.b_row = n_base + rank * (w.n_len / cg);
     o.d_row = o.a_row;
     o.d_col = n_base;
     return o;

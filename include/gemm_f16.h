@@ -116,30 +116,38 @@ int gemm_f16_last_device_status(void *stream, uint64_t *info);
 const char *gemm_f16_status_string(int status);
 
 /*
- * The persistent tile scheduler, as a pure host query (no CUDA call).  The
- * output is cut into tiles of (128 * cta_group) rows x 256 columns; cluster
- * `cluster_id` of `num_clusters` takes tiles cluster_id, cluster_id +
- * num_clusters, ... in a grouped order: groups of `raster_group` M-tiles, M
- * fastest inside a group, then N, then the next group (TIRx notes V6, "Better
- * L2 Locality").  Returns 1 and the tile's (m_idx, n_idx) if that cluster has
- * an iter-th tile, 0 if it has not, GEMM_ERR_INVALID_ARG for bad arguments.
+ * The persistent scheduler, as a pure host query (no CUDA call); the kernel
+ * runs the same code.  D is cut into tiles of (128 * cta_group) rows x 256
+ * columns, ordered in groups of `raster_group` M-tiles: M fastest inside a
+ * group, then N, then the next group (TIRx notes V6, "Better L2 Locality",
+ * l2_group_size = 8).  With T tiles and P = num_clusters persistent clusters,
+ * if the last wave is at most half full (T = qP + r, 0 < 2r <= P) its r tiles
+ * are split along N into 2r half tiles of 128 columns, so that the tail lasts
+ * half a tile (V6 notes that 1024 tiles over 148 CTAs leave 6.9 tiles per CTA,
+ * i.e. a partly idle last wave).  Cluster `cluster_id` takes work items
+ * cluster_id, cluster_id + P, ...  Returns 1 and the iter-th item of that
+ * cluster -- tile (m_idx, n_idx), columns n_off .. n_off + n_len of that tile
+ * (n_len 256, or 128 for a half) -- 0 if the cluster has no iter-th item, or
+ * GEMM_ERR_INVALID_ARG for bad arguments.
  */
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster_group, int64_t num_clusters,
-                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx);
+                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx, int64_t *n_off,
+                         int64_t *n_len);
 
 /*
- * Where CTA `rank` of tile (m_idx, n_idx) reads and writes, as a pure host
- * query (no CUDA call); the kernel uses the same function.  TIRx notes V8,
- * "Operand Partition" and "Output Ownership": with m_base = m_idx * 128 *
- * cta_group and n_base = n_idx * 256, the CTA loads A rows a_row = m_base +
- * 128 * rank (128 rows) and B rows b_row = n_base + (256 / cta_group) * rank
- * (256 / cta_group rows), and writes D rows d_row = a_row (128 rows) over the
- * 256 columns starting at d_col = n_base ("Epilogue Column Address": no rank
- * term).  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not 0/1/2, rank
- * out of range, negative or too large indices, null outputs).
+ * Where CTA `rank` of a work item reads and writes, as a pure host query (no
+ * CUDA call); the kernel uses the same function.  TIRx notes V8, "Operand
+ * Partition" and "Output Ownership": with m_base = m_idx * 128 * cta_group and
+ * n_base = n_idx * 256 + n_off, the CTA loads A rows a_row = m_base + 128 * rank
+ * (128 rows) and B rows b_row = n_base + (n_len / cta_group) * rank (n_len /
+ * cta_group rows), and writes D rows d_row = a_row (128 rows) over the n_len
+ * columns starting at d_col = n_base ("Epilogue Column Address": no rank
+ * term).  n_len is 256 (whole tile, n_off 0) or 128 (half tile, n_off 0 or
+ * 128).  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not 0/1/2, rank
+ * out of range, bad n_off/n_len, negative or too large indices, null outputs).
  */
-int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int32_t rank, int64_t *a_row,
-                           int64_t *b_row, int64_t *d_row, int64_t *d_col);
+int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int64_t n_off, int64_t n_len,
+                           int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row, int64_t *d_col);
 
 /*
  * The stage/phase bookkeeping of one SMEM or TMEM ring, run on the host with

@@ -94,37 +94,72 @@ def test_status_strings():
 @pytest.mark.parametrize("M,N,cg,group,clusters", [
     (4096, 4096, 2, 8, 74), (4096, 4096, 2, 8, 76), (8192, 28672, 2, 8, 76), (4096, 4096, 1, 8, 148),
     (300, 520, 2, 8, 3), (1, 8, 1, 1, 1), (2560, 1280, 2, 3, 7), (1000, 7000, 1, 5, 13), (128, 128, 2, 8, 1),
+    (128, 128, 2, 8, 76), (8192, 8192, 2, 8, 76), (1024, 1024, 2, 8, 5),
 ])
-def test_schedule_is_a_bijection(M, N, cg, group, clusters):
+def test_schedule_covers_every_output_once(M, N, cg, group, clusters):
+    """Every 128-column block of every tile is computed by exactly one work item."""
     num_m = -(-M // (128 * cg))
     num_n = -(-N // 256)
-    seen = {}
+    tiles = num_m * num_n
+    cover = {}
+    per_cluster = []
     for c in range(clusters):
         it = 0
         while True:
-            t = g.schedule(M, N, cg, group, clusters, c, it)
-            if t is None:
+            w = g.schedule(M, N, cg, group, clusters, c, it)
+            if w is None:
                 break
-            assert 0 <= t[0] < num_m and 0 <= t[1] < num_n
-            assert t not in seen, f"tile {t} assigned twice"
-            seen[t] = (c, it)
+            m_idx, n_idx, n_off, n_len = w
+            assert 0 <= m_idx < num_m and 0 <= n_idx < num_n and n_len in (128, 256)
+            for half in range(n_off // 128, (n_off + n_len) // 128):
+                key = (m_idx, n_idx, half)
+                assert key not in cover, f"{key} computed twice"
+                cover[key] = (c, it)
             it += 1
-        # cluster c has exactly the tiles c, c + P, c + 2P, ...
-        assert it == len(range(c, num_m * num_n, clusters))
-    assert len(seen) == num_m * num_n
+        per_cluster.append(it)
+    assert len(cover) == 2 * tiles
+    r = tiles % clusters
+    split = 0 < 2 * r <= clusters
+    items = tiles + (r if split else 0)
+    # items are dealt round-robin: cluster c has the items c, c + P, ...
+    assert per_cluster == [len(range(c, items, clusters)) for c in range(clusters)]
+    # with a split, no cluster runs more than ceil(tiles / P) - 1/2 tile-times
+    if split:
+        work = [0.0] * clusters
+        for (_, _, _), (c, _) in cover.items():
+            work[c] += 0.5
+        assert max(work) == tiles // clusters + 0.5
 
 
 def test_schedule_grouped_order():
     # 16 x 16 tiles, groups of 8 M-tiles: M fastest inside a group, then N.
-    order = [g.schedule(4096, 4096, 2, 8, 1, 0, i) for i in range(256)]
+    order = [g.schedule(4096, 4096, 2, 8, 1, 0, i)[:2] for i in range(256)]
     assert order[:9] == [(m, 0) for m in range(8)] + [(0, 1)]
     assert order[127] == (7, 15) and order[128] == (8, 0) and order[255] == (15, 15)
+
+
+def test_schedule_splits_the_last_wave_of_4096():
+    # 256 tiles over 76 CTA pairs: 3 full waves (228 tiles), then 28 tiles split
+    # into 56 half tiles, one per pair, so the tail lasts half a tile.
+    items = []
+    for c in range(76):
+        it = 0
+        while (w := g.schedule(4096, 4096, 2, 8, 76, c, it)) is not None:
+            items.append((c, it, w))
+            it += 1
+    assert len(items) == 228 + 56
+    assert all(w[3] == 256 for c, it, w in items if it < 3)
+    assert all(w[3] == 128 for c, it, w in items if it == 3)
+    assert sum(1 for c, it, w in items if it == 3) == 56
 
 
 def test_cta_origin_matches_the_pages_operand_partition():
     for m_idx, n_idx, cbx, a_row, b_row, d_row, d_col in _golden_rows("v8_operand_partition.txt"):
         got = g.cta_origin(2, m_idx, n_idx, cbx)
         assert got == dict(a_row=a_row, b_row=b_row, d_row=d_row, d_col=d_col)
+    # a half tile keeps the same partition inside its 128 columns
+    assert g.cta_origin(2, 1, 2, 1, n_off=128, n_len=128) == dict(a_row=384, b_row=704, d_row=384, d_col=640)
+    assert g.cta_origin(1, 1, 2, 0, n_off=128, n_len=128) == dict(a_row=128, b_row=640, d_row=128, d_col=640)
 
 
 def test_cta_origin_ownership_covers_each_output_once():
@@ -143,6 +178,8 @@ def test_cta_origin_ownership_covers_each_output_once():
         assert np.all(cover == 1)
     with pytest.raises(g.GemmError):
         g.cta_origin(2, 0, 0, 2)
+    with pytest.raises(g.GemmError):
+        g.cta_origin(2, 0, 0, 0, n_off=128, n_len=256)
 
 
 def test_pipeline_state_matches_the_pages_table():

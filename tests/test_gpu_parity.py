@@ -97,6 +97,20 @@ def test_few_persistent_clusters_run_many_tiles(gpu_lib, cg, clusters):
                  f"cg={cg} clusters={clusters}")
 
 
+@pytest.mark.parametrize("M,N,K,cg,clusters", [
+    (1024, 1024, 320, 2, 5),   # 16 tiles on 5 pairs: 15 whole + 1 split into halves
+    (1024, 1024, 320, 1, 30),  # 32 tiles on 30 CTAs: 2 split
+    (640, 776, 200, 2, 5),     # ragged N: a split half lies wholly past the last column
+    (256, 4096, 512, 2, 76),   # 16 tiles on 76 pairs: every tile split
+    (1024, 1024, 320, 2, 10),  # 16 % 10 = 6 > 10 / 2: no split
+])
+def test_split_last_wave(gpu_lib, M, N, K, cg, clusters):
+    w = si.custom(M, N, K, seed=M + N + K + cg)
+    A, B = w.operands()
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg, clusters)), oracle.gemm_f16_nt(A, B),
+                 f"split {M}x{N}x{K} cg={cg} clusters={clusters}")
+
+
 def test_guard_bands_and_full_overwrite(gpu_lib):
     # D sits inside a larger buffer filled with a NaN sentinel: every element of
     # D must be written, and nothing before or after it.
