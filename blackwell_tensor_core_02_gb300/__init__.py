@@ -38,7 +38,8 @@ class GemmError(RuntimeError):
 class Options(ctypes.Structure):
     """Mirror of ``gemm_f16_options`` (zero fields mean defaults)."""
     _fields_ = [("cta_group", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
-                ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64)]
+                ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
+                ("overlap_launch", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

@@ -31,7 +31,7 @@ DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 template <int CG>
-cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr) {
+cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr, bool overlap = false) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(Cfg<CG>::THREADS, 1, 1);
@@ -43,6 +43,14 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttri
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (overlap) {
+        // Programmatic dependent launch: this grid may be scheduled while the
+        // previous kernel of the stream finishes; the kernel waits for it
+        // (griddepcontrol.wait) before its first access to A, B or D.
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
     return cfg;
 }
 
@@ -124,7 +132,7 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 template <int CG>
 int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
            const DeviceInfo &dev, int32_t max_clusters, int32_t raster_group, int64_t timeout_ns,
-           uint32_t debug_flags) {
+           uint32_t debug_flags, bool overlap) {
     using C = Cfg<CG>;
     CUtensorMap tmA, tmB, tmBh, tmD;
     if (encode_map(&tmA, A, M, K, C::BLOCK_M) != GEMM_OK || encode_map(&tmB, B, N, K, C::B_ROWS) != GEMM_OK ||
@@ -149,8 +157,9 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     p.split_from = split_point(p.num_tiles, static_cast<int32_t>(clusters));
     p.num_items = p.num_tiles + (p.num_tiles - p.split_from);
     if (clusters > p.num_items) clusters = p.num_items;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config<CG>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg =
+        launch_config<CG>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr, overlap);
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG>, tmA, tmB, tmBh, tmD, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
@@ -187,7 +196,10 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
     int32_t cta_group = 2, max_clusters = 0, raster_group = kDefaultRasterGroup;
     int64_t timeout_ns = kDefaultTimeoutNs;
     uint32_t debug_flags = 0;
+    bool overlap = true;
     if (opts) {
+        if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
+        if (opts->overlap_launch == -1) overlap = false;
         if (opts->cta_group != 0) cta_group = opts->cta_group;
         if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
             (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
@@ -213,8 +225,9 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
     if (st != GEMM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_fill(D, M, N, s);
-    if (cta_group == 2) return launch<2>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags);
-    return launch<1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags);
+    if (cta_group == 2) return launch<2>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags,
+                                          overlap);
+    return launch<1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
 }
 
 int gemm_f16_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream) {

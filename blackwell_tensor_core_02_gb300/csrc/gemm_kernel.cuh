@@ -188,6 +188,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     }
     ptx::tcgen05_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+    // Everything above touches only this CTA's own resources, so with a
+    // programmatic launch it overlaps the tail of the previous kernel of the
+    // stream.  A, B and D are first touched below, after the wait.
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer

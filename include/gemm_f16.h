@@ -67,6 +67,12 @@ typedef enum gemm_status {
  *                 must end the kernel with GEMM_ERR_DEVICE_TIMEOUT, not hang.
  *                 Other bits: GEMM_ERR_INVALID_ARG.
  *   timeout_ns    limit of every wait inside the kernel; 0 = 4 s.
+ *   overlap_launch  0 or 1 (default): launch as a programmatic dependent of
+ *                 the previous kernel on the stream, so that this kernel's
+ *                 set-up (barriers, tensor memory) overlaps that kernel's
+ *                 tail; the kernel still waits for it to finish, and for its
+ *                 writes to be visible, before it reads A or B or writes D.
+ *                 -1: an ordinary launch.  Other values: GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;
@@ -74,6 +80,8 @@ typedef struct gemm_f16_options {
     int32_t raster_group;
     int32_t debug_flags;
     int64_t timeout_ns;
+    int32_t overlap_launch;
+    int32_t reserved;
 } gemm_f16_options;
 
 /*

@@ -73,7 +73,7 @@ def test_argument_errors_are_returned_before_any_launch():
     assert lib.gemm_f16_nt(None, None, None, 0, 128, 64, None) == OK
     assert lib.gemm_f16_nt(None, None, None, 128, 0, 64, None) == OK
     for bad in (g.Options(cta_group=3), g.Options(max_clusters=-1), g.Options(raster_group=-2),
-                g.Options(debug_flags=2), g.Options(timeout_ns=-5)):
+                g.Options(debug_flags=2), g.Options(timeout_ns=-5), g.Options(overlap_launch=2)):
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
 

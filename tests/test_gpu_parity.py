@@ -156,6 +156,27 @@ def test_argument_errors_on_device(gpu_lib):
     assert torch.count_nonzero(D).item() == 0
 
 
+@pytest.mark.parametrize("overlap", [1, -1])
+def test_back_to_back_dependent_calls(gpu_lib, overlap):
+    # D1 = A·Bᵀ, then D2 = D1·Cᵀ reads it, launched back to back on one stream
+    # with and without the overlapped (programmatic dependent) launch.  D1 is
+    # filled with NaN first, so a second kernel that read D1 before the first
+    # finished writing it would produce NaN or wrong values.
+    w = si.custom(512, 512, 256, seed=31)
+    A, B = w.operands()
+    C = si.custom(256, 8, 512, seed=32, dist=si.Dist("uniform", -0.125, 0.125)).operands()[0]  # 256 x 512
+    o = gpu_lib.Options(overlap_launch=overlap)
+    dA, dB, dC = to_dev(A), to_dev(B), to_dev(C)
+    for _ in range(4):
+        D1 = torch.full((512, 512), float("nan"), dtype=torch.float16, device="cuda")
+        gpu_lib.gemm_f16_nt(dA, dB, D1, options=o)
+        D2 = gpu_lib.gemm_f16_nt(D1, dC, options=o)
+        assert gpu_lib.last_device_status()[0] == 0
+        D1h = D1.cpu().numpy()
+        assert_close(D1h, oracle.gemm_f16_nt(A, B), "first")
+        assert_close(D2.cpu().numpy(), oracle.gemm_f16_nt(D1h, C), "second (reads the first)")
+
+
 def test_repeated_calls_and_streams(gpu_lib):
     w = si.WORKLOADS["ktile_grid_256x256x512"]
     A, B = w.operands()
