@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "GemmError", "Options", "load", "gemm_f16_nt", "gemm_f16_nt_ptr", "gemm_f16_nt_supported",
-    "gemm_f16_nt_host", "last_device_status", "status_string", "schedule", "cta_origin", "pipeline_trace", "STATUS",
+    "gemm_f16_nt_host", "HostPipeline", "last_device_status", "status_string", "schedule", "cta_origin", "pipeline_trace", "STATUS",
 ]
 
 STATUS = {
@@ -151,6 +151,83 @@ def gemm_f16_nt_host(A_host, B_host, D_host=None, *, device=None, stream=None, A
         D_host.copy_(D_dev, non_blocking=True)
     s.synchronize()
     return D_host
+
+
+class HostPipeline:
+    """GEMMs on HOST fp16 tensors with the copies overlapped: D_i = A_i·B_iᵀ.
+
+    Three streams: copy-in, compute, copy-out.  Device buffers come in
+    `depth` slots; step i uses slot i % depth, so step i+1's copy-in and step
+    i-1's copy-out run while step i's GEMM does.  Events keep each slot's
+    buffers from being overwritten before they are consumed.  Pass pinned host
+    tensors, and read a D_host only after synchronize().  Copy-outs run in
+    submission order on one stream, so reusing a D_host is ordered.
+    """
+
+    def __init__(self, M: int, N: int, K: int, *, device=None, depth: int = 2):
+        import torch
+
+        self.dev = torch.device(device or "cuda")
+        self.M, self.N, self.K = M, N, K
+        self.depth = depth
+        self.h2d = torch.cuda.Stream(self.dev)
+        self.comp = torch.cuda.Stream(self.dev)
+        self.d2h = torch.cuda.Stream(self.dev)
+        mk = lambda *shape: torch.empty(shape, dtype=torch.float16, device=self.dev)  # noqa: E731
+        self.A = [mk(M, K) for _ in range(depth)]
+        self.B = [mk(N, K) for _ in range(depth)]
+        self.D = [mk(M, N) for _ in range(depth)]
+        ev = lambda: [torch.cuda.Event() for _ in range(depth)]  # noqa: E731
+        self.loaded, self.computed, self.stored = ev(), ev(), ev()
+        self.used = [False] * depth
+        self.i = 0
+
+    def submit(self, A_host, B_host, D_host) -> None:
+        """Queue one step: copy A_host, B_host in, compute, copy D out into D_host."""
+        j = self.i % self.depth
+        self.i += 1
+        if self.used[j]:
+            self.h2d.wait_event(self.computed[j])   # slot j's A, B consumed by its last GEMM
+            self.comp.wait_event(self.stored[j])    # slot j's D copied out
+        with torch_stream(self.h2d):
+            self.A[j].copy_(A_host, non_blocking=True)
+            self.B[j].copy_(B_host, non_blocking=True)
+            self.loaded[j].record(self.h2d)
+        self.comp.wait_event(self.loaded[j])
+        gemm_f16_nt(self.A[j], self.B[j], self.D[j], stream=self.comp)
+        self.computed[j].record(self.comp)
+        self.d2h.wait_event(self.computed[j])
+        with torch_stream(self.d2h):
+            D_host.copy_(self.D[j], non_blocking=True)
+            self.stored[j].record(self.d2h)
+        self.used[j] = True
+
+    def record_start(self):
+        """An event on the copy-in stream before the next submit (for timing)."""
+        import torch
+
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.h2d)
+        return e
+
+    def record_end(self):
+        """An event on the copy-out stream after everything submitted so far (for timing)."""
+        import torch
+
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(self.d2h)
+        return e
+
+    def synchronize(self) -> None:
+        self.h2d.synchronize()
+        self.comp.synchronize()
+        self.d2h.synchronize()
+
+
+def torch_stream(s):
+    import torch
+
+    return torch.cuda.stream(s)
 
 
 def last_device_status(stream=None) -> tuple[int, int]:

@@ -110,16 +110,17 @@ __device__ __forceinline__ void record_failure(uint32_t role, uint32_t seq) {
 }
 
 // Bounded wait by one thread.  Returns false if the wait ran out (the failure
-// is recorded and the CTA's abort flag raised) or if another role of this CTA
-// already aborted.
+// is recorded and the CTA's abort flag raised) or, when `honor_abort`, as soon
+// as another role of this CTA has aborted.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             uint64_t timeout_ns, uint32_t role, uint32_t seq) {
+                                             uint64_t timeout_ns, uint32_t role, uint32_t seq,
+                                             bool honor_abort = true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
-            if (*abort_flag) return false;
+            if (honor_abort && *abort_flag) return false;
             if (ptx::globaltimer_ns() - t0 > timeout_ns) {
                 *abort_flag = 1;
                 record_failure(role, seq);
@@ -277,9 +278,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                 ptx::mma_commit<CG>(bar_tfull + 8 * acc.stage, pair_mask);  // accumulator ready, both CTAs
                 acc.advance();
             }
-            // Wait for every MMA issued so far before TMEM can be released.
+            // Wait for every MMA issued so far before TMEM can be released,
+            // also after an abort (then only the time limit ends the wait).
             ptx::mma_commit<CG>(bar_drain, 0x1);
-            wait_bounded(bar_drain, 0, abort_flag, p.timeout_ns, kRoleMma, 0xFFFFFFFFu);
+            wait_bounded(bar_drain, 0, abort_flag, p.timeout_ns, kRoleMma, 0xFFFFFFFFu, false);
         }
         __syncwarp();
     } else {

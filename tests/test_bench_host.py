@@ -1,0 +1,59 @@
+"""Host logic of bench.py: the cross-rank reduction (2 gloo ranks on CPU) and the CLI contract."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    elapsed = [10.0, 12.5][rank]  # rank 1 is the slow one
+    m = bench.max_over_ranks(elapsed, dist, "cpu")
+    v = bench.whole_job_tflops(1e12, 100, world, m)
+    with open(os.path.join(out_dir, f"r{rank}.json"), "w") as f:
+        json.dump({"max": m, "value": v}, f)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks(tmp_path):
+    torch = pytest.importorskip("torch")
+    import socket
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    torch.multiprocessing.spawn(_rank_main, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    res = [json.load(open(tmp_path / f"r{r}.json")) for r in range(2)]
+    assert res[0] == res[1]
+    assert res[0]["max"] == 12.5
+    # 2 replicas x 100 steps x 1 TFLOP in 12.5 ms
+    assert res[0]["value"] == pytest.approx(2 * 100 * 1e12 / 12.5e-3 / 1e12)
+
+
+def test_single_rank_reduction_is_identity():
+    assert bench.max_over_ranks(3.25) == 3.25
+    assert bench.whole_job_tflops(2e12, 10, 1, 20.0) == pytest.approx(1000.0)
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3",
+                        "--warmup", "3"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_warmup_below_three_is_rejected():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode != 0 and "warmup" in r.stderr

@@ -193,6 +193,23 @@ def test_repeated_calls_and_streams(gpu_lib):
         assert_close(o.cpu().numpy(), ref, "repeat")
 
 
+def test_host_pipeline_end_to_end(gpu_lib):
+    # Host-buffer path with overlapped copies: three different problems in
+    # flight through two device slots; every result must match its own oracle.
+    probs = [si.custom(384, 520, 264, seed=s).operands() for s in (41, 42, 43, 44, 45)]
+    pipe = gpu_lib.HostPipeline(384, 520, 264)
+    outs = [torch.empty((384, 520), dtype=torch.float16).pin_memory() for _ in probs]
+    for (A, B), D in zip(probs, outs):
+        pipe.submit(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory(), D)
+    pipe.synchronize()
+    assert gpu_lib.last_device_status()[0] == 0
+    for (A, B), D in zip(probs, outs):
+        assert_close(D.numpy(), oracle.gemm_f16_nt(A, B), "pipeline")
+    A, B = probs[0]
+    single = gpu_lib.gemm_f16_nt_host(torch.from_numpy(A).pin_memory(), torch.from_numpy(B).pin_memory())
+    assert_close(single.numpy(), oracle.gemm_f16_nt(A, B), "single host call")
+
+
 # ------------------------------------------------ full-size, sampled compares --
 
 def _sample_indices(n, tile, count, rng):
