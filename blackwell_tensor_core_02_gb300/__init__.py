@@ -66,7 +66,7 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_last_device_status.restype = ctypes.c_int
         lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
         lib.gemm_f16_status_string.restype = ctypes.c_char_p
-        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i32, i32, i64, i64, i64, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i64, i64, i64, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_schedule.restype = ctypes.c_int
         lib.gemm_f16_nt_cta_origin.argtypes = [i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
@@ -238,10 +238,10 @@ def last_device_status(stream=None) -> tuple[int, int]:
 
 
 def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
-             it: int):
+             it: int, K: int = 4096):
     """The iter-th work item (m_idx, n_idx, n_off, n_len) of one cluster, or None when it has no more."""
     out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_schedule(M, N, cta_group, raster_group, num_clusters, cluster_id, it,
+    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, raster_group, num_clusters, cluster_id, it,
                                      *[ctypes.byref(o) for o in out])
     if rc < 0:
         raise GemmError(rc, "gemm_f16_nt_schedule")

@@ -16,7 +16,6 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultTimeoutNs = 4000000000LL;
-constexpr int32_t kDefaultRasterGroup = 8;
 constexpr int64_t kDimLimit = (int64_t(1) << 31) - 1;
 
 struct DeviceInfo {
@@ -149,7 +148,7 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
     if (tiles > kDimLimit) return GEMM_ERR_UNSUPPORTED_SHAPE;
     p.num_tiles = static_cast<int32_t>(tiles);
-    p.raster_group = raster_group;
+    p.raster_group = raster_group > 0 ? raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
     p.debug_flags = debug_flags;
     p.timeout_ns = static_cast<uint64_t>(timeout_ns);
     int64_t clusters = dev.max_clusters[CG];
@@ -193,7 +192,7 @@ int gemm_f16_nt_supported(int64_t M, int64_t N, int64_t K) { return shape_ok(M, 
 
 int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
                    const gemm_f16_options *opts) {
-    int32_t cta_group = 2, max_clusters = 0, raster_group = kDefaultRasterGroup;
+    int32_t cta_group = 2, max_clusters = 0, raster_group = 0;
     int64_t timeout_ns = kDefaultTimeoutNs;
     uint32_t debug_flags = 0;
     bool overlap = true;
@@ -207,7 +206,7 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
         }
         debug_flags = static_cast<uint32_t>(opts->debug_flags);
         max_clusters = opts->max_clusters;
-        if (opts->raster_group != 0) raster_group = opts->raster_group;
+        raster_group = opts->raster_group;
         if (opts->timeout_ns != 0) timeout_ns = opts->timeout_ns;
     }
     if (cta_group != 1 && cta_group != 2) return GEMM_ERR_INVALID_ARG;
@@ -276,12 +275,12 @@ const char *gemm_f16_status_string(int status) {
     }
 }
 
-int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster_group, int64_t num_clusters,
-                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx, int64_t *n_off,
-                         int64_t *n_len) {
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t raster_group,
+                         int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx,
+                         int64_t *n_off, int64_t *n_len) {
     if (cta_group == 0) cta_group = 2;
-    if (raster_group == 0) raster_group = kDefaultRasterGroup;
-    if ((cta_group != 1 && cta_group != 2) || raster_group < 0 || M <= 0 || N <= 0 || M > kDimLimit ||
+    if ((cta_group != 1 && cta_group != 2) || raster_group < 0 || K < 0 || K > kDimLimit || M <= 0 || N <= 0 ||
+        M > kDimLimit ||
         N > kDimLimit || num_clusters <= 0 || num_clusters > kDimLimit || cluster_id < 0 ||
         cluster_id >= num_clusters || iter < 0 || !m_idx || !n_idx || !n_off || !n_len) {
         return GEMM_ERR_INVALID_ARG;
@@ -290,6 +289,7 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster
     const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
     const int64_t tiles = num_m * num_n;
     if (tiles > kDimLimit / 2) return GEMM_ERR_INVALID_ARG;
+    if (raster_group == 0) raster_group = auto_raster_group(static_cast<int32_t>(num_m), K, static_cast<int32_t>(tile_m));
     const int32_t split_from = split_point(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters));
     const int64_t items = tiles + (tiles - split_from);
     const int64_t item = cluster_id + iter * num_clusters;

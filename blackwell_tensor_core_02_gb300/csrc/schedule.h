@@ -57,6 +57,22 @@ GEMM_HD TileCoord tile_of(int32_t t, int32_t num_m, int32_t num_n, int32_t group
     return c;
 }
 
+// Default size of the grouped raster, in M-tiles.  Inside a group the A panel
+// (group x tile_m rows x K) is reused by every N-tile while B streams past, so
+// B is read from memory once per group: total reads ~ A + ceil(num_m/group)*B.
+// Larger groups read less, until the panel no longer stays in L2; the group
+// is the largest whose A panel fits in 32 MiB (a quarter of GB300's L2), at
+// least 1 and at most num_m.  (TIRx notes V6 fixes l2_group_size = 8 for
+// 128x128 tiles at K = 4096, i.e. a 8 MiB panel; the measured optimum on
+// GB300 with 256-row tiles is 16 at K = 4096 and 8 at K = 8192, both 32 MiB.)
+GEMM_HD int32_t auto_raster_group(int32_t num_m, int64_t K, int32_t tile_m) {
+    const int64_t panel = static_cast<int64_t>(tile_m) * (K > 0 ? K : 1) * 2;
+    int64_t g = (int64_t(32) << 20) / panel;
+    if (g < 1) g = 1;
+    if (g > num_m) g = num_m;
+    return static_cast<int32_t>(g);
+}
+
 // One unit of work of a persistent cluster: a whole tile, or one half of a
 // tile split along N.  Splitting the tiles of a last, partly filled wave in
 // two lets twice as many clusters share that wave, so the tail lasts half a

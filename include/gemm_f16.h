@@ -59,7 +59,9 @@ typedef enum gemm_status {
  *   max_clusters  cap on the persistent grid, in clusters (CTA pairs for
  *                 cta_group 2); 0 = as many as are co-resident on the device.
  *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes
- *                 V6 "l2_group_size = 8"); 0 = 8.
+ *                 V6, "l2_group_size"); 0 = chosen from the shape: the largest
+ *                 group whose A panel (group x 128*cta_group rows x K fp16)
+ *                 fits in 32 MiB, between 1 and the number of M-tiles.
  *   debug_flags   test hook, 0 in normal use.  1 starts the producer end of
  *                 the SMEM ring at phase 0 instead of 1 -- the pages' "subtlest
  *                 bug" ("GEMM III", "opposite initial phases") -- so that every
@@ -126,9 +128,9 @@ const char *gemm_f16_status_string(int status);
 /*
  * The persistent scheduler, as a pure host query (no CUDA call); the kernel
  * runs the same code.  D is cut into tiles of (128 * cta_group) rows x 256
- * columns, ordered in groups of `raster_group` M-tiles: M fastest inside a
- * group, then N, then the next group (TIRx notes V6, "Better L2 Locality",
- * l2_group_size = 8).  With T tiles and P = num_clusters persistent clusters,
+ * columns, ordered in groups of `raster_group` M-tiles (0 = the shape-derived
+ * default described under gemm_f16_options, which needs K): M fastest inside
+ * a group, then N, then the next group (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters persistent clusters,
  * if the last wave is at most half full (T = qP + r, 0 < 2r <= P) its r tiles
  * are split along N into 2r half tiles of 128 columns, so that the tail lasts
  * half a tile (V6 notes that 1024 tiles over 148 CTAs leave 6.9 tiles per CTA,
@@ -138,9 +140,9 @@ const char *gemm_f16_status_string(int status);
  * (n_len 256, or 128 for a half) -- 0 if the cluster has no iter-th item, or
  * GEMM_ERR_INVALID_ARG for bad arguments.
  */
-int gemm_f16_nt_schedule(int64_t M, int64_t N, int32_t cta_group, int32_t raster_group, int64_t num_clusters,
-                         int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx, int64_t *n_off,
-                         int64_t *n_len);
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t raster_group,
+                         int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx,
+                         int64_t *n_off, int64_t *n_len);
 
 /*
  * Where CTA `rank` of a work item reads and writes, as a pure host query (no

@@ -131,6 +131,16 @@ def test_schedule_covers_every_output_once(M, N, cg, group, clusters):
         assert max(work) == tiles // clusters + 0.5
 
 
+def test_default_raster_group_keeps_a_32mib_a_panel():
+    # 0 = automatic: the largest group of 256-row M-tiles whose A panel fits 32 MiB.
+    def group_of(M, N, K, cg=2):
+        first = [g.schedule(M, N, cg, 0, 1, 0, i, K=K)[0] for i in range(40)]
+        return next((i for i, m in enumerate(first) if m == 0 and i > 0), None)
+    assert group_of(8192, 28672, 4096) == 16  # 16 x 256 rows x 4096 x 2 B = 32 MiB
+    assert group_of(8192, 8192, 8192) == 8
+    assert group_of(2048, 8192, 4096) == 8    # capped at the 8 M-tiles there are
+
+
 def test_schedule_grouped_order():
     # 16 x 16 tiles, groups of 8 M-tiles: M fastest inside a group, then N.
     order = [g.schedule(4096, 4096, 2, 8, 1, 0, i)[:2] for i in range(256)]
