@@ -39,7 +39,7 @@ class Options(ctypes.Structure):
     """Mirror of ``gemm_f16_options`` (zero fields mean defaults)."""
     _fields_ = [("cta_group", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
-                ("overlap_launch", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("overlap_launch", ctypes.c_int32), ("consumers", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -66,9 +66,9 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_last_device_status.restype = ctypes.c_int
         lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
         lib.gemm_f16_status_string.restype = ctypes.c_char_p
-        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i64, i64, i64, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i64, i64, i64, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_schedule.restype = ctypes.c_int
-        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
         lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
         lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
@@ -238,20 +238,21 @@ def last_device_status(stream=None) -> tuple[int, int]:
 
 
 def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
-             it: int, K: int = 4096):
+             it: int, K: int = 4096, consumers: int = 1):
     """The iter-th work item (m_idx, n_idx, n_off, n_len) of one cluster, or None when it has no more."""
     out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, raster_group, num_clusters, cluster_id, it,
+    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, raster_group, num_clusters, cluster_id, it,
                                      *[ctypes.byref(o) for o in out])
     if rc < 0:
         raise GemmError(rc, "gemm_f16_nt_schedule")
     return tuple(o.value for o in out) if rc == 1 else None
 
 
-def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int, n_off: int = 0, n_len: int = 256) -> dict:
+def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int, n_off: int = 0, n_len: int = 256,
+               consumers: int = 1) -> dict:
     """Rows/columns CTA `rank` of a work item loads and writes (see the C header)."""
     out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_cta_origin(cta_group, m_idx, n_idx, n_off, n_len, rank,
+    rc = load().gemm_f16_nt_cta_origin(cta_group, consumers, m_idx, n_idx, n_off, n_len, rank,
                                        *[ctypes.byref(o) for o in out])
     if rc != 0:
         raise GemmError(rc, "gemm_f16_nt_cta_origin")

@@ -22,19 +22,19 @@ struct DeviceInfo {
     bool ready = false;
     int status = GEMM_OK;
     int sm_count = 0;
-    int max_clusters[3] = {0, 0, 0};  // co-resident clusters for cta_group 1 and 2
+    int max_clusters[3] = {0, 0, 0};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2 consumers
 };
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int CG>
+template <int CG, int NC>
 cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr, bool overlap = false) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(Cfg<CG>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<CG>::SMEM_ALLOC;
+    cfg.blockDim = dim3(Cfg<CG, NC>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG, NC>::SMEM_ALLOC;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
@@ -53,15 +53,15 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttri
     return cfg;
 }
 
-template <int CG>
+template <int CG, int NC>
 int prepare_kernel(int *max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<CG>::SMEM_ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<CG, NC>::SMEM_ALLOC);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config<CG>(dim3(CG, 1, 1), nullptr, attr);
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = launch_config<CG, NC>(dim3(CG, 1, 1), nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC>, &cfg);
     if (e != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
     *max_clusters = n;
     return GEMM_OK;
@@ -89,8 +89,9 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
         } else if (major != 10 || minor != 3) {
             d.status = GEMM_ERR_ARCH;
         } else {
-            d.status = prepare_kernel<1>(&d.max_clusters[1]);
-            if (d.status == GEMM_OK) d.status = prepare_kernel<2>(&d.max_clusters[2]);
+            d.status = prepare_kernel<1, 1>(&d.max_clusters[0]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<2, 1>(&d.max_clusters[1]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2>(&d.max_clusters[2]);
         }
         if (d.status == GEMM_OK && g_encode == nullptr) {
             void *fn = nullptr;
@@ -128,11 +129,11 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
            K % 8 == 0;
 }
 
-template <int CG>
+template <int CG, int NC>
 int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
            const DeviceInfo &dev, int32_t max_clusters, int32_t raster_group, int64_t timeout_ns,
            uint32_t debug_flags, bool overlap) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, NC>;
     CUtensorMap tmA, tmB, tmBh, tmD;
     if (encode_map(&tmA, A, M, K, C::BLOCK_M) != GEMM_OK || encode_map(&tmB, B, N, K, C::B_ROWS) != GEMM_OK ||
         encode_map(&tmBh, B, N, K, C::B_ROWS / 2) != GEMM_OK || encode_map(&tmD, D, M, N, 32) != GEMM_OK) {
@@ -150,16 +151,17 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     p.num_tiles = static_cast<int32_t>(tiles);
     p.raster_group = raster_group > 0 ? raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
     p.debug_flags = debug_flags;
+    p.D = reinterpret_cast<uint16_t *>(D);
     p.timeout_ns = static_cast<uint64_t>(timeout_ns);
-    int64_t clusters = dev.max_clusters[CG];
+    int64_t clusters = dev.max_clusters[CG == 1 ? 0 : NC];
     if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
     p.split_from = split_point(p.num_tiles, static_cast<int32_t>(clusters));
     p.num_items = p.num_tiles + (p.num_tiles - p.split_from);
     if (clusters > p.num_items) clusters = p.num_items;
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
-        launch_config<CG>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr, overlap);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG>, tmA, tmB, tmBh, tmD, p);
+        launch_config<CG, NC>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr, overlap);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC>, tmA, tmB, tmBh, tmD, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -196,7 +198,10 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
     int64_t timeout_ns = kDefaultTimeoutNs;
     uint32_t debug_flags = 0;
     bool overlap = true;
+    int32_t consumers = 1;
     if (opts) {
+        if (opts->consumers < 0 || opts->consumers > 2) return GEMM_ERR_INVALID_ARG;
+        if (opts->consumers == 2) consumers = 2;
         if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
         if (opts->overlap_launch == -1) overlap = false;
         if (opts->cta_group != 0) cta_group = opts->cta_group;
@@ -210,6 +215,7 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
         if (opts->timeout_ns != 0) timeout_ns = opts->timeout_ns;
     }
     if (cta_group != 1 && cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    if (consumers == 2 && cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
     if (M == 0 || N == 0) return GEMM_OK;  // empty product: nothing to write
@@ -224,9 +230,13 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
     if (st != GEMM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_fill(D, M, N, s);
-    if (cta_group == 2) return launch<2>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags,
-                                          overlap);
-    return launch<1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
+    if (cta_group == 2 && consumers == 2) {
+        return launch<2, 2>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
+    }
+    if (cta_group == 2) {
+        return launch<2, 1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
+    }
+    return launch<1, 1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
 }
 
 int gemm_f16_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream) {
@@ -275,17 +285,19 @@ const char *gemm_f16_status_string(int status) {
     }
 }
 
-int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t raster_group,
-                         int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx,
-                         int64_t *n_off, int64_t *n_len) {
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers,
+                         int32_t raster_group, int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx,
+                         int64_t *n_idx, int64_t *n_off, int64_t *n_len) {
     if (cta_group == 0) cta_group = 2;
-    if ((cta_group != 1 && cta_group != 2) || raster_group < 0 || K < 0 || K > kDimLimit || M <= 0 || N <= 0 ||
+    if (consumers == 0) consumers = 1;
+    if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
+        (consumers == 2 && cta_group != 2) || raster_group < 0 || K < 0 || K > kDimLimit || M <= 0 || N <= 0 ||
         M > kDimLimit ||
         N > kDimLimit || num_clusters <= 0 || num_clusters > kDimLimit || cluster_id < 0 ||
         cluster_id >= num_clusters || iter < 0 || !m_idx || !n_idx || !n_off || !n_len) {
         return GEMM_ERR_INVALID_ARG;
     }
-    const int64_t tile_m = 128 * cta_group, tile_n = 256;
+    const int64_t tile_m = 128 * cta_group * consumers, tile_n = 256;
     const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
     const int64_t tiles = num_m * num_n;
     if (tiles > kDimLimit / 2) return GEMM_ERR_INVALID_ARG;
@@ -303,11 +315,14 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
     return 1;
 }
 
-int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int64_t n_off, int64_t n_len,
-                           int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row, int64_t *d_col) {
+int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int64_t m_idx, int64_t n_idx, int64_t n_off,
+                           int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row,
+                           int64_t *d_col) {
     if (cta_group == 0) cta_group = 2;
-    if ((cta_group != 1 && cta_group != 2) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
-        m_idx * 128 * cta_group > kDimLimit || n_idx * 256 > kDimLimit || !(n_len == 256 || n_len == 128) ||
+    if (consumers == 0) consumers = 1;
+    if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
+        (consumers == 2 && cta_group != 2) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
+        m_idx * 128 * cta_group * consumers > kDimLimit || n_idx * 256 > kDimLimit || !(n_len == 256 || n_len == 128) ||
         !(n_off == 0 || (n_len == 128 && n_off == 128)) || !a_row || !b_row || !d_row || !d_col) {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -316,7 +331,7 @@ int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int6
     w.n_idx = static_cast<int32_t>(n_idx);
     w.n_off = static_cast<int32_t>(n_off);
     w.n_len = static_cast<int32_t>(n_len);
-    const CtaOrigin o = cta_origin(w, cta_group, rank);
+    const CtaOrigin o = cta_origin(w, cta_group, rank, consumers);
     *a_row = o.a_row;
     *b_row = o.b_row;
     *d_row = o.d_row;

@@ -30,6 +30,16 @@
 // (cta_mask 0b11); tmem_empty[a] on the leader counts the epilogue warps of
 // both CTAs.
 //
+// Two MMA consumers (NC = 2, CG = 2; "GEMM III", Step 9; TIRx notes V9): the
+// cluster tile grows to 512 x 256.  Each stage holds two A blocks (one per
+// consumer, 256 rows apart) and one B block that both consumers read, so B
+// is loaded once for twice the math.  Consumer c accumulates into TMEM
+// columns [256c, 256c + 256); with all 512 columns taken there is no second
+// accumulator buffer, so the next tile waits for the epilogue to drain TMEM.
+// The CTA has three warpgroups: warps 0-1 as above (2-3 idle), warps 4-7
+// drain consumer 0 and warps 8-11 consumer 1.  Its epilogue writes D from
+// registers (the SMEM goes to four 48 KiB stages).
+//
 // Every wait is bounded: after `timeout_ns` the waiting role records an error
 // in the device status word, raises the CTA's abort flag and falls through to
 // teardown, so a protocol error ends the kernel instead of hanging the GPU.
@@ -48,28 +58,33 @@ __device__ unsigned long long g_info; // where it happened (role, CTA, tile seq)
 enum : int { kStatusTimeout = -7 };
 enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 
-template <int CG>
+template <int CG, int NC>
 struct Cfg {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
-    static constexpr int BLOCK_M = 128;                 // rows of D per CTA
+    static_assert(NC == 1 || (NC == 2 && CG == 2), "two consumers need a CTA pair");
+    static constexpr int BLOCK_M = 128;                 // rows of D per CTA and consumer
     static constexpr int BLOCK_N = 256;                 // columns of D per tile (MMA N)
     static constexpr int BLOCK_K = 64;                  // one 128-byte swizzle row of fp16
-    static constexpr int TILE_M = BLOCK_M * CG;         // rows of D per tile (MMA M)
+    static constexpr int MMA_M = BLOCK_M * CG;          // M of one tcgen05.mma (one consumer)
+    static constexpr int TILE_M = MMA_M * NC;           // rows of D per tile
     static constexpr int UMMA_K = 16;                   // K of one tcgen05.mma kind::f16
     static constexpr int B_ROWS = BLOCK_N / CG;         // rows of B each CTA loads
-    static constexpr int A_STAGE = BLOCK_M * BLOCK_K * 2;
+    static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
+    static constexpr int A_STAGE = A_BLOCK * NC;
     static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
-    static constexpr int STAGES = CG == 2 ? 6 : 4;
+    static constexpr int STAGES = NC == 2 ? 4 : (CG == 2 ? 6 : 4);
     static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
     static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
-    static constexpr int ACC_BUFS = 2;
-    static constexpr int TMEM_COLS = ACC_BUFS * BLOCK_N;            // 512: all of TMEM
-    static constexpr int EPI_WARPS = 4;
+    static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
+    static constexpr int TMEM_COLS = 512;                               // all of TMEM
+    static_assert(ACC_BUFS * NC * BLOCK_N == TMEM_COLS, "accumulators fill TMEM");
+    static constexpr int EPI_WARPS = 4 * NC;
+    static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
+    static constexpr bool EPI_DIRECT = NC == 2;         // store D from registers instead of via SMEM + TMA
     static constexpr int EPI_N = 64;                    // columns per epilogue chunk
-    static constexpr int EPI_CHUNKS = BLOCK_N / EPI_N;
-    static constexpr int EPI_BUFS = 2;
+    static constexpr int EPI_BUFS = EPI_DIRECT ? 0 : 2;
     static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
-    static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+    static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     // Shared-memory layout (offsets from a 1024-byte aligned base; identical
     // in both CTAs of a pair, which the pair MMA relies on).
     static constexpr int OFF_A = 0;
@@ -81,7 +96,7 @@ struct Cfg {
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;            // alignment slack
     static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KiB per-block shared memory limit");
-    static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0 && EPI_BUF % 1024 == 0, "1 KiB swizzle atoms");
+    static_assert(A_BLOCK % 1024 == 0 && B_STAGE % 1024 == 0 && EPI_BUF % 1024 == 0, "1 KiB swizzle atoms");
 };
 
 struct Params {
@@ -91,6 +106,7 @@ struct Params {
     int32_t raster_group;
     uint32_t debug_flags;
     uint64_t timeout_ns;
+    uint16_t *D;  // for the direct-store epilogue (row-major, ldd = N)
 };
 
 enum : uint32_t { kDebugProducerPhase0 = 1u };
@@ -130,12 +146,12 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
-template <int CG>
-__global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
+template <int CG, int NC>
+__global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
                        const Params p) {
-    using C = Cfg<CG>;
+    using C = Cfg<CG, NC>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -207,7 +223,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             bool ok = true;
             for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
                 const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from);
-                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank));
+                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
                 const bool half = w.n_len < C::BLOCK_N;
                 const CUtensorMap *mapB = half ? &tmBh : &tmB;
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
@@ -221,7 +237,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                     const int32_t k0 = kt * C::BLOCK_K;
                     if constexpr (CG == 2) {
                         const uint32_t full_leader = ptx::mapa(full, 0);
-                        ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE, &tmA, full_leader, k0, o.a_row);
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {  // consumer c's A rows lie c * MMA_M below
+                            ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK, &tmA, full_leader,
+                                                  k0, o.a_row + c * C::MMA_M);
+                        }
                         ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, mapB, full_leader, k0, o.b_row);
                     } else {
                         ptx::tma_load_2d(sA + ring.stage * C::A_STAGE, &tmA, full, k0, o.a_row);
@@ -240,8 +260,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (leader && ptx::elect_one()) {
-            constexpr uint32_t idesc_full = idesc_f16_f32(C::TILE_M, C::BLOCK_N);
-            constexpr uint32_t idesc_half = idesc_f16_f32(C::TILE_M, C::BLOCK_N / 2);
+            constexpr uint32_t idesc_full = idesc_f16_f32(C::MMA_M, C::BLOCK_N);
+            constexpr uint32_t idesc_half = idesc_f16_f32(C::MMA_M, C::BLOCK_N / 2);
             constexpr uint16_t pair_mask = CG == 2 ? 0x3 : 0x1;
             PipelineState ring(C::STAGES, 0u);
             PipelineState acc(C::ACC_BUFS, 1u);
@@ -255,7 +275,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                     break;
                 }
                 ptx::tcgen05_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * C::BLOCK_N);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * NC * C::BLOCK_N);
                 for (int kt = 0; kt < p.k_tiles; ++kt) {
                     if (!wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
                                       seq)) {
@@ -263,13 +283,18 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                         break;
                     }
                     ptx::tcgen05_fence_after();
-                    const uint64_t a_desc = ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE);
                     const uint64_t b_desc = ptx::smem_desc_k_sw128(sB + ring.stage * C::B_STAGE);
 #pragma unroll
-                    for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
-                        // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
-                        const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
-                        ptx::mma_f16<CG>(d_tmem, a_desc + koff, b_desc + koff, idesc, (kt | k) != 0 ? 1u : 0u);
+                    for (int c = 0; c < NC; ++c) {  // both consumers read the same B stage
+                        const uint64_t a_desc =
+                            ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK);
+#pragma unroll
+                        for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
+                            // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
+                            const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
+                            ptx::mma_f16<CG>(d_tmem + c * C::BLOCK_N, a_desc + koff, b_desc + koff, idesc,
+                                             (kt | k) != 0 ? 1u : 0u);
+                        }
                     }
                     ptx::mma_commit<CG>(bar_empty + 8 * ring.stage, pair_mask);  // stage free, both CTAs
                     ring.advance();
@@ -284,18 +309,19 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             wait_bounded(bar_drain, 0, abort_flag, p.timeout_ns, kRoleMma, 0xFFFFFFFFu, false);
         }
         __syncwarp();
-    } else {
+    } else if (warp >= C::EPI_WARP0) {
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 = rows of this warp
+        const int consumer = (warp - C::EPI_WARP0) / 4;
         const uint32_t stage_base = sD + static_cast<uint32_t>(quarter * C::EPI_BUFS * C::EPI_BUF);
         PipelineState acc(C::ACC_BUFS, 0u);
         uint32_t buf = 0;
         uint32_t seq = 0;
         for (int item = cluster; item < p.num_items; item += num_clusters, ++seq) {
             const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from);
-            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank));
+            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
             const int chunks = w.n_len / C::EPI_N;
-            const int32_t row0 = o.d_row + quarter * 32;
+            const int32_t row0 = o.d_row + consumer * C::MMA_M + quarter * 32;
             const int32_t col0 = o.d_col;
             bool ok = true;
             if (lane == 0) {
@@ -306,7 +332,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             if (!ok) break;
             ptx::tcgen05_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(acc.stage * C::BLOCK_N);
+                                   static_cast<uint32_t>((acc.stage * NC + consumer) * C::BLOCK_N);
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 uint32_t lo[32], hi[32];
@@ -338,9 +364,25 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                     const __half2 v = __floats2half2_rn(__uint_as_float(hi[2 * j]), __uint_as_float(hi[2 * j + 1]));
                     h[16 + j] = *reinterpret_cast<const uint32_t *>(&v);
                 }
+                if constexpr (C::EPI_DIRECT) {
+                    // Row `lane` of this warp: 64 columns = eight 16-byte stores
+                    // (N % 8 == 0, so a 16-byte unit is all in range or all out).
+                    const int32_t row = row0 + lane;
+                    const int32_t col = col0 + c * C::EPI_N;
+                    if (row < p.M) {
+                        uint16_t *dst = p.D + static_cast<int64_t>(row) * p.N + col;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            if (col + 8 * j < p.N) {
+                                ptx::st_global_v4(dst + 8 * j, h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                            }
+                        }
+                    }
+                    continue;
+                }
                 // The store issued from this buffer two chunks ago must have
                 // finished reading it.
-                if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
+                if (lane == 0) ptx::bulk_wait_group_read<(C::EPI_BUFS > 0 ? C::EPI_BUFS - 1 : 0)>();
                 __syncwarp();
                 // Row `lane` of the 32 x 64 staging tile, in the 128-byte
                 // swizzle the D tensor map expects: 16-byte unit j of row r

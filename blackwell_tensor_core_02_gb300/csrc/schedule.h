@@ -118,8 +118,10 @@ GEMM_HD int32_t split_point(int32_t num_tiles, int32_t clusters) {
 
 // Where one CTA of a work item reads and writes (TIRx notes V8, "Operand
 // Partition", "Output Ownership", "Epilogue Column Address").  An item covers
-// (128 * cg) rows x n_len columns of D.  CTA `rank` of the pair loads A rows
-// a_row .. +128 and B rows b_row .. +n_len/cg, and writes D rows d_row .. +128
+// (128 * cg * nc) rows x n_len columns of D, nc being the number of MMA
+// consumers (TIRx notes V9: two consumers stack their 128*cg rows along M).
+// CTA `rank` loads, for consumer c, A rows a_row + c*128*cg .. +128 and the
+// shared B rows b_row .. +n_len/cg, and writes D rows d_row + c*128*cg .. +128
 // over all n_len columns from d_col: the rank selects the A rows and the
 // output rows, and only the slice of B it loads, never the output columns.
 struct CtaOrigin {
@@ -129,9 +131,9 @@ struct CtaOrigin {
     int32_t d_col;
 };
 
-GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank) {
+GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank, int32_t nc = 1) {
     CtaOrigin o;
-    const int32_t m_base = w.m_idx * 128 * cg;
+    const int32_t m_base = w.m_idx * 128 * cg * nc;
     const int32_t n_base = w.n_idx * 256 + w.n_off;
     o.a_row = m_base + rank * 128;
     o.b_row = n_base + rank * (w.n_len / cg);

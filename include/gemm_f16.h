@@ -75,6 +75,12 @@ typedef enum gemm_status {
  *                 tail; the kernel still waits for it to finish, and for its
  *                 writes to be visible, before it reads A or B or writes D.
  *                 -1: an ordinary launch.  Other values: GEMM_ERR_INVALID_ARG.
+ *   consumers     0 or 1 (default): one MMA consumer per CTA pair, 256 x 256
+ *                 tiles, two accumulator buffers in tensor memory so the
+ *                 epilogue overlaps the next tile.  2 (needs cta_group 2):
+ *                 two consumers share each staged B tile, 512 x 256 tiles
+ *                 ("GEMM III", Step 9; TIRx notes V9), one accumulator per
+ *                 consumer.  Other values: GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;
@@ -83,7 +89,7 @@ typedef struct gemm_f16_options {
     int32_t debug_flags;
     int64_t timeout_ns;
     int32_t overlap_launch;
-    int32_t reserved;
+    int32_t consumers;
 } gemm_f16_options;
 
 /*
@@ -127,8 +133,8 @@ const char *gemm_f16_status_string(int status);
 
 /*
  * The persistent scheduler, as a pure host query (no CUDA call); the kernel
- * runs the same code.  D is cut into tiles of (128 * cta_group) rows x 256
- * columns, ordered in groups of `raster_group` M-tiles (0 = the shape-derived
+ * runs the same code.  D is cut into tiles of (128 * cta_group * consumers)
+ * rows x 256 columns (consumers 0 means 1), ordered in groups of `raster_group` M-tiles (0 = the shape-derived
  * default described under gemm_f16_options, which needs K): M fastest inside
  * a group, then N, then the next group (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters persistent clusters,
  * if the last wave is at most half full (T = qP + r, 0 < 2r <= P) its r tiles
@@ -140,24 +146,27 @@ const char *gemm_f16_status_string(int status);
  * (n_len 256, or 128 for a half) -- 0 if the cluster has no iter-th item, or
  * GEMM_ERR_INVALID_ARG for bad arguments.
  */
-int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t raster_group,
-                         int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx, int64_t *n_idx,
-                         int64_t *n_off, int64_t *n_len);
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers,
+                         int32_t raster_group, int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx,
+                         int64_t *n_idx, int64_t *n_off, int64_t *n_len);
 
 /*
  * Where CTA `rank` of a work item reads and writes, as a pure host query (no
  * CUDA call); the kernel uses the same function.  TIRx notes V8, "Operand
- * Partition" and "Output Ownership": with m_base = m_idx * 128 * cta_group and
- * n_base = n_idx * 256 + n_off, the CTA loads A rows a_row = m_base + 128 * rank
- * (128 rows) and B rows b_row = n_base + (n_len / cta_group) * rank (n_len /
- * cta_group rows), and writes D rows d_row = a_row (128 rows) over the n_len
- * columns starting at d_col = n_base ("Epilogue Column Address": no rank
- * term).  n_len is 256 (whole tile, n_off 0) or 128 (half tile, n_off 0 or
- * 128).  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not 0/1/2, rank
- * out of range, bad n_off/n_len, negative or too large indices, null outputs).
+ * Partition" and "Output Ownership": with m_base = m_idx * 128 * cta_group *
+ * consumers and n_base = n_idx * 256 + n_off, the CTA loads A rows a_row =
+ * m_base + 128 * rank (128 rows; consumer c's block lies c * 128 * cta_group
+ * rows further, TIRx notes V9) and B rows b_row = n_base + (n_len / cta_group)
+ * * rank (n_len / cta_group rows, shared by the consumers), and writes D rows
+ * d_row = a_row (128 rows per consumer) over the n_len columns starting at
+ * d_col = n_base ("Epilogue Column Address": no rank term).  n_len is 256 (whole tile, n_off 0) or 128 (half tile, n_off 0 or
+ * 128).  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not 0/1/2,
+ * consumers not 0/1/2 or 2 without a pair, rank out of range, bad
+ * n_off/n_len, negative or too large indices, null outputs).
  */
-int gemm_f16_nt_cta_origin(int32_t cta_group, int64_t m_idx, int64_t n_idx, int64_t n_off, int64_t n_len,
-                           int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row, int64_t *d_col);
+int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int64_t m_idx, int64_t n_idx, int64_t n_off,
+                           int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row,
+                           int64_t *d_col);
 
 /*
  * The stage/phase bookkeeping of one SMEM or TMEM ring, run on the host with

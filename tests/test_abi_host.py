@@ -73,7 +73,8 @@ def test_argument_errors_are_returned_before_any_launch():
     assert lib.gemm_f16_nt(None, None, None, 0, 128, 64, None) == OK
     assert lib.gemm_f16_nt(None, None, None, 128, 0, 64, None) == OK
     for bad in (g.Options(cta_group=3), g.Options(max_clusters=-1), g.Options(raster_group=-2),
-                g.Options(debug_flags=2), g.Options(timeout_ns=-5), g.Options(overlap_launch=2)):
+                g.Options(debug_flags=2), g.Options(timeout_ns=-5), g.Options(overlap_launch=2),
+                g.Options(consumers=3), g.Options(cta_group=1, consumers=2)):
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
 
@@ -95,10 +96,16 @@ def test_status_strings():
     (4096, 4096, 2, 8, 74), (4096, 4096, 2, 8, 76), (8192, 28672, 2, 8, 76), (4096, 4096, 1, 8, 148),
     (300, 520, 2, 8, 3), (1, 8, 1, 1, 1), (2560, 1280, 2, 3, 7), (1000, 7000, 1, 5, 13), (128, 128, 2, 8, 1),
     (128, 128, 2, 8, 76), (8192, 8192, 2, 8, 76), (1024, 1024, 2, 8, 5),
+    (4096, 4096, 4, 8, 76), (8192, 28672, 4, 0, 76), (640, 776, 4, 2, 7),
 ])
 def test_schedule_covers_every_output_once(M, N, cg, group, clusters):
-    """Every 128-column block of every tile is computed by exactly one work item."""
-    num_m = -(-M // (128 * cg))
+    """Every 128-column block of every tile is computed by exactly one work item.
+
+    cg = 4 stands for a CTA pair with two MMA consumers (512-row tiles).
+    """
+    consumers = 2 if cg == 4 else 1
+    cg = 2 if cg == 4 else cg
+    num_m = -(-M // (128 * cg * consumers))
     num_n = -(-N // 256)
     tiles = num_m * num_n
     cover = {}
@@ -106,7 +113,7 @@ def test_schedule_covers_every_output_once(M, N, cg, group, clusters):
     for c in range(clusters):
         it = 0
         while True:
-            w = g.schedule(M, N, cg, group, clusters, c, it)
+            w = g.schedule(M, N, cg, group, clusters, c, it, consumers=consumers)
             if w is None:
                 break
             m_idx, n_idx, n_off, n_len = w
@@ -170,6 +177,11 @@ def test_cta_origin_matches_the_pages_operand_partition():
     # a half tile keeps the same partition inside its 128 columns
     assert g.cta_origin(2, 1, 2, 1, n_off=128, n_len=128) == dict(a_row=384, b_row=704, d_row=384, d_col=640)
     assert g.cta_origin(1, 1, 2, 0, n_off=128, n_len=128) == dict(a_row=128, b_row=640, d_row=128, d_col=640)
+    # two consumers (TIRx notes V9): the tile is 512 rows; consumer 1's block of
+    # each CTA lies 256 rows below consumer 0's, B is shared
+    assert g.cta_origin(2, 1, 2, 1, consumers=2) == dict(a_row=640, b_row=640, d_row=640, d_col=512)
+    with pytest.raises(g.GemmError):
+        g.cta_origin(1, 0, 0, 0, consumers=2)
 
 
 def test_cta_origin_ownership_covers_each_output_once():

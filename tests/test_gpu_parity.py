@@ -48,67 +48,76 @@ def assert_close(gpu_f16, ref_bits, what=""):
                              f"gpu={got[i]!r} oracle={ref[i]!r}")
 
 
-def opts(g, cta_group=0, max_clusters=0):
-    return g.Options(cta_group=cta_group, max_clusters=max_clusters)
+# (cta_group, consumers): the CTA pair with one MMA consumer (the default),
+# a single CTA, and the pair with two consumers sharing each B stage.
+VARIANTS = [(2, 1), (1, 1), (2, 2)]
+VIDS = ["pair", "single", "pair-2consumers"]
+
+
+def opts(g, variant=(0, 0), max_clusters=0):
+    return g.Options(cta_group=variant[0], max_clusters=max_clusters, consumers=variant[1])
 
 
 # ----------------------------------------------------------- full compares --
 
-@pytest.mark.parametrize("cg", [2, 1])
+@pytest.mark.parametrize("v", VARIANTS, ids=VIDS)
 @pytest.mark.parametrize("name", ["single_tile_128x128x64", "ktile_grid_256x256x512"])
-def test_small_workloads_full(gpu_lib, name, cg):
+def test_small_workloads_full(gpu_lib, name, v):
     w = si.WORKLOADS[name]
     A, B = w.operands()
-    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg)), oracle.gemm_f16_nt(A, B), f"{name} cg={cg}")
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, v)), oracle.gemm_f16_nt(A, B), f"{name} {v}")
 
 
-@pytest.mark.parametrize("cg", [2, 1])
-def test_identity_operands_are_exact(gpu_lib, cg):
+@pytest.mark.parametrize("v", VARIANTS, ids=VIDS)
+def test_identity_operands_are_exact(gpu_lib, v):
     # One product per output element: the result is exact, so bit equality.
     # A = I (M = K = 384, 1.5 cluster tiles) gives D = Bᵀ; B = I gives D = A.
     rng = np.random.default_rng(21)
     K = 384
     B = rng.uniform(-2, 2, size=(520, K)).astype(np.float16)
-    D = run(gpu_lib, np.eye(K, dtype=np.float16), B, opts(gpu_lib, cg))
+    D = run(gpu_lib, np.eye(K, dtype=np.float16), B, opts(gpu_lib, v))
     assert np.array_equal(D.view(np.uint16), np.ascontiguousarray(B.T).view(np.uint16))
     A = rng.uniform(-2, 2, size=(200, K)).astype(np.float16)
-    D = run(gpu_lib, A, np.eye(K, dtype=np.float16), opts(gpu_lib, cg))
+    D = run(gpu_lib, A, np.eye(K, dtype=np.float16), opts(gpu_lib, v))
     assert np.array_equal(D.view(np.uint16), A.view(np.uint16))
 
 
 RAGGED = [(1, 8, 8), (200, 136, 72), (129, 264, 520), (383, 1032, 1000), (1000, 8, 64), (640, 776, 8)]
 
 
-@pytest.mark.parametrize("cg", [2, 1])
+@pytest.mark.parametrize("v", VARIANTS, ids=VIDS)
 @pytest.mark.parametrize("M,N,K", RAGGED)
-def test_ragged_shapes_full(gpu_lib, M, N, K, cg):
+def test_ragged_shapes_full(gpu_lib, M, N, K, v):
     w = si.custom(M, N, K, seed=M * 7 + N * 3 + K)
     A, B = w.operands()
-    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg)), oracle.gemm_f16_nt(A, B), f"{M}x{N}x{K} cg={cg}")
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, v)), oracle.gemm_f16_nt(A, B), f"{M}x{N}x{K} {v}")
 
 
-@pytest.mark.parametrize("cg,clusters", [(2, 1), (2, 3), (1, 1), (1, 5)])
-def test_few_persistent_clusters_run_many_tiles(gpu_lib, cg, clusters):
-    # 1024 x 1024 x 320: 16 (cg 2) or 32 (cg 1) tiles, so each persistent CTA
-    # runs several tiles and both rings wrap many times across tiles.
+@pytest.mark.parametrize("v,clusters", [((2, 1), 1), ((2, 1), 3), ((1, 1), 1), ((1, 1), 5), ((2, 2), 1), ((2, 2), 3)])
+def test_few_persistent_clusters_run_many_tiles(gpu_lib, v, clusters):
+    # 1024 x 1024 x 320: 16 (pair), 32 (single CTA) or 8 (two consumers)
+    # tiles, so each persistent CTA runs several tiles and both rings wrap many
+    # times across tiles.
     w = si.custom(1024, 1024, 320, seed=77)
     A, B = w.operands()
-    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg, clusters)), oracle.gemm_f16_nt(A, B),
-                 f"cg={cg} clusters={clusters}")
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, v, clusters)), oracle.gemm_f16_nt(A, B),
+                 f"{v} clusters={clusters}")
 
 
-@pytest.mark.parametrize("M,N,K,cg,clusters", [
-    (1024, 1024, 320, 2, 5),   # 16 tiles on 5 pairs: 15 whole + 1 split into halves
-    (1024, 1024, 320, 1, 30),  # 32 tiles on 30 CTAs: 2 split
-    (640, 776, 200, 2, 5),     # ragged N: a split half lies wholly past the last column
-    (256, 4096, 512, 2, 76),   # 16 tiles on 76 pairs: every tile split
-    (1024, 1024, 320, 2, 10),  # 16 % 10 = 6 > 10 / 2: no split
+@pytest.mark.parametrize("M,N,K,v,clusters", [
+    (1024, 1024, 320, (2, 1), 5),   # 16 tiles on 5 pairs: 15 whole + 1 split into halves
+    (1024, 1024, 320, (1, 1), 30),  # 32 tiles on 30 CTAs: 2 split
+    (640, 776, 200, (2, 1), 5),     # ragged N: a split half lies wholly past the last column
+    (256, 4096, 512, (2, 1), 76),   # 16 tiles on 76 pairs: every tile split
+    (1024, 1024, 320, (2, 1), 10),  # 16 % 10 = 6 > 10 / 2: no split
+    (1024, 1024, 320, (2, 2), 3),   # two consumers: 8 tiles on 3 pairs, 2 split
+    (640, 776, 200, (2, 2), 7),     # two consumers, ragged M and N, split halves past N
 ])
-def test_split_last_wave(gpu_lib, M, N, K, cg, clusters):
-    w = si.custom(M, N, K, seed=M + N + K + cg)
+def test_split_last_wave(gpu_lib, M, N, K, v, clusters):
+    w = si.custom(M, N, K, seed=M + N + K + v[0])
     A, B = w.operands()
-    assert_close(run(gpu_lib, A, B, opts(gpu_lib, cg, clusters)), oracle.gemm_f16_nt(A, B),
-                 f"split {M}x{N}x{K} cg={cg} clusters={clusters}")
+    assert_close(run(gpu_lib, A, B, opts(gpu_lib, v, clusters)), oracle.gemm_f16_nt(A, B),
+                 f"split {M}x{N}x{K} {v} clusters={clusters}")
 
 
 def test_guard_bands_and_full_overwrite(gpu_lib):
@@ -221,11 +230,13 @@ def _sample_indices(n, tile, count, rng):
     return np.array(sorted(idx))
 
 
+@pytest.mark.parametrize("consumers", [1, 2], ids=["default", "2consumers"])
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "mlp_proj_8192x28672x4096"])
-def test_full_size_workloads_sampled(gpu_lib, name):
+def test_full_size_workloads_sampled(gpu_lib, name, consumers):
     w = si.WORKLOADS[name]
     A, B = w.operands()
-    D = run(gpu_lib, A, B)  # default options: the launch configuration the benchmark times
+    # consumers 1: the default options, the launch configuration the benchmark times
+    D = run(gpu_lib, A, B, None if consumers == 1 else gpu_lib.Options(consumers=2))
     rng = np.random.default_rng(w.seed + 100)
     rows = _sample_indices(w.M, 128, 40, rng)
     cols = _sample_indices(w.N, 256, 40, rng)

@@ -20,13 +20,13 @@ pytestmark = pytest.mark.gpu
 TIMEOUT = -7
 
 
-@pytest.mark.parametrize("cg", [2, 1])
-def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg):
+@pytest.mark.parametrize("cg,consumers", [(2, 1), (1, 1), (2, 2)])
+def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg, consumers):
     w = si.WORKLOADS["ktile_grid_256x256x512"]
     A, B = w.operands()
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     D = torch.zeros((w.M, w.N), dtype=torch.float16, device="cuda")
-    bad = gpu_lib.Options(cta_group=cg, debug_flags=1, timeout_ns=100_000_000)  # 0.1 s per wait
+    bad = gpu_lib.Options(cta_group=cg, consumers=consumers, debug_flags=1, timeout_ns=100_000_000)  # 0.1 s a wait
     gpu_lib.gemm_f16_nt(dA, dB, D, options=bad)
     status, info = gpu_lib.last_device_status()
     assert status == TIMEOUT, gpu_lib.status_string(status)
@@ -34,7 +34,7 @@ def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg):
     # limit runs out first is recorded (producer 1, MMA issuer 2, epilogue 3)
     assert info >> 56 in (1, 2, 3)
     # a later, correct launch on the same context works and leaves the status clear
-    D2 = gpu_lib.gemm_f16_nt(dA, dB, options=gpu_lib.Options(cta_group=cg))
+    D2 = gpu_lib.gemm_f16_nt(dA, dB, options=gpu_lib.Options(cta_group=cg, consumers=consumers))
     assert gpu_lib.last_device_status()[0] == 0
     got = D2.cpu().numpy().astype(np.float64)
     ref = oracle.gemm_f16_nt(A, B).view(np.float16).astype(np.float64)
