@@ -228,6 +228,92 @@ def run_reference(args) -> None:
     }), flush=True)
 
 
+# ------------------------------------------------------ all five workloads --
+
+def survey_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float = 0.4) -> list[dict]:
+    """Each synthetic shape once: TFLOP/s, fraction of the tensor peak, and HBM GB/s of the
+    compulsory bytes (the figure that matters for the small, latency-bound shapes).
+
+    Inputs rotate over enough device copies that one pass through them exceeds
+    the 129 MB L2 (one copy when a single problem already does), so every
+    launch reads A and B from HBM.  The launches are captured once in a CUDA
+    graph and the graph is replayed, so the small shapes are timed on the
+    device, not by the host's launch rate.  cuBLAS (torch.matmul) runs the
+    same way on the same rotation as a reference point.
+    """
+    import torch
+
+    import oracle
+
+    torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+    out = []
+    stream = torch.cuda.Stream(dev)
+    for name in si.WORKLOAD_ORDER:
+        w = si.WORKLOADS[name]
+        A, B = (A3, B3) if (name == si.HEADLINE and A3 is not None) else w.operands()
+        rot = 1 if w.min_bytes > (256 << 20) else min(4096, -(-(256 << 20) // w.min_bytes))
+        with torch.cuda.stream(stream):
+            Ar = torch.from_numpy(A).to(dev).unsqueeze(0).repeat(rot, 1, 1)
+            Br = torch.from_numpy(B).to(dev).unsqueeze(0).repeat(rot, 1, 1)
+            Dr = torch.empty((rot, w.M, w.N), dtype=torch.float16, device=dev)
+        stream.synchronize()
+        sh = stream.cuda_stream
+
+        def ours(i):
+            j = i % rot
+            rc = g.gemm_f16_nt_ptr(Ar[j].data_ptr(), Br[j].data_ptr(), Dr[j].data_ptr(), w.M, w.N, w.K, sh)
+            if rc != 0:
+                raise g.GemmError(rc, f"gemm_f16_nt ({name})")
+
+        def cublas(i):
+            j = i % rot
+            with torch.cuda.stream(stream):
+                torch.matmul(Ar[j], Br[j].t(), out=Dr[j])
+
+        ours(0)
+        if g.last_device_status(stream)[0] != 0:
+            raise RuntimeError(f"device status after {name}")
+        rng = np.random.default_rng(7)
+        pr, pc = rng.integers(0, w.M, 256), rng.integers(0, w.N, 256)
+        ref = oracle.gemm_f16_nt_points(A, B, pr, pc).view(np.float16).astype(np.float64)
+        got = Dr[0].cpu().numpy()[pr, pc].astype(np.float64)
+        if not np.all(np.abs(got - ref) <= 2.0 ** -9 * np.abs(ref) + 1e-3):
+            raise RuntimeError(f"correctness guard failed for {name}")
+        per_graph = int(min(1000, max(10, budget_s / 4 / max(w.flop / 1.5e15, 3e-6))))
+        replays = 4
+        res = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "steps": per_graph * replays,
+               "rotated_copies": rot, "timing": "CUDA graph replay"}
+        for label, fn in (("ours", ours), ("cublas", cublas)):
+            for i in range(5):
+                fn(i)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                for i in range(per_graph):
+                    fn(i)
+            with torch.cuda.stream(stream):
+                graph.replay()  # warm-up replay
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(replays):
+                    graph.replay()
+                e1.record(stream)
+            e1.synchronize()
+            del graph
+            ms = e0.elapsed_time(e1) / (per_graph * replays)
+            tf = w.flop / (ms * 1e-3) / 1e12
+            if label == "ours":
+                res.update(ms_per_step=ms, tflops=tf, frac_of_peak=tf / peak,
+                           hbm_gbs_compulsory=w.min_bytes / (ms * 1e-3) / 1e9)
+            else:
+                res["cublas_tflops"] = tf
+        out.append(res)
+        del Ar, Br, Dr
+        torch.cuda.empty_cache()
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm --
 
 def run_ours(args) -> None:
@@ -389,6 +475,8 @@ def run_ours(args) -> None:
         }
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(A, B)
+        if world == 1 and not args.no_workloads:
+            line["workloads"] = survey_workloads(g, dev, peak, A, B)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -404,6 +492,7 @@ def main(argv=None) -> None:
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the pass over all five shapes")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

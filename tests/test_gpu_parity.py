@@ -219,6 +219,34 @@ def test_host_pipeline_end_to_end(gpu_lib):
     assert_close(single.numpy(), oracle.gemm_f16_nt(A, B), "single host call")
 
 
+def test_cuda_graph_capture_and_replay(gpu_lib):
+    # Launches captured in a CUDA graph (after a first eager call has done the
+    # per-device set-up) replay correctly, including a GEMM that reads the
+    # previous one's output through the overlapped launch.
+    w = si.custom(384, 512, 256, seed=51)
+    A, B = w.operands()
+    C = si.custom(256, 8, 512, seed=52, dist=si.Dist("uniform", -0.125, 0.125)).operands()[0]
+    dA, dB, dC = to_dev(A), to_dev(B), to_dev(C)
+    D1 = torch.empty((384, 512), dtype=torch.float16, device="cuda")
+    D2 = torch.empty((384, 256), dtype=torch.float16, device="cuda")
+    gpu_lib.gemm_f16_nt(dA, dB, D1)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s, capture_error_mode="thread_local"):
+        gpu_lib.gemm_f16_nt(dA, dB, D1, stream=s)
+        gpu_lib.gemm_f16_nt(D1, dC, D2, stream=s)
+    for _ in range(3):
+        D1.fill_(float("nan"))
+        D2.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert gpu_lib.last_device_status()[0] == 0
+        D1h = D1.cpu().numpy()
+        assert_close(D1h, oracle.gemm_f16_nt(A, B), "graph first")
+        assert_close(D2.cpu().numpy(), oracle.gemm_f16_nt(D1h, C), "graph second")
+
+
 # ------------------------------------------------ full-size, sampled compares --
 
 def _sample_indices(n, tile, count, rng):
