@@ -406,7 +406,10 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
             }
             acc.advance();
         }
-        if (lane == 0) ptx::bulk_wait_group<0>();
+        // The staging buffers must stay valid until the last stores have read
+        // them; the stores' writes to D complete with the grid (and a
+        // dependent launch's griddepcontrol.wait orders after them).
+        if (lane == 0) ptx::bulk_wait_group_read<0>();
         __syncwarp();
     }
 
