@@ -19,7 +19,7 @@ from . import build as _build
 
 __all__ = [
     "GemmError", "Options", "load", "gemm_f16_nt", "gemm_f16_nt_ptr", "gemm_f16_nt_supported",
-    "gemm_f16_nt_host", "HostPipeline", "last_device_status", "status_string", "schedule", "cta_origin", "pipeline_trace", "STATUS",
+    "gemm_f16_nt_host", "HostPipeline", "workspace_size", "WorkItem", "last_device_status", "status_string", "schedule", "cta_origin", "pipeline_trace", "STATUS",
 ]
 
 STATUS = {
@@ -33,6 +33,11 @@ class GemmError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
         super().__init__(f"{where}: {status_string(code)} ({code})")
+
+
+class WorkItem(ctypes.Structure):
+    """Mirror of ``gemm_f16_work_item``."""
+    _fields_ = [(n, ctypes.c_int64) for n in ("m_idx", "n_idx", "n_off", "n_len", "slice", "kt_begin", "kt_end")]
 
 
 class Options(ctypes.Structure):
@@ -66,10 +71,14 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_last_device_status.restype = ctypes.c_int
         lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
         lib.gemm_f16_status_string.restype = ctypes.c_char_p
-        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i64, i64, i64, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i64, i64, i64, ctypes.POINTER(WorkItem)]
         lib.gemm_f16_nt_schedule.restype = ctypes.c_int
         lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
+        lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, vp, ctypes.POINTER(Options)]
+        lib.gemm_f16_nt_ws.restype = ctypes.c_int
+        lib.gemm_f16_nt_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Options)]
+        lib.gemm_f16_nt_workspace_size.restype = ctypes.c_int64
         lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
         lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
         _lib = lib
@@ -95,16 +104,50 @@ def _stream_handle(stream) -> int | None:
 
 
 def gemm_f16_nt_ptr(A_ptr: int, B_ptr: int, D_ptr: int, M: int, N: int, K: int, stream: int | None = 0,
-                    options: Options | None = None) -> int:
-    """Raw C-ABI call with device pointers; returns the status code (no raise)."""
+                    options: Options | None = None, workspace_ptr: int | None = None, workspace_bytes: int = 0) -> int:
+    """Raw C-ABI call with device pointers; returns the status code (no raise).
+
+    With a workspace the call goes through ``gemm_f16_nt_ws`` (split-K allowed)."""
     lib = load()
+    if workspace_ptr is not None:
+        return lib.gemm_f16_nt_ws(A_ptr, B_ptr, D_ptr, M, N, K, workspace_ptr, workspace_bytes, stream,
+                                  ctypes.byref(options) if options is not None else None)
     if options is None:
         return lib.gemm_f16_nt(A_ptr, B_ptr, D_ptr, M, N, K, stream)
     return lib.gemm_f16_nt_ex(A_ptr, B_ptr, D_ptr, M, N, K, stream, ctypes.byref(options))
 
 
-def gemm_f16_nt(A, B, D=None, *, stream=None, options: Options | None = None):
-    """D = A·Bᵀ for fp16 CUDA tensors A (M×K) and B (N×K); returns D (M×N)."""
+def workspace_size(M: int, N: int, K: int, options: Options | None = None) -> int:
+    """Bytes of split-K workspace gemm_f16_nt_ws would use on the current device (0: no split)."""
+    rc = load().gemm_f16_nt_workspace_size(M, N, K, ctypes.byref(options) if options is not None else None)
+    if rc < 0:
+        raise GemmError(int(rc), "gemm_f16_nt_workspace_size")
+    return int(rc)
+
+
+_workspaces: dict = {}
+
+
+def _workspace_for(nbytes: int, device, stream):
+    """A cached device buffer of at least `nbytes` for this device and stream (torch's allocator)."""
+    import torch
+
+    key = (device.index if device.index is not None else torch.cuda.current_device(), stream)
+    buf = _workspaces.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        _workspaces[key] = buf
+    return buf
+
+
+def gemm_f16_nt(A, B, D=None, *, stream=None, options: Options | None = None, workspace=True):
+    """D = A·Bᵀ for fp16 CUDA tensors A (M×K) and B (N×K); returns D (M×N).
+
+    With ``workspace=True`` (default) a cached device buffer per device and
+    stream is passed, so that few-tile problems may split their K-loop
+    (``gemm_f16_nt_ws``); ``False`` calls ``gemm_f16_nt_ex`` without one; a
+    uint8 CUDA tensor uses that buffer.
+    """
     import torch
 
     if A.dtype != torch.float16 or B.dtype != torch.float16:
@@ -120,7 +163,16 @@ def gemm_f16_nt(A, B, D=None, *, stream=None, options: Options | None = None):
     elif D.dtype != torch.float16 or tuple(D.shape) != (M, N) or not D.is_contiguous() or not D.is_cuda:
         raise ValueError("D must be a contiguous fp16 CUDA tensor of shape (M, N)")
     with torch.cuda.device(A.device):
-        rc = gemm_f16_nt_ptr(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, _stream_handle(stream), options)
+        sh = _stream_handle(stream)
+        ws_ptr, ws_bytes = None, 0
+        if workspace is True:
+            need = workspace_size(M, N, K, options)
+            if need > 0:
+                buf = _workspace_for(need, A.device, sh)
+                ws_ptr, ws_bytes = buf.data_ptr(), buf.numel()
+        elif workspace is not False and workspace is not None:
+            ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+        rc = gemm_f16_nt_ptr(A.data_ptr(), B.data_ptr(), D.data_ptr(), M, N, K, sh, options, ws_ptr, ws_bytes)
     if rc != 0:
         raise GemmError(rc, "gemm_f16_nt")
     return D
@@ -238,14 +290,15 @@ def last_device_status(stream=None) -> tuple[int, int]:
 
 
 def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
-             it: int, K: int = 4096, consumers: int = 1):
-    """The iter-th work item (m_idx, n_idx, n_off, n_len) of one cluster, or None when it has no more."""
-    out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, raster_group, num_clusters, cluster_id, it,
-                                     *[ctypes.byref(o) for o in out])
+             it: int, K: int = 4096, consumers: int = 1, split_k: int = 0):
+    """The iter-th work item of one cluster as (m_idx, n_idx, n_off, n_len, slice, kt_begin, kt_end),
+    or None when it has no more."""
+    w = WorkItem()
+    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, raster_group, split_k, num_clusters, cluster_id,
+                                     it, ctypes.byref(w))
     if rc < 0:
         raise GemmError(rc, "gemm_f16_nt_schedule")
-    return tuple(o.value for o in out) if rc == 1 else None
+    return tuple(getattr(w, f) for f, _ in WorkItem._fields_) if rc == 1 else None
 
 
 def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int, n_off: int = 0, n_len: int = 256,

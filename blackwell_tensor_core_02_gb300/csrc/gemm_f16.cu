@@ -124,22 +124,69 @@ int encode_map(CUtensorMap *map, const void *ptr, int64_t rows, int64_t cols, ui
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// The split-K workspace viewed as [slices][M][N] fp32, stored in 32 x 32 boxes
+// with the 128-byte swizzle (each box row is 32 fp32 = 128 bytes).
+int encode_partial_map(CUtensorMap *map, void *ptr, int64_t slices, int64_t M, int64_t N) {
+    cuuint64_t gdim[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(slices)};
+    cuuint64_t gstride[2] = {static_cast<cuuint64_t>(N) * 4, static_cast<cuuint64_t>(M) * N * 4};
+    cuuint32_t box[3] = {32u, 32u, 1u};
+    cuuint32_t estride[3] = {1u, 1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, gdim, gstride, box, estride,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
 bool shape_ok(int64_t M, int64_t N, int64_t K) {
     return M >= 0 && N >= 0 && K >= 0 && M <= kDimLimit && N <= kDimLimit && K <= kDimLimit && N % 8 == 0 &&
            K % 8 == 0;
 }
 
-template <int CG, int NC>
-int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
-           const DeviceInfo &dev, int32_t max_clusters, int32_t raster_group, int64_t timeout_ns,
-           uint32_t debug_flags, bool overlap) {
-    using C = Cfg<CG, NC>;
-    CUtensorMap tmA, tmB, tmBh, tmD;
-    if (encode_map(&tmA, A, M, K, C::BLOCK_M) != GEMM_OK || encode_map(&tmB, B, N, K, C::B_ROWS) != GEMM_OK ||
-        encode_map(&tmBh, B, N, K, C::B_ROWS / 2) != GEMM_OK || encode_map(&tmD, D, M, N, 32) != GEMM_OK) {
-        return GEMM_ERR_CUDA;
+struct Opts {
+    int32_t cta_group = 2;
+    int32_t consumers = 1;
+    int32_t max_clusters = 0;
+    int32_t raster_group = 0;
+    int64_t timeout_ns = kDefaultTimeoutNs;
+    uint32_t debug_flags = 0;
+    bool overlap = true;
+};
+
+int parse_options(const gemm_f16_options *opts, Opts *o) {
+    if (opts) {
+        if (opts->consumers < 0 || opts->consumers > 2) return GEMM_ERR_INVALID_ARG;
+        if (opts->consumers == 2) o->consumers = 2;
+        if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
+        if (opts->overlap_launch == -1) o->overlap = false;
+        if (opts->cta_group != 0) o->cta_group = opts->cta_group;
+        if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
+            (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
+            return GEMM_ERR_INVALID_ARG;
+        }
+        o->debug_flags = static_cast<uint32_t>(opts->debug_flags);
+        o->max_clusters = opts->max_clusters;
+        o->raster_group = opts->raster_group;
+        if (opts->timeout_ns != 0) o->timeout_ns = opts->timeout_ns;
     }
+    if (o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    if (o->consumers == 2 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
+    return GEMM_OK;
+}
+
+// Everything about one launch that follows from the shape, the options and
+// the device: tile counts, scheduler parameters, split-K slices, grid size.
+struct Plan {
     Params p;
+    int64_t clusters;          // persistent clusters launched
+    int64_t workspace_bytes;   // split-K partials, 0 without split-K
+};
+
+template <int CG, int NC>
+int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o, bool allow_splitk,
+              Plan *out) {
+    using C = Cfg<CG, NC>;
+    Params &p = out->p;
+    p = Params{};
     p.M = static_cast<int32_t>(M);
     p.N = static_cast<int32_t>(N);
     p.K = static_cast<int32_t>(K);
@@ -147,26 +194,137 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     p.num_n_tiles = static_cast<int32_t>((N + C::BLOCK_N - 1) / C::BLOCK_N);
     p.k_tiles = static_cast<int32_t>((K + C::BLOCK_K - 1) / C::BLOCK_K);
     const int64_t tiles = static_cast<int64_t>(p.num_m_tiles) * p.num_n_tiles;
-    if (tiles > kDimLimit) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (tiles > kDimLimit / 16) return GEMM_ERR_UNSUPPORTED_SHAPE;
     p.num_tiles = static_cast<int32_t>(tiles);
-    p.raster_group = raster_group > 0 ? raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
-    p.debug_flags = debug_flags;
-    p.D = reinterpret_cast<uint16_t *>(D);
-    p.timeout_ns = static_cast<uint64_t>(timeout_ns);
+    p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
+    p.debug_flags = o.debug_flags;
+    p.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
     int64_t clusters = dev.max_clusters[CG == 1 ? 0 : NC];
-    if (max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
-    p.split_from = split_point(p.num_tiles, static_cast<int32_t>(clusters));
-    p.num_items = p.num_tiles + (p.num_tiles - p.split_from);
+    if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
+    p.slices = (allow_splitk && NC == 1) ? splitk_slices(p.num_tiles, static_cast<int32_t>(clusters), p.k_tiles) : 1;
+    if (p.slices > kMaxSlices) p.slices = kMaxSlices;
+    if (p.slices > 1) {
+        p.split_from = p.num_tiles;
+        p.num_items = p.num_tiles * p.slices;
+        out->workspace_bytes = static_cast<int64_t>(p.slices) * M * N * static_cast<int64_t>(sizeof(float));
+    } else {
+        p.split_from = split_point(p.num_tiles, static_cast<int32_t>(clusters));
+        p.num_items = p.num_tiles + (p.num_tiles - p.split_from);
+        out->workspace_bytes = 0;
+    }
     if (clusters > p.num_items) clusters = p.num_items;
+    out->clusters = clusters;
+    return GEMM_OK;
+}
+
+template <int S>
+cudaError_t launch_reduce_s(const cudaLaunchConfig_t *cfg, const float *partial, uint16_t *D, int64_t mn) {
+    return cudaLaunchKernelEx(cfg, splitk_reduce_kernel<S>, partial, D, mn);
+}
+
+cudaError_t launch_reduce(const cudaLaunchConfig_t *cfg, int slices, const float *partial, uint16_t *D, int64_t mn) {
+    switch (slices) {
+        case 4: return launch_reduce_s<4>(cfg, partial, D, mn);
+        case 5: return launch_reduce_s<5>(cfg, partial, D, mn);
+        case 6: return launch_reduce_s<6>(cfg, partial, D, mn);
+        case 7: return launch_reduce_s<7>(cfg, partial, D, mn);
+        case 8: return launch_reduce_s<8>(cfg, partial, D, mn);
+        case 9: return launch_reduce_s<9>(cfg, partial, D, mn);
+        case 10: return launch_reduce_s<10>(cfg, partial, D, mn);
+        case 11: return launch_reduce_s<11>(cfg, partial, D, mn);
+        case 12: return launch_reduce_s<12>(cfg, partial, D, mn);
+        case 13: return launch_reduce_s<13>(cfg, partial, D, mn);
+        case 14: return launch_reduce_s<14>(cfg, partial, D, mn);
+        case 15: return launch_reduce_s<15>(cfg, partial, D, mn);
+        case 16: return launch_reduce_s<16>(cfg, partial, D, mn);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int CG, int NC>
+int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
+           const DeviceInfo &dev, const Opts &o, void *workspace, int64_t workspace_bytes) {
+    using C = Cfg<CG, NC>;
+    Plan plan;
+    int st = make_plan<CG, NC>(M, N, K, dev, o, workspace != nullptr, &plan);
+    if (st != GEMM_OK) return st;
+    if (plan.p.slices > 1 && (workspace_bytes < plan.workspace_bytes ||
+                              (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)) {
+        st = make_plan<CG, NC>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
+        if (st != GEMM_OK) return st;
+    }
+    Params &p = plan.p;
+    CUtensorMap tmA, tmB, tmBh, tmD;
+    if (encode_map(&tmA, A, M, K, C::BLOCK_M) != GEMM_OK || encode_map(&tmB, B, N, K, C::B_ROWS) != GEMM_OK ||
+        encode_map(&tmBh, B, N, K, C::B_ROWS / 2) != GEMM_OK || encode_map(&tmD, D, M, N, 32) != GEMM_OK) {
+        return GEMM_ERR_CUDA;
+    }
+    p.D = reinterpret_cast<uint16_t *>(D);
+    p.partial = p.slices > 1 ? reinterpret_cast<float *>(workspace) : nullptr;
+    CUtensorMap tmP;
+    if (p.slices > 1) {
+        if (encode_partial_map(&tmP, workspace, p.slices, M, N) != GEMM_OK) return GEMM_ERR_CUDA;
+    } else {
+        tmP = tmD;  // unused without split-K
+    }
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
-        launch_config<CG, NC>(dim3(static_cast<unsigned>(clusters * CG), 1, 1), stream, attr, overlap);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC>, tmA, tmB, tmBh, tmD, p);
+        launch_config<CG, NC>(dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1), stream, attr, o.overlap);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC>, tmA, tmB, tmBh, tmD, tmP, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
+    if (p.slices > 1) {
+        // second pass: add the slices' partials and round once (its CTAs may
+        // start early; griddepcontrol.wait orders it after the GEMM)
+        const int64_t units = M * N / 4;
+        int64_t blocks = (units + 255) / 256;
+        if (blocks > 8 * dev.sm_count) blocks = 8 * dev.sm_count;
+        if (blocks < 1) blocks = 1;
+        cudaLaunchConfig_t rcfg = {};
+        rcfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+        rcfg.blockDim = dim3(256, 1, 1);
+        rcfg.stream = stream;
+        cudaLaunchAttribute rattr[1];
+        rattr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        rattr[0].val.programmaticStreamSerializationAllowed = 1;
+        rcfg.attrs = rattr;
+        rcfg.numAttrs = 1;
+        e = launch_reduce(&rcfg, p.slices, static_cast<const float *>(p.partial), reinterpret_cast<uint16_t *>(D),
+                          M * N);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_LAUNCH;
+        }
+    }
     return GEMM_OK;
+}
+
+int zero_fill(void *D, int64_t M, int64_t N, cudaStream_t stream);
+
+int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
+        const gemm_f16_options *opts, void *workspace, int64_t workspace_bytes) {
+    Opts o;
+    int st = parse_options(opts, &o);
+    if (st != GEMM_OK) return st;
+    if (M < 0 || N < 0 || K < 0 || workspace_bytes < 0) return GEMM_ERR_INVALID_ARG;
+    if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return GEMM_OK;  // empty product: nothing to write
+    if (!D || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(D) & 15u) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) ||
+                                                             (reinterpret_cast<uintptr_t>(B) & 15u)))) {
+        return GEMM_ERR_MISALIGNED;
+    }
+    int dev = -1;
+    DeviceInfo *info = nullptr;
+    st = device_setup(&dev, &info);
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_fill(D, M, N, s);
+    if (o.cta_group == 2 && o.consumers == 2) return launch<2, 2>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+    if (o.cta_group == 2) return launch<2, 1>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
+    return launch<1, 1>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
 }
 
 int zero_fill(void *D, int64_t M, int64_t N, cudaStream_t stream) {
@@ -194,53 +352,35 @@ int gemm_f16_nt_supported(int64_t M, int64_t N, int64_t K) { return shape_ok(M, 
 
 int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
                    const gemm_f16_options *opts) {
-    int32_t cta_group = 2, max_clusters = 0, raster_group = 0;
-    int64_t timeout_ns = kDefaultTimeoutNs;
-    uint32_t debug_flags = 0;
-    bool overlap = true;
-    int32_t consumers = 1;
-    if (opts) {
-        if (opts->consumers < 0 || opts->consumers > 2) return GEMM_ERR_INVALID_ARG;
-        if (opts->consumers == 2) consumers = 2;
-        if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
-        if (opts->overlap_launch == -1) overlap = false;
-        if (opts->cta_group != 0) cta_group = opts->cta_group;
-        if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
-            (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
-            return GEMM_ERR_INVALID_ARG;
-        }
-        debug_flags = static_cast<uint32_t>(opts->debug_flags);
-        max_clusters = opts->max_clusters;
-        raster_group = opts->raster_group;
-        if (opts->timeout_ns != 0) timeout_ns = opts->timeout_ns;
-    }
-    if (cta_group != 1 && cta_group != 2) return GEMM_ERR_INVALID_ARG;
-    if (consumers == 2 && cta_group != 2) return GEMM_ERR_INVALID_ARG;
-    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
-    if (M == 0 || N == 0) return GEMM_OK;  // empty product: nothing to write
-    if (!D || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(D) & 15u) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) ||
-                                                             (reinterpret_cast<uintptr_t>(B) & 15u)))) {
-        return GEMM_ERR_MISALIGNED;
-    }
-    int dev = -1;
-    DeviceInfo *info = nullptr;
-    const int st = device_setup(&dev, &info);
-    if (st != GEMM_OK) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (K == 0) return zero_fill(D, M, N, s);
-    if (cta_group == 2 && consumers == 2) {
-        return launch<2, 2>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
-    }
-    if (cta_group == 2) {
-        return launch<2, 1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
-    }
-    return launch<1, 1>(A, B, D, M, N, K, s, *info, max_clusters, raster_group, timeout_ns, debug_flags, overlap);
+    return run(A, B, D, M, N, K, stream, opts, nullptr, 0);
 }
 
 int gemm_f16_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream) {
-    return gemm_f16_nt_ex(A, B, D, M, N, K, stream, nullptr);
+    return run(A, B, D, M, N, K, stream, nullptr, nullptr, 0);
+}
+
+int gemm_f16_nt_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *workspace,
+                   int64_t workspace_bytes, void *stream, const gemm_f16_options *opts) {
+    if (!workspace && workspace_bytes != 0) return GEMM_ERR_INVALID_ARG;
+    return run(A, B, D, M, N, K, stream, opts, workspace, workspace_bytes);
+}
+
+int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts) {
+    Opts o;
+    int st = parse_options(opts, &o);
+    if (st != GEMM_OK) return st;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0 || K == 0 || o.consumers == 2) return 0;
+    int dev = -1;
+    DeviceInfo *info = nullptr;
+    st = device_setup(&dev, &info);
+    if (st != GEMM_OK) return st;
+    Plan plan;
+    st = o.cta_group == 2 ? make_plan<2, 1>(M, N, K, *info, o, true, &plan)
+                          : make_plan<1, 1>(M, N, K, *info, o, true, &plan);
+    if (st != GEMM_OK) return st;
+    return plan.workspace_bytes;
 }
 
 int gemm_f16_last_device_status(void *stream, uint64_t *info) {
@@ -286,32 +426,45 @@ const char *gemm_f16_status_string(int status) {
 }
 
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers,
-                         int32_t raster_group, int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx,
-                         int64_t *n_idx, int64_t *n_off, int64_t *n_len) {
+                         int32_t raster_group, int32_t split_k, int64_t num_clusters, int64_t cluster_id, int64_t iter,
+                         gemm_f16_work_item *out) {
     if (cta_group == 0) cta_group = 2;
     if (consumers == 0) consumers = 1;
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
-        (consumers == 2 && cta_group != 2) || raster_group < 0 || K < 0 || K > kDimLimit || M <= 0 || N <= 0 ||
-        M > kDimLimit ||
-        N > kDimLimit || num_clusters <= 0 || num_clusters > kDimLimit || cluster_id < 0 ||
-        cluster_id >= num_clusters || iter < 0 || !m_idx || !n_idx || !n_off || !n_len) {
+        (consumers == 2 && cta_group != 2) || raster_group < 0 || (split_k != 0 && split_k != 1) || K < 0 ||
+        K > kDimLimit || M <= 0 || N <= 0 || M > kDimLimit || N > kDimLimit || num_clusters <= 0 ||
+        num_clusters > kDimLimit || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !out) {
         return GEMM_ERR_INVALID_ARG;
     }
     const int64_t tile_m = 128 * cta_group * consumers, tile_n = 256;
     const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
     const int64_t tiles = num_m * num_n;
-    if (tiles > kDimLimit / 2) return GEMM_ERR_INVALID_ARG;
+    if (tiles > kDimLimit / 16) return GEMM_ERR_INVALID_ARG;
+    const int32_t k_tiles = static_cast<int32_t>((K + 63) / 64);
     if (raster_group == 0) raster_group = auto_raster_group(static_cast<int32_t>(num_m), K, static_cast<int32_t>(tile_m));
-    const int32_t split_from = split_point(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters));
-    const int64_t items = tiles + (tiles - split_from);
+    const int32_t slices = (split_k && consumers == 1)
+                               ? splitk_slices(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters), k_tiles)
+                               : 1;
+    int32_t split_from;
+    int64_t items;
+    if (slices > 1) {
+        split_from = static_cast<int32_t>(tiles);
+        items = tiles * slices;
+    } else {
+        split_from = split_point(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters));
+        items = tiles + (tiles - split_from);
+    }
     const int64_t item = cluster_id + iter * num_clusters;
     if (item >= items) return 0;
-    const WorkItem w = work_of(static_cast<int32_t>(item), static_cast<int32_t>(num_m),
-                               static_cast<int32_t>(num_n), raster_group, split_from);
-    *m_idx = w.m_idx;
-    *n_idx = w.n_idx;
-    *n_off = w.n_off;
-    *n_len = w.n_len;
+    const WorkItem w = work_of(static_cast<int32_t>(item), static_cast<int32_t>(num_m), static_cast<int32_t>(num_n),
+                               raster_group, split_from, k_tiles, slices);
+    out->m_idx = w.m_idx;
+    out->n_idx = w.n_idx;
+    out->n_off = w.n_off;
+    out->n_len = w.n_len;
+    out->slice = w.slice;
+    out->kt_begin = w.kt_begin;
+    out->kt_end = w.kt_end;
     return 1;
 }
 

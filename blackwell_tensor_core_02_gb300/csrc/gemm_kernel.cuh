@@ -40,6 +40,11 @@
 // drain consumer 0 and warps 8-11 consumer 1.  Its epilogue writes D from
 // registers (the SMEM goes to four 48 KiB stages).
 //
+// Split-K (NC = 1): with very few tiles, item t*S + s runs K slice s of tile
+// t and its epilogue writes the fp32 partial sum of that slice to a workspace
+// [S][M][N]; splitk_reduce_kernel then adds the S partials in fp32 and rounds
+// once to fp16 (the sum is still accumulated in fp32 and rounded once).
+//
 // Every wait is bounded: after `timeout_ns` the waiting role records an error
 // in the device status word, raises the CTA's abort flag and falls through to
 // teardown, so a protocol error ends the kernel instead of hanging the GPU.
@@ -103,10 +108,12 @@ struct Params {
     int32_t M, N, K;
     int32_t num_m_tiles, num_n_tiles, k_tiles, num_tiles;
     int32_t num_items, split_from;  // work items; items from split_from on are half tiles
+    int32_t slices;                 // split-K slices (1: none)
     int32_t raster_group;
     uint32_t debug_flags;
     uint64_t timeout_ns;
-    uint16_t *D;  // for the direct-store epilogue (row-major, ldd = N)
+    uint16_t *D;       // for the direct-store epilogue (row-major, ldd = N)
+    float *partial;    // split-K workspace [slices][M][N] fp32, when slices > 1
 };
 
 enum : uint32_t { kDebugProducerPhase0 = 1u };
@@ -150,7 +157,7 @@ template <int CG, int NC>
 __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
-                       const Params p) {
+                       const __grid_constant__ CUtensorMap tmP, const Params p) {
     using C = Cfg<CG, NC>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
@@ -181,6 +188,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
         ptx::prefetch_tensormap(&tmB);
         ptx::prefetch_tensormap(&tmBh);
         ptx::prefetch_tensormap(&tmD);
+        if (p.slices > 1) ptx::prefetch_tensormap(&tmP);
         for (int s = 0; s < C::STAGES; ++s) {
             ptx::mbar_init(bar_full + 8 * s, 1);
             ptx::mbar_init(bar_empty + 8 * s, 1);
@@ -222,11 +230,12 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
             uint32_t seq = 0;
             bool ok = true;
             for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
-                const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from);
+                const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
+                                           p.k_tiles, p.slices);
                 const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
                 const bool half = w.n_len < C::BLOCK_N;
                 const CUtensorMap *mapB = half ? &tmBh : &tmB;
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
                     if (!wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
                                       kRoleProducer, seq)) {
                         ok = false;
@@ -268,7 +277,9 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
             uint32_t seq = 0;
             bool ok = true;
             for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
-                const uint32_t idesc = item >= p.split_from ? idesc_half : idesc_full;
+                const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
+                                           p.k_tiles, p.slices);
+                const uint32_t idesc = w.n_len < C::BLOCK_N ? idesc_half : idesc_full;
                 if (!wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
                                   seq)) {
                     ok = false;
@@ -276,7 +287,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
                 }
                 ptx::tcgen05_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * NC * C::BLOCK_N);
-                for (int kt = 0; kt < p.k_tiles; ++kt) {
+                for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
                     if (!wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
                                       seq)) {
                         ok = false;
@@ -293,7 +304,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
                             // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
                             const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
                             ptx::mma_f16<CG>(d_tmem + c * C::BLOCK_N, a_desc + koff, b_desc + koff, idesc,
-                                             (kt | k) != 0 ? 1u : 0u);
+                                             (kt != w.kt_begin || k != 0) ? 1u : 0u);
                         }
                     }
                     ptx::mma_commit<CG>(bar_empty + 8 * ring.stage, pair_mask);  // stage free, both CTAs
@@ -318,7 +329,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
         uint32_t buf = 0;
         uint32_t seq = 0;
         for (int item = cluster; item < p.num_items; item += num_clusters, ++seq) {
-            const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from);
+            const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
+                                       p.k_tiles, p.slices);
             const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
             const int chunks = w.n_len / C::EPI_N;
             const int32_t row0 = o.d_row + consumer * C::MMA_M + quarter * 32;
@@ -351,6 +363,35 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
                             ptx::mbar_arrive(bar_tempty + 8 * acc.stage);
                         }
                     }
+                }
+                if (p.slices > 1) {
+                    // Split-K: this slice's fp32 partial sums go to the
+                    // workspace [slice][M][N] as two 32 x 32 fp32 boxes per
+                    // chunk (128-byte rows, the same swizzled staging as the
+                    // fp16 path; the 3-D map clips each slice at its own M).
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t *v = half ? hi : lo;
+                        if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
+                        __syncwarp();
+                        const uint32_t row_addr = stage_base + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
+                            ptx::st_shared_v4(row_addr + unit * 16u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int32_t col = col0 + c * C::EPI_N + 32 * half;
+                            if (row0 < p.M && col < p.N) {
+                                ptx::tma_store_3d(&tmP, stage_base + buf * C::EPI_BUF, col, row0, w.slice);
+                            }
+                            ptx::bulk_commit_group();
+                        }
+                        buf ^= 1u;
+                    }
+                    continue;
                 }
                 // fp32 -> fp16, round to nearest even, packed two per word.
                 uint32_t h[32];
@@ -423,6 +464,39 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
     if (warp == 1) {
         ptx::tcgen05_fence_after();
         ptx::tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// Split-K, second pass: D = fp16_RNE(sum over slices of the fp32 partials),
+// 8 columns (16 bytes of D) per thread and step.  Launched right behind the
+// GEMM as a programmatic dependent; griddepcontrol.wait makes the partials
+// visible before they are read.
+constexpr int kMaxSlices = 16;
+
+template <int S>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float *__restrict__ partial,
+                                                            uint16_t *__restrict__ D, int64_t mn) {
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    const int64_t units = mn / 4;  // 4 columns (one float4 per slice) per thread and step
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t u = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; u < units; u += stride) {
+        // all S loads in flight before the first add; slices added in order
+        float4 v[S];
+#pragma unroll
+        for (int s = 0; s < S; ++s) v[s] = __ldg(reinterpret_cast<const float4 *>(partial + s * mn) + u);
+        float4 acc = v[0];
+#pragma unroll
+        for (int s = 1; s < S; ++s) {
+            acc.x += v[s].x;
+            acc.y += v[s].y;
+            acc.z += v[s].z;
+            acc.w += v[s].w;
+        }
+        const __half2 h0 = __floats2half2_rn(acc.x, acc.y);
+        const __half2 h1 = __floats2half2_rn(acc.z, acc.w);
+        *reinterpret_cast<uint2 *>(D + u * 4) =
+            make_uint2(*reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1));
     }
 }
 

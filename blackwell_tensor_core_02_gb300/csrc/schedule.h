@@ -82,13 +82,33 @@ GEMM_HD int32_t auto_raster_group(int32_t num_m, int64_t K, int32_t tile_m) {
 struct WorkItem {
     int32_t m_idx;
     int32_t n_idx;
-    int32_t n_off;  // 0, or 128 for the second half of a split tile
-    int32_t n_len;  // 256, or 128 for a half tile
+    int32_t n_off;    // 0, or 128 for the second half of a split tile
+    int32_t n_len;    // 256, or 128 for a half tile
+    int32_t slice;    // K slice of a split-K tile (0 without split-K)
+    int32_t kt_begin; // first and one-past-last 64-wide K tile of the item
+    int32_t kt_end;
 };
 
 // Items [0, split_from) are whole tiles t = item in grouped order; items from
 // split_from on are the two halves of tiles split_from, split_from + 1, ...
-GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t group, int32_t split_from) {
+// With slices > 1 (split-K; nothing is then split along N) item t*slices + s
+// is K slice s of tile t: K tiles [s*k_tiles/slices, (s+1)*k_tiles/slices).
+GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t group, int32_t split_from,
+                         int32_t k_tiles = 0, int32_t slices = 1) {
+    if (slices > 1) {
+        const int32_t t = item / slices;
+        const int32_t sl = item - t * slices;
+        const TileCoord c = tile_of(t, num_m, num_n, group);
+        WorkItem w;
+        w.m_idx = c.m_idx;
+        w.n_idx = c.n_idx;
+        w.n_off = 0;
+        w.n_len = 256;
+        w.slice = sl;
+        w.kt_begin = static_cast<int32_t>(static_cast<int64_t>(sl) * k_tiles / slices);
+        w.kt_end = static_cast<int32_t>(static_cast<int64_t>(sl + 1) * k_tiles / slices);
+        return w;
+    }
     int32_t t = item;
     int32_t half = -1;
     if (item >= split_from) {
@@ -102,7 +122,24 @@ GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t gro
     w.n_idx = c.n_idx;
     w.n_off = half < 0 ? 0 : 128 * half;
     w.n_len = half < 0 ? 256 : 128;
+    w.slice = 0;
+    w.kt_begin = 0;
+    w.kt_end = k_tiles;
     return w;
+}
+
+// Split-K (TIRx notes V6 leaves a partly idle last wave; with very few tiles
+// most of the GPU would idle for the whole K-loop).  With num_tiles tiles on
+// `clusters` persistent clusters and k_tiles K tiles per tile, K is cut into
+// S = min(clusters / num_tiles, k_tiles / 8, 16) slices when that gives at
+// least 4 (a 2-way N split already halves the K-loop's time, so fewer slices
+// would not gain); otherwise 1.  Each slice then runs at least 8 K tiles.
+GEMM_HD int32_t splitk_slices(int32_t num_tiles, int32_t clusters, int32_t k_tiles) {
+    if (num_tiles <= 0 || clusters <= 0) return 1;
+    int32_t s = clusters / num_tiles;
+    if (s > k_tiles / 8) s = k_tiles / 8;
+    if (s > 16) s = 16;
+    return s >= 4 ? s : 1;
 }
 
 // Tiles [split_from, num_tiles) are split in two when that fits the last

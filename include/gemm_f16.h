@@ -118,6 +118,35 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
                    const gemm_f16_options *opts);
 
 /*
+ * As gemm_f16_nt_ex(), with a caller-owned device workspace that lets the
+ * library split the K-loop across CTA pairs when the output has few tiles
+ * (split-K: at most a quarter as many 256x256 tiles as co-resident pairs, and
+ * at least 32 K tiles of 64; the pages' persistent scheduler, TIRx notes V6,
+ * would otherwise leave most SMs idle for the whole K-loop).  K is then cut
+ * into S slices (4..16); each slice's fp32 partial sums go to the workspace
+ * as [S][M][N] fp32 and a second kernel on `stream` adds them in fp32 and
+ * rounds once to fp16.  `workspace` is a device pointer, 16-byte aligned,
+ * owned by the caller, needing no initialisation; its contents are scratch
+ * (overwritten by each call, meaningless afterwards) and it must not be used
+ * by two calls that may overlap on the GPU.  If workspace_bytes is smaller
+ * than gemm_f16_nt_workspace_size() for the same arguments, or the pointer is
+ * misaligned, the call runs without split-K.  NULL with 0 bytes is allowed
+ * (= gemm_f16_nt_ex).  Errors as gemm_f16_nt_ex(), and GEMM_ERR_INVALID_ARG for
+ * a NULL workspace with a non-zero size or a negative size.
+ */
+int gemm_f16_nt_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *workspace,
+                   int64_t workspace_bytes, void *stream, const gemm_f16_options *opts);
+
+/*
+ * Bytes of workspace gemm_f16_nt_ws() will use for these arguments on the
+ * current device (S * M * N * 4 with split-K, 0 when it would not split), or
+ * a negative gemm_status_t (bad options or shape, no usable device).  The
+ * choice depends on how many clusters fit on the device, so this makes the
+ * same per-device set-up as the first GEMM call (no GPU work is enqueued).
+ */
+int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a wait inside a kernel ran out
  * (the kernel then skipped its remaining work and exited; D is incomplete).
@@ -131,24 +160,34 @@ int gemm_f16_last_device_status(void *stream, uint64_t *info);
 /* A static, human-readable name for a gemm_status_t value. */
 const char *gemm_f16_status_string(int status);
 
+/* One unit of work of a persistent cluster (see gemm_f16_nt_schedule()). */
+typedef struct gemm_f16_work_item {
+    int64_t m_idx, n_idx;     /* the tile: rows m_idx * 128*cta_group*consumers, columns n_idx * 256 */
+    int64_t n_off, n_len;     /* columns n_off .. n_off + n_len of that tile (256, or a 128 half) */
+    int64_t slice;            /* K slice under split-K, else 0 */
+    int64_t kt_begin, kt_end; /* 64-wide K tiles [kt_begin, kt_end) */
+} gemm_f16_work_item;
+
 /*
  * The persistent scheduler, as a pure host query (no CUDA call); the kernel
  * runs the same code.  D is cut into tiles of (128 * cta_group * consumers)
- * rows x 256 columns (consumers 0 means 1), ordered in groups of `raster_group` M-tiles (0 = the shape-derived
- * default described under gemm_f16_options, which needs K): M fastest inside
- * a group, then N, then the next group (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters persistent clusters,
- * if the last wave is at most half full (T = qP + r, 0 < 2r <= P) its r tiles
- * are split along N into 2r half tiles of 128 columns, so that the tail lasts
- * half a tile (V6 notes that 1024 tiles over 148 CTAs leave 6.9 tiles per CTA,
- * i.e. a partly idle last wave).  Cluster `cluster_id` takes work items
- * cluster_id, cluster_id + P, ...  Returns 1 and the iter-th item of that
- * cluster -- tile (m_idx, n_idx), columns n_off .. n_off + n_len of that tile
- * (n_len 256, or 128 for a half) -- 0 if the cluster has no iter-th item, or
- * GEMM_ERR_INVALID_ARG for bad arguments.
+ * rows x 256 columns (consumers 0 means 1), ordered in groups of
+ * `raster_group` M-tiles (0 = the shape-derived default described under
+ * gemm_f16_options): M fastest inside a group, then N, then the next group
+ * (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters
+ * persistent clusters, if the last wave is at most half full (T = qP + r,
+ * 0 < 2r <= P) its r tiles are split along N into 2r half tiles of 128
+ * columns, so that the tail lasts half a tile (V6 notes that 1024 tiles over
+ * 148 CTAs leave 6.9 tiles per CTA, i.e. a partly idle last wave).  With
+ * split_k = 1 (what gemm_f16_nt_ws() does given enough workspace) and few
+ * tiles, K is instead cut into slices: item t*S + s is slice s of tile t.
+ * Cluster `cluster_id` takes work items cluster_id, cluster_id + P, ...
+ * Returns 1 and fills *out with the iter-th item of that cluster, 0 if the
+ * cluster has no iter-th item, or GEMM_ERR_INVALID_ARG for bad arguments.
  */
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers,
-                         int32_t raster_group, int64_t num_clusters, int64_t cluster_id, int64_t iter, int64_t *m_idx,
-                         int64_t *n_idx, int64_t *n_off, int64_t *n_len);
+                         int32_t raster_group, int32_t split_k, int64_t num_clusters, int64_t cluster_id, int64_t iter,
+                         gemm_f16_work_item *out);
 
 /*
  * Where CTA `rank` of a work item reads and writes, as a pure host query (no

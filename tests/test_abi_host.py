@@ -72,6 +72,10 @@ def test_argument_errors_are_returned_before_any_launch():
     # empty products are accepted and launch nothing, even with null operands
     assert lib.gemm_f16_nt(None, None, None, 0, 128, 64, None) == OK
     assert lib.gemm_f16_nt(None, None, None, 128, 0, 64, None) == OK
+    # a workspace of non-zero size must exist; negative sizes are rejected
+    assert lib.gemm_f16_nt_ws(a, b, d, 128, 128, 64, None, 4096, None, None) == INVALID
+    assert lib.gemm_f16_nt_ws(a, b, d, 128, 128, 64, 0x40000, -1, None, None) == INVALID
+    assert lib.gemm_f16_nt_ws(None, None, None, 0, 128, 64, None, 0, None, None) == OK
     for bad in (g.Options(cta_group=3), g.Options(max_clusters=-1), g.Options(raster_group=-2),
                 g.Options(debug_flags=2), g.Options(timeout_ns=-5), g.Options(overlap_launch=2),
                 g.Options(consumers=3), g.Options(cta_group=1, consumers=2)):
@@ -84,6 +88,8 @@ def test_no_device_reported_without_gpu():
         pytest.skip("only meaningful on a machine without a GPU (the pointers here are fake)")
     lib = g.load()
     assert lib.gemm_f16_nt(0x10000, 0x20000, 0x30000, 128, 128, 64, None) == NO_DEVICE
+    assert lib.gemm_f16_nt_workspace_size(256, 256, 4096, None) == NO_DEVICE
+    assert lib.gemm_f16_nt_workspace_size(256, 12, 4096, None) == UNSUPPORTED
 
 
 def test_status_strings():
@@ -116,7 +122,8 @@ def test_schedule_covers_every_output_once(M, N, cg, group, clusters):
             w = g.schedule(M, N, cg, group, clusters, c, it, consumers=consumers)
             if w is None:
                 break
-            m_idx, n_idx, n_off, n_len = w
+            m_idx, n_idx, n_off, n_len = w[:4]
+            assert w[4:] == (0, 0, -(-4096 // 64))  # no split-K: every item runs all of K
             assert 0 <= m_idx < num_m and 0 <= n_idx < num_n and n_len in (128, 256)
             for half in range(n_off // 128, (n_off + n_len) // 128):
                 key = (m_idx, n_idx, half)
@@ -155,6 +162,38 @@ def test_schedule_grouped_order():
     assert order[127] == (7, 15) and order[128] == (8, 0) and order[255] == (15, 15)
 
 
+@pytest.mark.parametrize("M,N,K,cg,clusters,slices", [
+    (256, 256, 4096, 2, 76, 8),     # 1 tile: S = min(76, 64/8, 16) = 8
+    (1024, 1024, 4096, 2, 76, 4),   # 16 tiles: S = 76 // 16 = 4
+    (256, 4096, 2048, 2, 76, 4),    # 16 tiles, 32 K tiles: S = min(4, 4) = 4
+    (300, 520, 3000, 2, 76, 5),     # 6 tiles, 47 K tiles: S = 47 // 8 = 5, ragged K slices
+    (256, 256, 4096, 1, 152, 8),    # single-CTA tiles
+    (1536, 1536, 4096, 2, 76, 1),   # 36 tiles: at most 2 slices would fit, so no split-K
+    (256, 256, 512, 2, 76, 1),      # 8 K tiles: too short to split
+])
+def test_split_k_schedule_covers_k_once(M, N, K, cg, clusters, slices):
+    num_m = -(-M // (128 * cg))
+    num_n = -(-N // 256)
+    k_tiles = -(-K // 64)
+    seen = {}
+    got_slices = set()
+    for c in range(clusters):
+        it = 0
+        while (w := g.schedule(M, N, cg, 0, clusters, c, it, K=K, split_k=1)) is not None:
+            m_idx, n_idx, n_off, n_len, sl, kb, ke = w
+            got_slices.add(sl)
+            if slices > 1:
+                assert (n_off, n_len) == (0, 256) and kb < ke and ke - kb >= 8
+            for kt in range(kb, ke):
+                for half in range(n_off // 128, (n_off + n_len) // 128):
+                    key = (m_idx, n_idx, half, kt)
+                    assert key not in seen, f"{key} twice"
+                    seen[key] = c
+            it += 1
+    assert len(seen) == num_m * num_n * 2 * k_tiles
+    assert got_slices == set(range(slices))
+
+
 def test_schedule_splits_the_last_wave_of_4096():
     # 256 tiles over 76 CTA pairs: 3 full waves (228 tiles), then 28 tiles split
     # into 56 half tiles, one per pair, so the tail lasts half a tile.
@@ -167,6 +206,8 @@ def test_schedule_splits_the_last_wave_of_4096():
     assert len(items) == 228 + 56
     assert all(w[3] == 256 for c, it, w in items if it < 3)
     assert all(w[3] == 128 for c, it, w in items if it == 3)
+    # split_k does not change a shape with this many tiles
+    assert all(g.schedule(4096, 4096, 2, 8, 76, c, it, split_k=1) == w for c, it, w in items)
     assert sum(1 for c, it, w in items if it == 3) == 56
 
 

@@ -120,6 +120,39 @@ def test_split_last_wave(gpu_lib, M, N, K, v, clusters):
                  f"split {M}x{N}x{K} {v} clusters={clusters}")
 
 
+@pytest.mark.parametrize("M,N,K,cg", [
+    (256, 256, 4096, 2),     # one tile, 8 K slices
+    (1024, 1024, 4096, 2),   # 16 tiles, 4 slices
+    (256, 4096, 2048, 2),    # a skinny M: 16 tiles, 4 slices
+    (300, 520, 3000, 2),     # ragged M, N and K: 6 tiles, 5 uneven slices
+    (256, 256, 4096, 1),     # single-CTA tiles
+])
+def test_split_k_full(gpu_lib, M, N, K, cg):
+    w = si.custom(M, N, K, seed=M + N + K)
+    A, B = w.operands()
+    o = gpu_lib.Options(cta_group=cg)
+    need = gpu_lib.workspace_size(M, N, K, o)
+    assert need > 0 and need % (4 * M * N) == 0, "this shape is meant to split K"
+    dA, dB = to_dev(A), to_dev(B)
+    # the workspace needs no initialisation: fill it with NaN
+    ws = torch.full((need // 4,), float("nan"), dtype=torch.float32, device="cuda")
+    D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    rc = gpu_lib.gemm_f16_nt_ptr(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), M, N, K,
+                                 torch.cuda.current_stream().cuda_stream, o, ws.data_ptr(), need)
+    assert rc == 0
+    assert gpu_lib.last_device_status()[0] == 0
+    ref = oracle.gemm_f16_nt(A, B)
+    assert_close(D.cpu().numpy(), ref, f"split-K {M}x{N}x{K} cg={cg}")
+    # a workspace one byte too small: no split-K, same answer
+    D2 = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    rc = gpu_lib.gemm_f16_nt_ptr(dA.data_ptr(), dB.data_ptr(), D2.data_ptr(), M, N, K,
+                                 torch.cuda.current_stream().cuda_stream, o, ws.data_ptr(), need - 1)
+    assert rc == 0 and gpu_lib.last_device_status()[0] == 0
+    assert_close(D2.cpu().numpy(), ref, f"no split-K {M}x{N}x{K} cg={cg}")
+    # the Python call supplies a workspace by itself
+    assert_close(gpu_lib.gemm_f16_nt(dA, dB, options=o).cpu().numpy(), ref, "binding")
+
+
 def test_guard_bands_and_full_overwrite(gpu_lib):
     # D sits inside a larger buffer filled with a NaN sentinel: every element of
     # D must be written, and nothing before or after it.
@@ -184,6 +217,39 @@ def test_back_to_back_dependent_calls(gpu_lib, overlap):
         D1h = D1.cpu().numpy()
         assert_close(D1h, oracle.gemm_f16_nt(A, B), "first")
         assert_close(D2.cpu().numpy(), oracle.gemm_f16_nt(D1h, C), "second (reads the first)")
+
+
+def test_concurrent_host_threads(gpu_lib):
+    # Four host threads, each on its own stream, call the library at once
+    # (device set-up is guarded; tensor maps are built per call).
+    import threading
+
+    probs = [si.custom(256 + 64 * t, 520, 200 + 8 * t, seed=60 + t).operands() for t in range(4)]
+    outs = [None] * 4
+    errors = []
+
+    def worker(t):
+        try:
+            A, B = probs[t]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                dA, dB = to_dev(A), to_dev(B)
+                for _ in range(10):
+                    D = gpu_lib.gemm_f16_nt(dA, dB, stream=s)
+            s.synchronize()
+            outs[t] = D.cpu().numpy()
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    assert gpu_lib.last_device_status()[0] == 0
+    for (A, B), D in zip(probs, outs):
+        assert_close(D, oracle.gemm_f16_nt(A, B), "thread")
 
 
 def test_repeated_calls_and_streams(gpu_lib):
