@@ -25,7 +25,7 @@ __all__ = [
 STATUS = {
     0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED_SHAPE", -3: "GEMM_ERR_MISALIGNED",
     -4: "GEMM_ERR_NO_DEVICE", -5: "GEMM_ERR_ARCH", -6: "GEMM_ERR_LAUNCH", -7: "GEMM_ERR_DEVICE_TIMEOUT",
-    -8: "GEMM_ERR_CUDA",
+    -8: "GEMM_ERR_CUDA", -9: "GEMM_ERR_SCRATCH_LIMIT",
 }
 
 
@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_nt_ws.restype = ctypes.c_int
         lib.gemm_f16_nt_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Options)]
         lib.gemm_f16_nt_workspace_size.restype = ctypes.c_int64
+        lib.gemm_f16_nt_static_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+        lib.gemm_f16_nt_static_ws.restype = ctypes.c_int
         lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
         lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
         _lib = lib

@@ -421,6 +421,9 @@ const char *gemm_f16_status_string(int status) {
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
         case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a wait inside the kernel ran out";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime or driver error";
+        case GEMM_ERR_SCRATCH_LIMIT:
+            return "GEMM_ERR_SCRATCH_LIMIT: the split-K scratch this problem needs exceeds the library's fixed "
+                   "16 MiB scratch array (use gemm_f16_nt_ws with a larger workspace)";
         default: return "unknown gemm_f16 status";
     }
 }
@@ -508,3 +511,68 @@ int gemm_f16_pipeline_trace(int32_t depth, int32_t initial_phase, int32_t steps,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// A GEMM entry point that allocates nothing: the split-K scratch lives in a
+// fixed device array of this library instead of memory the caller provides.
+//
+// Who needs it: code that must not allocate device memory while it runs --
+// for example a caller that sets its memory budget up front and forbids any
+// later allocation, a plug-in that lives inside a host application owning all
+// of the GPU's memory, or a real-time loop where an allocation (which can
+// block and synchronise the device) is not allowed.  Such callers can still
+// get split-K by using this fixed array.
+//
+// Cost: every GPU on which this library's device code is loaded holds the
+// array (kStaticScratchBytes) until the process exits.  All calls on a device
+// share it, and it keeps whatever the last call wrote; split-K overwrites
+// every partial it later reads, so nothing in it has to start at zero, but
+// two calls that may run at the same time on the GPU (different streams
+// without ordering, or concurrent host threads) race on it.
+// ---------------------------------------------------------------------------
+namespace gemm_f16 {
+namespace {
+
+constexpr int64_t kStaticScratchBytes = int64_t(16) << 20;
+
+static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
+
+std::mutex g_static_mutex;
+void *g_static_ptr[kMaxDevices] = {};
+
+// The array's device address on the current device.  In host code the name
+// g_static_scratch is only a host-side handle, never a device address, so it
+// is resolved once per device, with that device current.
+int static_scratch(void **out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_NO_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_NO_DEVICE;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_ptr[dev] == nullptr) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
+            cudaGetLastError();
+            return GEMM_ERR_CUDA;
+        }
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gemm_f16
+
+extern "C" int gemm_f16_nt_static_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K,
+                                     void *stream, const gemm_f16_options *opts) {
+    const int64_t need = gemm_f16_nt_workspace_size(M, N, K, opts);
+    if (need < 0) return static_cast<int>(need);
+    if (need > kStaticScratchBytes) return GEMM_ERR_SCRATCH_LIMIT;
+    void *scratch = nullptr;
+    const int st = static_scratch(&scratch);
+    if (st != GEMM_OK) return st;
+    return gemm_f16_nt_ws(A, B, D, M, N, K, scratch, kStaticScratchBytes, stream, opts);
+}

@@ -46,7 +46,8 @@ typedef enum gemm_status {
     GEMM_ERR_ARCH = -5,              /* current device is not sm_103 (GB300)    */
     GEMM_ERR_LAUNCH = -6,            /* the kernel launch itself failed         */
     GEMM_ERR_DEVICE_TIMEOUT = -7,    /* a bounded wait inside the kernel ran out */
-    GEMM_ERR_CUDA = -8               /* another CUDA runtime/driver error        */
+    GEMM_ERR_CUDA = -8,              /* another CUDA runtime/driver error        */
+    GEMM_ERR_SCRATCH_LIMIT = -9      /* gemm_f16_nt_static_ws: scratch too small  */
 } gemm_status_t;
 
 /*
@@ -145,6 +146,38 @@ int gemm_f16_nt_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, 
  * same per-device set-up as the first GEMM call (no GPU work is enqueued).
  */
 int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts);
+
+/*
+ * Bytes of the library's fixed device scratch array used by
+ * gemm_f16_nt_static_ws().
+ */
+#define GEMM_F16_STATIC_SCRATCH_BYTES (16ll << 20)
+
+/*
+ * As gemm_f16_nt_ws(), but the split-K scratch is a fixed array inside this
+ * library (GEMM_F16_STATIC_SCRATCH_BYTES = 16 MiB per GPU) instead of memory
+ * the caller passes, so the call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.  It is for callers that cannot
+ * allocate device memory while they run -- code that fixes its memory budget
+ * once and forbids later allocation, a plug-in inside an application that
+ * owns the GPU's memory, or a loop where an allocation (which may block and
+ * synchronise the device) is not allowed.  The pages have no counterpart of
+ * this entry point; it is a property of this library, not of the method.
+ *
+ * A, B, D, M, N, K, stream and opts mean what they mean for gemm_f16_nt_ex().
+ * The first call on each device also resolves the array's device address (and
+ * does the per-device set-up every first call does); make that first call
+ * before any stream capture.  Every GPU that loads this library's device code
+ * holds the array until the process exits.  All calls on a device share it
+ * and it keeps the last call's contents; nothing in it needs to start at
+ * zero, but calls that may overlap on the GPU race on it, so order them (one
+ * stream, or events).  Returns GEMM_ERR_SCRATCH_LIMIT, before anything is
+ * enqueued, when the split-K scratch the problem would use
+ * (gemm_f16_nt_workspace_size()) exceeds the array; otherwise the errors of
+ * gemm_f16_nt_ex().
+ */
+int gemm_f16_nt_static_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
+                          const gemm_f16_options *opts);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's status
