@@ -53,10 +53,13 @@ typedef enum gemm_status {
 /*
  * Options for gemm_f16_nt_ex().  Zero-initialise and set what you need; every
  * zero field means "the default".
- *   cta_group     2 (default): a 2-CTA cluster issues one cta_group::2 MMA
- *                 over a 256 x 256 tile per CTA pair ("GEMM III -- warp
+ *   cta_group     2: a 2-CTA cluster issues one cta_group::2 MMA over a
+ *                 256 x 256 tile per CTA pair ("GEMM III -- warp
  *                 specialization & clusters to SOTA", Step 8; TIRx notes V8).
  *                 1: each CTA computes a 128 x 256 tile alone (Step 7 / V7).
+ *                 0 (default): 1 when the K-loop is at most 8 tiles of 64 and
+ *                 the pair tiles would occupy at most half the co-resident
+ *                 pairs (small, latency-bound problems), else 2.
  *   max_clusters  cap on the persistent grid, in clusters (CTA pairs for
  *                 cta_group 2); 0 = as many as are co-resident on the device.
  *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes

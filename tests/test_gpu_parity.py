@@ -60,7 +60,7 @@ def opts(g, variant=(0, 0), max_clusters=0):
 
 # ----------------------------------------------------------- full compares --
 
-@pytest.mark.parametrize("v", VARIANTS, ids=VIDS)
+@pytest.mark.parametrize("v", VARIANTS + [(0, 0)], ids=VIDS + ["default"])
 @pytest.mark.parametrize("name", ["single_tile_128x128x64", "ktile_grid_256x256x512"])
 def test_small_workloads_full(gpu_lib, name, v):
     w = si.WORKLOADS[name]
