@@ -230,7 +230,7 @@ def run_reference(args) -> None:
 
 # ------------------------------------------------------ all five workloads --
 
-def survey_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float = 0.4) -> list[dict]:
+def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float = 0.4) -> list[dict]:
     """Each synthetic shape once: TFLOP/s, fraction of the tensor peak, and HBM GB/s of the
     compulsory bytes (the figure that matters for the small, latency-bound shapes).
 
@@ -476,7 +476,7 @@ def run_ours(args) -> None:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(A, B)
         if world == 1 and not args.no_workloads:
-            line["workloads"] = survey_workloads(g, dev, peak, A, B)
+            line["workloads"] = measure_all_workloads(g, dev, peak, A, B)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
