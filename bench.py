@@ -279,10 +279,12 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
         got = Dr[0].cpu().numpy()[pr, pc].astype(np.float64)
         if not np.all(np.abs(got - ref) <= 2.0 ** -9 * np.abs(ref) + 1e-3):
             raise RuntimeError(f"correctness guard failed for {name}")
-        per_graph = int(min(1000, max(10, budget_s / 4 / max(w.flop / 1.5e15, 3e-6))))
-        replays = 4
+        replays = 10
+        per_graph = int(min(400, max(10, budget_s / replays / max(w.flop / 1.5e15, 3e-6))))
         res = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "steps": per_graph * replays,
-               "rotated_copies": rot, "timing": "CUDA graph replay"}
+               "rotated_copies": rot,
+               "timing": f"CUDA graph of {per_graph} launches, replayed {replays} times; "
+                         "percentiles over the per-replay mean"}
         for label, fn in (("ours", ours), ("cublas", cublas)):
             for i in range(5):
                 fn(i)
@@ -291,23 +293,27 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
             with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
                 for i in range(per_graph):
                     fn(i)
+            # one event per replay boundary: the spread over replays gives p10 / median / p90
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
             with torch.cuda.stream(stream):
                 graph.replay()  # warm-up replay
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(replays):
+                ev[0].record(stream)
+                for r in range(replays):
                     graph.replay()
-                e1.record(stream)
-            e1.synchronize()
+                    ev[r + 1].record(stream)
+            ev[-1].synchronize()
             del graph
-            ms = e0.elapsed_time(e1) / (per_graph * replays)
+            per = sorted(ev[r].elapsed_time(ev[r + 1]) / per_graph for r in range(replays))
+            ms = ev[0].elapsed_time(ev[-1]) / (per_graph * replays)
             tf = w.flop / (ms * 1e-3) / 1e12
+            pct = {"ms_p10": float(np.percentile(per, 10)), "ms_median": float(np.percentile(per, 50)),
+                   "ms_p90": float(np.percentile(per, 90))}
             if label == "ours":
                 res.update(ms_per_step=ms, tflops=tf, frac_of_peak=tf / peak,
-                           hbm_gbs_compulsory=w.min_bytes / (ms * 1e-3) / 1e9)
+                           hbm_gbs_compulsory=w.min_bytes / (ms * 1e-3) / 1e9, **pct)
             else:
                 res["cublas_tflops"] = tf
+                res["cublas_ms_median"] = pct["ms_median"]
         out.append(res)
         del Ar, Br, Dr
         torch.cuda.empty_cache()
