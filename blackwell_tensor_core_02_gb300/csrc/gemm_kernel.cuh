@@ -20,6 +20,10 @@
 //   TMEM ring:  tmem_empty[a] (ld2mma) -> MMA -> tmem_full[a] (mma2ld) -> epilogue
 // The TMEM ring has two accumulator buffers, so the epilogue of tile i runs
 // while the MMA issuer already accumulates tile i+1 into the other buffer.
+// The epilogue reads its whole share of the accumulator and rounds it to
+// packed fp16 in registers before it stages and stores anything, so the
+// buffer goes back to the MMA after the TMEM reads alone; the slower SMEM
+// staging and TMA stores then run beside the next tile's MMAs.
 //
 // CTA pair (CG = 2; "GEMM III", Step 8; TIRx notes V8): a 2-CTA cluster owns a
 // 256 x 256 tile.  CTA r loads A rows m_base + 128r and B rows n_base + 128r
@@ -153,6 +157,16 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// fp32 -> fp16 with round to nearest even, two values packed per word:
+// out[j] = (fp16(in[2j+1]) << 16) | fp16(in[2j]), j < 16.
+__device__ __forceinline__ void to_f16x2(const uint32_t (&in)[32], uint32_t *out) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const __half2 v = __floats2half2_rn(__uint_as_float(in[2 * j]), __uint_as_float(in[2 * j + 1]));
+        out[j] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+}
+
 template <int CG, int NC>
 __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -215,7 +229,24 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     // Everything above touches only this CTA's own resources, so with a
     // programmatic launch it overlaps the tail of the previous kernel of the
-    // stream.  A, B and D are first touched below, after the wait.
+    // stream.  A, B and D are first read and written below, after the wait.
+    // Before it, the producer only asks L2 to fetch the A and B boxes of its
+    // first ring fill: L2 is where every later load reads them, and a line
+    // the previous kernel still writes is updated there, so the prefetch
+    // changes no value; it moves the HBM latency of the first k-tiles under
+    // the previous kernel's tail.
+    if (warp == 0 && lane == 0 && cluster < p.num_items) {
+        const WorkItem w = work_of(cluster, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
+                                   p.slices);
+        const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
+        const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
+        const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
+        for (int kt = w.kt_begin; kt < kt_end; ++kt) {
+#pragma unroll
+            for (int c = 0; c < NC; ++c) ptx::tma_prefetch_l2_2d(&tmA, kt * C::BLOCK_K, o.a_row + c * C::MMA_M);
+            ptx::tma_prefetch_l2_2d(mapB, kt * C::BLOCK_K, o.b_row);
+        }
+    }
     if (threadIdx.x == 0) ptx::griddep_launch_dependents();
     ptx::griddep_wait();
 
@@ -345,26 +376,81 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
             ptx::tcgen05_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>((acc.stage * NC + consumer) * C::BLOCK_N);
+            auto release_tmem = [&]() {
+                // This warp's part of the accumulator is in registers: hand
+                // the TMEM buffer back (TIRx notes V7, "Writeback Flow").
+                ptx::tcgen05_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (CG == 2) {
+                        ptx::mbar_arrive_cluster(ptx::mapa(bar_tempty + 8 * acc.stage, 0));
+                    } else {
+                        ptx::mbar_arrive(bar_tempty + 8 * acc.stage);
+                    }
+                }
+            };
+            if constexpr (!C::EPI_DIRECT) {
+                if (p.slices == 1) {
+                    // fp16 D through TMA stores.  All chunks are read from TMEM
+                    // and rounded to packed fp16 first (128 registers), so the
+                    // buffer goes back to the MMA before any store is staged:
+                    // the stores then overlap the next tile's MMAs instead of
+                    // holding the accumulator.
+                    uint32_t h[C::BLOCK_N / C::EPI_N][32];
+#pragma unroll
+                    for (int c = 0; c < C::BLOCK_N / C::EPI_N; ++c) {
+                        if (c < chunks) {
+                            uint32_t lo[32], hi[32];
+                            ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N, lo);
+                            ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
+                            ptx::tmem_wait_ld();
+                            to_f16x2(lo, h[c]);
+                            to_f16x2(hi, h[c] + 16);
+                        }
+                    }
+                    release_tmem();
+#pragma unroll
+                    for (int c = 0; c < C::BLOCK_N / C::EPI_N; ++c) {
+                        if (c < chunks) {
+                            // The store issued from this buffer two chunks ago
+                            // must have finished reading it.
+                            if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
+                            __syncwarp();
+                            // Row `lane` of the 32 x 64 staging tile, in the
+                            // 128-byte swizzle the D tensor map expects:
+                            // 16-byte unit j of row r sits at unit j ^ (r % 8).
+                            const uint32_t row_addr =
+                                stage_base + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
+                                ptx::st_shared_v4(row_addr + unit * 16u, h[c][4 * j], h[c][4 * j + 1],
+                                                  h[c][4 * j + 2], h[c][4 * j + 3]);
+                            }
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int32_t col = col0 + c * C::EPI_N;
+                                if (row0 < p.M && col < p.N) {
+                                    ptx::tma_store_2d(&tmD, stage_base + buf * C::EPI_BUF, col, row0);
+                                }
+                                ptx::bulk_commit_group();
+                            }
+                            buf ^= 1u;
+                        }
+                    }
+                    acc.advance();
+                    continue;
+                }
+            }
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c) {
                 uint32_t lo[32], hi[32];
                 ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N, lo);
                 ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
                 ptx::tmem_wait_ld();
-                if (c == chunks - 1) {
-                    // The whole accumulator of this warp is in registers: hand
-                    // the TMEM buffer back (TIRx notes V7, "Writeback Flow").
-                    ptx::tcgen05_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CG == 2) {
-                            ptx::mbar_arrive_cluster(ptx::mapa(bar_tempty + 8 * acc.stage, 0));
-                        } else {
-                            ptx::mbar_arrive(bar_tempty + 8 * acc.stage);
-                        }
-                    }
-                }
-                if (p.slices > 1) {
+                if (c == chunks - 1) release_tmem();
+                if constexpr (!C::EPI_DIRECT) {
                     // Split-K: this slice's fp32 partial sums go to the
                     // workspace [slice][M][N] as two 32 x 32 fp32 boxes per
                     // chunk (128-byte rows, the same swizzled staging as the
@@ -391,23 +477,13 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
                         }
                         buf ^= 1u;
                     }
-                    continue;
-                }
-                // fp32 -> fp16, round to nearest even, packed two per word.
-                uint32_t h[32];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const __half2 v = __floats2half2_rn(__uint_as_float(lo[2 * j]), __uint_as_float(lo[2 * j + 1]));
-                    h[j] = *reinterpret_cast<const uint32_t *>(&v);
-                }
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const __half2 v = __floats2half2_rn(__uint_as_float(hi[2 * j]), __uint_as_float(hi[2 * j + 1]));
-                    h[16 + j] = *reinterpret_cast<const uint32_t *>(&v);
-                }
-                if constexpr (C::EPI_DIRECT) {
-                    // Row `lane` of this warp: 64 columns = eight 16-byte stores
-                    // (N % 8 == 0, so a 16-byte unit is all in range or all out).
+                } else {
+                    // Two-consumer variant: row `lane` of this warp, 64 columns
+                    // = eight 16-byte stores straight from registers (N % 8 == 0,
+                    // so a 16-byte unit is all in range or all out).
+                    uint32_t h[32];
+                    to_f16x2(lo, h);
+                    to_f16x2(hi, h + 16);
                     const int32_t row = row0 + lane;
                     const int32_t col = col0 + c * C::EPI_N;
                     if (row < p.M) {
@@ -419,31 +495,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
                             }
                         }
                     }
-                    continue;
                 }
-                // The store issued from this buffer two chunks ago must have
-                // finished reading it.
-                if (lane == 0) ptx::bulk_wait_group_read<(C::EPI_BUFS > 0 ? C::EPI_BUFS - 1 : 0)>();
-                __syncwarp();
-                // Row `lane` of the 32 x 64 staging tile, in the 128-byte
-                // swizzle the D tensor map expects: 16-byte unit j of row r
-                // sits at unit j ^ (r % 8).
-                const uint32_t row_addr = stage_base + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
-                    ptx::st_shared_v4(row_addr + unit * 16u, h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int32_t col = col0 + c * C::EPI_N;
-                    if (row0 < p.M && col < p.N) {
-                        ptx::tma_store_2d(&tmD, stage_base + buf * C::EPI_BUF, col, row0);
-                    }
-                    ptx::bulk_commit_group();
-                }
-                buf ^= 1u;
             }
             acc.advance();
         }

@@ -120,6 +120,15 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Bring one 2-D box of a tensor into L2 only (no shared memory, no barrier).
+// A hint: it changes no value any later load observes.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // The same load for a CTA pair: the data lands in this CTA's shared memory,
 // the completion may be signalled on the peer's barrier (`bar` is a
 // shared::cluster address), which is how both CTAs' operand bytes are counted
