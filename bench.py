@@ -281,7 +281,9 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
             raise RuntimeError(f"correctness guard failed for {name}")
         replays = 10
         per_graph = int(min(400, max(10, budget_s / replays / max(w.flop / 1.5e15, 3e-6))))
+        cfg = g.describe(w.M, w.N, w.K)
         res = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "steps": per_graph * replays,
+               "kernel": {k: cfg[k] for k in ("cta_group", "block_n", "split_k", "clusters", "work_items")},
                "rotated_copies": rot,
                "timing": f"CUDA graph of {per_graph} launches, replayed {replays} times; "
                          "percentiles over the per-replay mean"}

@@ -40,11 +40,18 @@ class WorkItem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in ("m_idx", "n_idx", "n_off", "n_len", "slice", "kt_begin", "kt_end")]
 
 
+class LaunchInfo(ctypes.Structure):
+    """Mirror of ``gemm_f16_launch_info``."""
+    _fields_ = [("cta_group", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("split_k", ctypes.c_int32), ("clusters", ctypes.c_int64), ("work_items", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
 class Options(ctypes.Structure):
     """Mirror of ``gemm_f16_options`` (zero fields mean defaults)."""
     _fields_ = [("cta_group", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
-                ("overlap_launch", ctypes.c_int32), ("consumers", ctypes.c_int32)]
+                ("overlap_launch", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -71,9 +78,10 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_last_device_status.restype = ctypes.c_int
         lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
         lib.gemm_f16_status_string.restype = ctypes.c_char_p
-        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i64, i64, i64, ctypes.POINTER(WorkItem)]
+        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i64, i64, i64,
+                                             ctypes.POINTER(WorkItem)]
         lib.gemm_f16_nt_schedule.restype = ctypes.c_int
-        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
+        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
         lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
         lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, vp, ctypes.POINTER(Options)]
         lib.gemm_f16_nt_ws.restype = ctypes.c_int
@@ -81,6 +89,8 @@ def load() -> ctypes.CDLL:
         lib.gemm_f16_nt_workspace_size.restype = ctypes.c_int64
         lib.gemm_f16_nt_static_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
         lib.gemm_f16_nt_static_ws.restype = ctypes.c_int
+        lib.gemm_f16_nt_describe.argtypes = [i64, i64, i64, ctypes.POINTER(Options), i32, ctypes.POINTER(LaunchInfo)]
+        lib.gemm_f16_nt_describe.restype = ctypes.c_int
         lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
         lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
         _lib = lib
@@ -292,26 +302,36 @@ def last_device_status(stream=None) -> tuple[int, int]:
 
 
 def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
-             it: int, K: int = 4096, consumers: int = 1, split_k: int = 0):
+             it: int, K: int = 4096, consumers: int = 1, split_k: int = 0, block_n: int = 256):
     """The iter-th work item of one cluster as (m_idx, n_idx, n_off, n_len, slice, kt_begin, kt_end),
     or None when it has no more."""
     w = WorkItem()
-    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, raster_group, split_k, num_clusters, cluster_id,
-                                     it, ctypes.byref(w))
+    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, block_n, raster_group, split_k, num_clusters,
+                                     cluster_id, it, ctypes.byref(w))
     if rc < 0:
         raise GemmError(rc, "gemm_f16_nt_schedule")
     return tuple(getattr(w, f) for f, _ in WorkItem._fields_) if rc == 1 else None
 
 
 def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int, n_off: int = 0, n_len: int = 256,
-               consumers: int = 1) -> dict:
+               consumers: int = 1, block_n: int = 256) -> dict:
     """Rows/columns CTA `rank` of a work item loads and writes (see the C header)."""
     out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_cta_origin(cta_group, consumers, m_idx, n_idx, n_off, n_len, rank,
+    rc = load().gemm_f16_nt_cta_origin(cta_group, consumers, block_n, m_idx, n_idx, n_off, n_len, rank,
                                        *[ctypes.byref(o) for o in out])
     if rc != 0:
         raise GemmError(rc, "gemm_f16_nt_cta_origin")
     return dict(zip(("a_row", "b_row", "d_row", "d_col"), (o.value for o in out)))
+
+
+def describe(M: int, N: int, K: int, options: Options | None = None, with_workspace: bool = False) -> dict:
+    """The kernel configuration a call would launch for this shape on the current device (see the C header)."""
+    info = LaunchInfo()
+    rc = load().gemm_f16_nt_describe(M, N, K, ctypes.byref(options) if options is not None else None,
+                                     1 if with_workspace else 0, ctypes.byref(info))
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_nt_describe")
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
 
 
 def pipeline_trace(depth: int, initial_phase: int, steps: int) -> list[tuple[int, int]]:

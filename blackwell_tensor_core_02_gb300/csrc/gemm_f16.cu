@@ -22,19 +22,20 @@ struct DeviceInfo {
     bool ready = false;
     int status = GEMM_OK;
     int sm_count = 0;
-    int max_clusters[3] = {0, 0, 0};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2 consumers
+    int max_clusters[4] = {0, 0, 0, 0};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2
+                                         // consumers, [3] narrow single-CTA tiles
 };
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int CG, int NC>
+template <int CG, int NC, int BN>
 cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr, bool overlap = false) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(Cfg<CG, NC>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<CG, NC>::SMEM_ALLOC;
+    cfg.blockDim = dim3(Cfg<CG, NC, BN>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG, NC, BN>::SMEM_ALLOC;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
@@ -53,15 +54,15 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttri
     return cfg;
 }
 
-template <int CG, int NC>
+template <int CG, int NC, int BN>
 int prepare_kernel(int *max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<CG, NC>::SMEM_ALLOC);
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG, NC, BN>::SMEM_ALLOC);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<CG, NC>(dim3(CG, 1, 1), nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<CG, NC, BN>(dim3(CG, 1, 1), nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC, BN>, &cfg);
     if (e != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
     *max_clusters = n;
     return GEMM_OK;
@@ -89,9 +90,10 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
         } else if (major != 10 || minor != 3) {
             d.status = GEMM_ERR_ARCH;
         } else {
-            d.status = prepare_kernel<1, 1>(&d.max_clusters[0]);
-            if (d.status == GEMM_OK) d.status = prepare_kernel<2, 1>(&d.max_clusters[1]);
-            if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2>(&d.max_clusters[2]);
+            d.status = prepare_kernel<1, 1, 256>(&d.max_clusters[0]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<2, 1, 256>(&d.max_clusters[1]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2, 256>(&d.max_clusters[2]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64>(&d.max_clusters[3]);
         }
         if (d.status == GEMM_OK && g_encode == nullptr) {
             void *fn = nullptr;
@@ -143,8 +145,9 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 }
 
 struct Opts {
-    int32_t cta_group = 0;  // 0: chosen from the shape (resolve_cta_group)
+    int32_t cta_group = 0;  // 0: chosen from the shape (resolve_config)
     int32_t consumers = 1;
+    int32_t block_n = 0;    // tile width 256 or 64; 0: chosen from the shape (resolve_config)
     int32_t max_clusters = 0;
     int32_t raster_group = 0;
     int64_t timeout_ns = kDefaultTimeoutNs;
@@ -159,6 +162,8 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
         if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
         if (opts->overlap_launch == -1) o->overlap = false;
         if (opts->cta_group != 0) o->cta_group = opts->cta_group;
+        if (opts->block_n != 0 && opts->block_n != 64 && opts->block_n != 256) return GEMM_ERR_INVALID_ARG;
+        o->block_n = opts->block_n;
         if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
             (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
             return GEMM_ERR_INVALID_ARG;
@@ -170,23 +175,61 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     }
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o->consumers == 2 && o->cta_group == 1) return GEMM_ERR_INVALID_ARG;
+    if (o->block_n == 64 && (o->cta_group == 2 || o->consumers == 2)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }
 
-// The default CTA group.  A CTA pair pays a cluster handshake per stage and a
-// cluster barrier at both ends of the kernel; that is repaid by its halved
-// operand traffic over a long K-loop, but not when the K-loop is at most 8
-// tiles of 64 and the pair tiles would occupy at most half the pairs (measured
-// on GB300: 128x128x64 2.9 vs 3.7 us, 256x256x512 5.0 vs 5.5 us single vs
-// pair).  Such problems run on single CTAs; everything else on pairs.
-int32_t resolve_cta_group(int64_t M, int64_t N, int64_t K, const Opts &o, const DeviceInfo &dev) {
-    if (o.cta_group != 0) return o.cta_group;
-    if (o.consumers == 2) return 2;
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+// The default CTA group and tile width.
+// - A CTA pair pays a cluster handshake per stage and a cluster barrier at both
+//   ends of the kernel.  That is repaid by its halved operand traffic over a
+//   long K-loop, but not when the K-loop is at most 8 tiles of 64 and the pair
+//   tiles would occupy at most half the pairs (measured on GB300: 128x128x64
+//   2.9 vs 3.7 us, 256x256x512 5.0 vs 5.5 us single vs pair).  Such problems
+//   run on single CTAs; everything else on pairs.
+// - A problem whose 128 x 64 tiles fit one wave of co-resident CTAs leaves
+//   most SMs idle with 256-wide tiles.  Narrow tiles spread it over up to 4x
+//   as many SMs, each with a K-loop a quarter as long, and their 8-stage ring
+//   holds a K of 512 at once (one load latency for a short problem).  Measured
+//   on GB300 (graph-timed, us, narrow vs 256-wide): 128x128x64 2.56 vs 2.95,
+//   256x256x512 3.83 vs 4.85, 1024x1024x1024 5.6 vs 6.4, 1024x1024x4096 12.1
+//   vs 15.4; past one wave the 256-wide tiles win (2048x1024x512 5.7 vs 5.2).
+//   With a workspace (allow_splitk), a split-K of at least 8 slices over CTA
+//   pairs beats them (512x512x4096 9.8 vs 11.4, 256x256x4096 9.2 vs 11.6); 4
+//   slices do not (1024x1024x4096 14.9 vs 12.1).
+void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool allow_splitk, Opts *o) {
     const int64_t k_tiles = (K + 63) / 64;
+    if (o->block_n == 0) {
+        bool narrow = false;
+        if (o->cta_group == 0 && o->consumers == 1) {
+            int64_t ctas = dev.max_clusters[3];
+            if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
+            narrow = ((M + 127) / 128) * ((N + 63) / 64) <= ctas;
+            if (narrow && allow_splitk) {
+                int64_t pairs = dev.max_clusters[1];
+                if (o->max_clusters > 0 && o->max_clusters < pairs) pairs = o->max_clusters;
+                const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+                if (pair_tiles <= kDimLimit && splitk_slices(static_cast<int32_t>(pair_tiles),
+                                                             static_cast<int32_t>(pairs),
+                                                             static_cast<int32_t>(k_tiles)) >= 8) {
+                    narrow = false;
+                }
+            }
+        }
+        o->block_n = narrow ? 64 : 256;
+    }
+    if (o->block_n == 64) {
+        o->cta_group = 1;
+        return;
+    }
+    if (o->cta_group != 0) return;
+    if (o->consumers == 2) {
+        o->cta_group = 2;
+        return;
+    }
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
     int64_t pairs = dev.max_clusters[1];
-    if (o.max_clusters > 0 && o.max_clusters < pairs) pairs = o.max_clusters;
-    return (k_tiles <= 8 && 2 * pair_tiles <= pairs) ? 1 : 2;
+    if (o->max_clusters > 0 && o->max_clusters < pairs) pairs = o->max_clusters;
+    o->cta_group = (k_tiles <= 8 && 2 * pair_tiles <= pairs) ? 1 : 2;
 }
 
 // Everything about one launch that follows from the shape, the options and
@@ -197,10 +240,10 @@ struct Plan {
     int64_t workspace_bytes;   // split-K partials, 0 without split-K
 };
 
-template <int CG, int NC>
+template <int CG, int NC, int BN>
 int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o, bool allow_splitk,
               Plan *out) {
-    using C = Cfg<CG, NC>;
+    using C = Cfg<CG, NC, BN>;
     Params &p = out->p;
     p = Params{};
     p.M = static_cast<int32_t>(M);
@@ -215,16 +258,20 @@ int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts
     p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
     p.debug_flags = o.debug_flags;
     p.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
-    int64_t clusters = dev.max_clusters[CG == 1 ? 0 : NC];
+    int64_t clusters = dev.max_clusters[C::NARROW ? 3 : (CG == 1 ? 0 : NC)];
     if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
-    p.slices = (allow_splitk && NC == 1) ? splitk_slices(p.num_tiles, static_cast<int32_t>(clusters), p.k_tiles) : 1;
+    p.slices = (allow_splitk && NC == 1 && !C::NARROW)
+                   ? splitk_slices(p.num_tiles, static_cast<int32_t>(clusters), p.k_tiles)
+                   : 1;
     if (p.slices > kMaxSlices) p.slices = kMaxSlices;
     if (p.slices > 1) {
         p.split_from = p.num_tiles;
         p.num_items = p.num_tiles * p.slices;
         out->workspace_bytes = static_cast<int64_t>(p.slices) * M * N * static_cast<int64_t>(sizeof(float));
     } else {
-        p.split_from = split_point(p.num_tiles, static_cast<int32_t>(clusters));
+        // narrow tiles are not split along N: a 32-column half would leave
+        // the MMA bound by its A operand reads
+        p.split_from = C::NARROW ? p.num_tiles : split_point(p.num_tiles, static_cast<int32_t>(clusters));
         p.num_items = p.num_tiles + (p.num_tiles - p.split_from);
         out->workspace_bytes = 0;
     }
@@ -257,16 +304,16 @@ cudaError_t launch_reduce(const cudaLaunchConfig_t *cfg, int slices, const float
     }
 }
 
-template <int CG, int NC>
+template <int CG, int NC, int BN>
 int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
            const DeviceInfo &dev, const Opts &o, void *workspace, int64_t workspace_bytes) {
-    using C = Cfg<CG, NC>;
+    using C = Cfg<CG, NC, BN>;
     Plan plan;
-    int st = make_plan<CG, NC>(M, N, K, dev, o, workspace != nullptr, &plan);
+    int st = make_plan<CG, NC, BN>(M, N, K, dev, o, workspace != nullptr, &plan);
     if (st != GEMM_OK) return st;
     if (plan.p.slices > 1 && (workspace_bytes < plan.workspace_bytes ||
                               (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)) {
-        st = make_plan<CG, NC>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
+        st = make_plan<CG, NC, BN>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
         if (st != GEMM_OK) return st;
     }
     Params &p = plan.p;
@@ -285,8 +332,8 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     }
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
-        launch_config<CG, NC>(dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1), stream, attr, o.overlap);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC>, tmA, tmB, tmBh, tmD, tmP, p);
+        launch_config<CG, NC, BN>(dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1), stream, attr, o.overlap);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC, BN>, tmA, tmB, tmBh, tmD, tmP, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -338,10 +385,11 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     if (st != GEMM_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_fill(D, M, N, s);
-    o.cta_group = resolve_cta_group(M, N, K, o, *info);
-    if (o.cta_group == 2 && o.consumers == 2) return launch<2, 2>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
-    if (o.cta_group == 2) return launch<2, 1>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
-    return launch<1, 1>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
+    resolve_config(M, N, K, *info, workspace != nullptr, &o);
+    if (o.block_n == 64) return launch<1, 1, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+    if (o.cta_group == 2 && o.consumers == 2) return launch<2, 2, 256>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+    if (o.cta_group == 2) return launch<2, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
+    return launch<1, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
 }
 
 int zero_fill(void *D, int64_t M, int64_t N, cudaStream_t stream) {
@@ -394,11 +442,48 @@ int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f
     st = device_setup(&dev, &info);
     if (st != GEMM_OK) return st;
     Plan plan;
-    o.cta_group = resolve_cta_group(M, N, K, o, *info);
-    st = o.cta_group == 2 ? make_plan<2, 1>(M, N, K, *info, o, true, &plan)
-                          : make_plan<1, 1>(M, N, K, *info, o, true, &plan);
+    resolve_config(M, N, K, *info, true, &o);
+    if (o.block_n == 64) return 0;  // narrow tiles never split K
+    st = o.cta_group == 2 ? make_plan<2, 1, 256>(M, N, K, *info, o, true, &plan)
+                          : make_plan<1, 1, 256>(M, N, K, *info, o, true, &plan);
     if (st != GEMM_OK) return st;
     return plan.workspace_bytes;
+}
+
+int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts, int32_t with_workspace,
+                         gemm_f16_launch_info *out) {
+    Opts o;
+    int st = parse_options(opts, &o);
+    if (st != GEMM_OK) return st;
+    if (M < 0 || N < 0 || K < 0 || !out || (with_workspace != 0 && with_workspace != 1)) return GEMM_ERR_INVALID_ARG;
+    if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    *out = gemm_f16_launch_info{};
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+    int dev = -1;
+    DeviceInfo *info = nullptr;
+    st = device_setup(&dev, &info);
+    if (st != GEMM_OK) return st;
+    const bool ws = with_workspace != 0;
+    resolve_config(M, N, K, *info, ws, &o);
+    Plan plan;
+    if (o.block_n == 64) {
+        st = make_plan<1, 1, 64>(M, N, K, *info, o, false, &plan);
+    } else if (o.cta_group == 2 && o.consumers == 2) {
+        st = make_plan<2, 2, 256>(M, N, K, *info, o, false, &plan);
+    } else if (o.cta_group == 2) {
+        st = make_plan<2, 1, 256>(M, N, K, *info, o, ws, &plan);
+    } else {
+        st = make_plan<1, 1, 256>(M, N, K, *info, o, ws, &plan);
+    }
+    if (st != GEMM_OK) return st;
+    out->cta_group = o.cta_group;
+    out->consumers = o.consumers;
+    out->block_n = o.block_n;
+    out->split_k = plan.p.slices;
+    out->clusters = plan.clusters;
+    out->work_items = plan.p.num_items;
+    out->workspace_bytes = plan.workspace_bytes;
+    return GEMM_OK;
 }
 
 int gemm_f16_last_device_status(void *stream, uint64_t *info) {
@@ -446,24 +531,28 @@ const char *gemm_f16_status_string(int status) {
     }
 }
 
-int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers,
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers, int32_t block_n,
                          int32_t raster_group, int32_t split_k, int64_t num_clusters, int64_t cluster_id, int64_t iter,
                          gemm_f16_work_item *out) {
-    if (cta_group == 0) cta_group = 2;
+    if (block_n == 0) block_n = 256;
+    if (cta_group == 0) cta_group = block_n == 64 ? 1 : 2;
     if (consumers == 0) consumers = 1;
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
-        (consumers == 2 && cta_group != 2) || raster_group < 0 || (split_k != 0 && split_k != 1) || K < 0 ||
+        (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
+        (block_n == 64 && (cta_group != 1 || consumers != 1)) || raster_group < 0 ||
+        (split_k != 0 && split_k != 1) || K < 0 ||
         K > kDimLimit || M <= 0 || N <= 0 || M > kDimLimit || N > kDimLimit || num_clusters <= 0 ||
         num_clusters > kDimLimit || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !out) {
         return GEMM_ERR_INVALID_ARG;
     }
-    const int64_t tile_m = 128 * cta_group * consumers, tile_n = 256;
+    const int64_t tile_m = 128 * cta_group * consumers, tile_n = block_n;
     const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
     const int64_t tiles = num_m * num_n;
     if (tiles > kDimLimit / 16) return GEMM_ERR_INVALID_ARG;
     const int32_t k_tiles = static_cast<int32_t>((K + 63) / 64);
     if (raster_group == 0) raster_group = auto_raster_group(static_cast<int32_t>(num_m), K, static_cast<int32_t>(tile_m));
-    const int32_t slices = (split_k && consumers == 1)
+    const bool narrow = block_n == 64;
+    const int32_t slices = (split_k && consumers == 1 && !narrow)
                                ? splitk_slices(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters), k_tiles)
                                : 1;
     int32_t split_from;
@@ -472,13 +561,14 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
         split_from = static_cast<int32_t>(tiles);
         items = tiles * slices;
     } else {
-        split_from = split_point(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters));
+        split_from = narrow ? static_cast<int32_t>(tiles)
+                            : split_point(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters));
         items = tiles + (tiles - split_from);
     }
     const int64_t item = cluster_id + iter * num_clusters;
     if (item >= items) return 0;
     const WorkItem w = work_of(static_cast<int32_t>(item), static_cast<int32_t>(num_m), static_cast<int32_t>(num_n),
-                               raster_group, split_from, k_tiles, slices);
+                               raster_group, split_from, k_tiles, slices, block_n);
     out->m_idx = w.m_idx;
     out->n_idx = w.n_idx;
     out->n_off = w.n_off;
@@ -489,15 +579,19 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
     return 1;
 }
 
-int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int64_t m_idx, int64_t n_idx, int64_t n_off,
-                           int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row,
-                           int64_t *d_col) {
-    if (cta_group == 0) cta_group = 2;
+int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int64_t m_idx, int64_t n_idx,
+                           int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
+                           int64_t *d_row, int64_t *d_col) {
+    if (block_n == 0) block_n = 256;
+    if (cta_group == 0) cta_group = block_n == 64 ? 1 : 2;
     if (consumers == 0) consumers = 1;
+    const bool lens_ok = block_n == 64 ? (n_len == 64 && n_off == 0)
+                                       : ((n_len == 256 && n_off == 0) || (n_len == 128 && (n_off == 0 || n_off == 128)));
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
-        (consumers == 2 && cta_group != 2) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
-        m_idx * 128 * cta_group * consumers > kDimLimit || n_idx * 256 > kDimLimit || !(n_len == 256 || n_len == 128) ||
-        !(n_off == 0 || (n_len == 128 && n_off == 128)) || !a_row || !b_row || !d_row || !d_col) {
+        (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
+        (block_n == 64 && (cta_group != 1 || consumers != 1)) || rank < 0 || rank >= cta_group || m_idx < 0 ||
+        n_idx < 0 || m_idx * 128 * cta_group * consumers > kDimLimit || n_idx * block_n > kDimLimit || !lens_ok ||
+        !a_row || !b_row || !d_row || !d_col) {
         return GEMM_ERR_INVALID_ARG;
     }
     WorkItem w;
@@ -505,7 +599,7 @@ int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int64_t m_idx, 
     w.n_idx = static_cast<int32_t>(n_idx);
     w.n_off = static_cast<int32_t>(n_off);
     w.n_len = static_cast<int32_t>(n_len);
-    const CtaOrigin o = cta_origin(w, cta_group, rank, consumers);
+    const CtaOrigin o = cta_origin(w, cta_group, rank, consumers, block_n);
     *a_row = o.a_row;
     *b_row = o.b_row;
     *d_row = o.d_row;

@@ -67,12 +67,16 @@ __device__ unsigned long long g_info; // where it happened (role, CTA, tile seq)
 enum : int { kStatusTimeout = -7 };
 enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 
-template <int CG, int NC>
+// BN is the tile width: 256, or 64 for the narrow single-CTA tiles of small
+// problems (more CTAs, and a ring deep enough to hold a K of 512 at once).
+template <int CG, int NC, int BN = 256>
 struct Cfg {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(NC == 1 || (NC == 2 && CG == 2), "two consumers need a CTA pair");
+    static_assert(BN == 256 || (BN == 64 && CG == 1 && NC == 1), "narrow tiles are single-CTA, one consumer");
+    static constexpr bool NARROW = BN != 256;
     static constexpr int BLOCK_M = 128;                 // rows of D per CTA and consumer
-    static constexpr int BLOCK_N = 256;                 // columns of D per tile (MMA N)
+    static constexpr int BLOCK_N = BN;                  // columns of D per tile (MMA N)
     static constexpr int BLOCK_K = 64;                  // one 128-byte swizzle row of fp16
     static constexpr int MMA_M = BLOCK_M * CG;          // M of one tcgen05.mma (one consumer)
     static constexpr int TILE_M = MMA_M * NC;           // rows of D per tile
@@ -81,15 +85,15 @@ struct Cfg {
     static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
     static constexpr int A_STAGE = A_BLOCK * NC;
     static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
-    static constexpr int STAGES = NC == 2 ? 4 : (CG == 2 ? 6 : 4);
+    static constexpr int STAGES = NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4));
     static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
     static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
-    static constexpr int TMEM_COLS = 512;                               // all of TMEM
-    static_assert(ACC_BUFS * NC * BLOCK_N == TMEM_COLS, "accumulators fill TMEM");
+    static constexpr int TMEM_COLS = ACC_BUFS * NC * BLOCK_N;           // 512 (all of TMEM) or 128
+    static_assert(TMEM_COLS == 512 || TMEM_COLS == 128, "a power of two of at least 32 columns");
     static constexpr int EPI_WARPS = 4 * NC;
     static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
-    static constexpr bool EPI_DIRECT = NC == 2;         // store D from registers instead of via SMEM + TMA
+    static constexpr bool EPI_DIRECT = NC == 2 || NARROW;  // store D from registers instead of via SMEM + TMA
     static constexpr int EPI_N = 64;                    // columns per epilogue chunk
     static constexpr int EPI_BUFS = EPI_DIRECT ? 0 : 2;
     static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
@@ -167,12 +171,12 @@ __device__ __forceinline__ void to_f16x2(const uint32_t (&in)[32], uint32_t *out
     }
 }
 
-template <int CG, int NC>
-__global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
+template <int CG, int NC, int BN>
+__global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
                        const __grid_constant__ CUtensorMap tmP, const Params p) {
-    using C = Cfg<CG, NC>;
+    using C = Cfg<CG, NC, BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -237,8 +241,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
     // the previous kernel's tail.
     if (warp == 0 && lane == 0 && cluster < p.num_items) {
         const WorkItem w = work_of(cluster, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
-                                   p.slices);
-        const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
+                                   p.slices, C::BLOCK_N);
+        const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
         const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
         const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
         for (int kt = w.kt_begin; kt < kt_end; ++kt) {
@@ -262,8 +266,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
             bool ok = true;
             for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
                 const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
-                                           p.k_tiles, p.slices);
-                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
+                                           p.k_tiles, p.slices, C::BLOCK_N);
+                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
                 const bool half = w.n_len < C::BLOCK_N;
                 const CUtensorMap *mapB = half ? &tmBh : &tmB;
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
             bool ok = true;
             for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
                 const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
-                                           p.k_tiles, p.slices);
+                                           p.k_tiles, p.slices, C::BLOCK_N);
                 const uint32_t idesc = w.n_len < C::BLOCK_N ? idesc_half : idesc_full;
                 if (!wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
                                   seq)) {
@@ -361,8 +365,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC>::THREADS, 1)
         uint32_t seq = 0;
         for (int item = cluster; item < p.num_items; item += num_clusters, ++seq) {
             const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
-                                       p.k_tiles, p.slices);
-            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC);
+                                       p.k_tiles, p.slices, C::BLOCK_N);
+            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
             const int chunks = w.n_len / C::EPI_N;
             const int32_t row0 = o.d_row + consumer * C::MMA_M + quarter * 32;
             const int32_t col0 = o.d_col;

@@ -82,8 +82,8 @@ GEMM_HD int32_t auto_raster_group(int32_t num_m, int64_t K, int32_t tile_m) {
 struct WorkItem {
     int32_t m_idx;
     int32_t n_idx;
-    int32_t n_off;    // 0, or 128 for the second half of a split tile
-    int32_t n_len;    // 256, or 128 for a half tile
+    int32_t n_off;    // 0, or bn / 2 for the second half of a split tile
+    int32_t n_len;    // the tile width bn, or bn / 2 for a half tile
     int32_t slice;    // K slice of a split-K tile (0 without split-K)
     int32_t kt_begin; // first and one-past-last 64-wide K tile of the item
     int32_t kt_end;
@@ -93,8 +93,9 @@ struct WorkItem {
 // split_from on are the two halves of tiles split_from, split_from + 1, ...
 // With slices > 1 (split-K; nothing is then split along N) item t*slices + s
 // is K slice s of tile t: K tiles [s*k_tiles/slices, (s+1)*k_tiles/slices).
+// Tiles are bn columns wide (256, or 64 for the narrow small-problem tiles).
 GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t group, int32_t split_from,
-                         int32_t k_tiles = 0, int32_t slices = 1) {
+                         int32_t k_tiles = 0, int32_t slices = 1, int32_t bn = 256) {
     if (slices > 1) {
         const int32_t t = item / slices;
         const int32_t sl = item - t * slices;
@@ -103,7 +104,7 @@ GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t gro
         w.m_idx = c.m_idx;
         w.n_idx = c.n_idx;
         w.n_off = 0;
-        w.n_len = 256;
+        w.n_len = bn;
         w.slice = sl;
         w.kt_begin = static_cast<int32_t>(static_cast<int64_t>(sl) * k_tiles / slices);
         w.kt_end = static_cast<int32_t>(static_cast<int64_t>(sl + 1) * k_tiles / slices);
@@ -120,8 +121,8 @@ GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t gro
     WorkItem w;
     w.m_idx = c.m_idx;
     w.n_idx = c.n_idx;
-    w.n_off = half < 0 ? 0 : 128 * half;
-    w.n_len = half < 0 ? 256 : 128;
+    w.n_off = half < 0 ? 0 : (bn / 2) * half;
+    w.n_len = half < 0 ? bn : bn / 2;
     w.slice = 0;
     w.kt_begin = 0;
     w.kt_end = k_tiles;
@@ -156,7 +157,8 @@ GEMM_HD int32_t split_point(int32_t num_tiles, int32_t clusters) {
 // Where one CTA of a work item reads and writes (TIRx notes V8, "Operand
 // Partition", "Output Ownership", "Epilogue Column Address").  An item covers
 // (128 * cg * nc) rows x n_len columns of D, nc being the number of MMA
-// consumers (TIRx notes V9: two consumers stack their 128*cg rows along M).
+// consumers (TIRx notes V9: two consumers stack their 128*cg rows along M),
+// in a grid of tiles bn columns wide.
 // CTA `rank` loads, for consumer c, A rows a_row + c*128*cg .. +128 and the
 // shared B rows b_row .. +n_len/cg, and writes D rows d_row + c*128*cg .. +128
 // over all n_len columns from d_col: the rank selects the A rows and the
@@ -168,10 +170,10 @@ struct CtaOrigin {
     int32_t d_col;
 };
 
-GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank, int32_t nc = 1) {
+GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank, int32_t nc = 1, int32_t bn = 256) {
     CtaOrigin o;
     const int32_t m_base = w.m_idx * 128 * cg * nc;
-    const int32_t n_base = w.n_idx * 256 + w.n_off;
+    const int32_t n_base = w.n_idx * bn + w.n_off;
     o.a_row = m_base + rank * 128;
     o.b_row = n_base + rank * (w.n_len / cg);
     o.d_row = o.a_row;

@@ -59,7 +59,9 @@ typedef enum gemm_status {
  *                 1: each CTA computes a 128 x 256 tile alone (Step 7 / V7).
  *                 0 (default): 1 when the K-loop is at most 8 tiles of 64 and
  *                 the pair tiles would occupy at most half the co-resident
- *                 pairs (small, latency-bound problems), else 2.
+ *                 pairs (small, latency-bound problems), else 2.  With both
+ *                 cta_group and block_n at 0, small problems may instead take
+ *                 the narrow tiles of block_n 64.
  *   max_clusters  cap on the persistent grid, in clusters (CTA pairs for
  *                 cta_group 2); 0 = as many as are co-resident on the device.
  *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes
@@ -85,6 +87,16 @@ typedef enum gemm_status {
  *                 two consumers share each staged B tile, 512 x 256 tiles
  *                 ("GEMM III", Step 9; TIRx notes V9), one accumulator per
  *                 consumer.  Other values: GEMM_ERR_INVALID_ARG.
+ *   block_n       tile width in columns of D.  256: the tiles above.  64
+ *                 (needs cta_group 0 or 1 and one consumer): single CTAs
+ *                 with 128 x 64 tiles and an 8-stage ring (all of a K up to
+ *                 512 in flight after one load latency), D stored straight
+ *                 from registers; for small, latency-bound problems.  Not on
+ *                 the pages: they fix the tile at 128 or 256 x 256.  0
+ *                 (default): 64 when cta_group is 0, the K-loop is at most 8
+ *                 tiles of 64 and the 128 x 64 tiles fit one wave of
+ *                 co-resident CTAs, else 256.  Other values:
+ *                 GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;
@@ -94,6 +106,7 @@ typedef struct gemm_f16_options {
     int64_t timeout_ns;
     int32_t overlap_launch;
     int32_t consumers;
+    int32_t block_n;
 } gemm_f16_options;
 
 /*
@@ -126,8 +139,10 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
  * library split the K-loop across CTA pairs when the output has few tiles
  * (split-K: at most a quarter as many 256x256 tiles as co-resident pairs, and
  * at least 32 K tiles of 64; the pages' persistent scheduler, TIRx notes V6,
- * would otherwise leave most SMs idle for the whole K-loop).  K is then cut
- * into S slices (4..16); each slice's fp32 partial sums go to the workspace
+ * would otherwise leave most SMs idle for the whole K-loop).  With the default
+ * options a problem whose narrow 128 x 64 tiles fit one wave (see block_n)
+ * takes those instead, unless the split would cut K into at least 8 slices.
+ * K is then cut into S slices (4..16); each slice's fp32 partial sums go to the workspace
  * as [S][M][N] fp32 and a second kernel on `stream` adds them in fp32 and
  * rounds once to fp16.  `workspace` is a device pointer, 16-byte aligned,
  * owned by the caller, needing no initialisation; its contents are scratch
@@ -182,6 +197,30 @@ int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f
 int gemm_f16_nt_static_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
                           const gemm_f16_options *opts);
 
+/* What a call would launch (see gemm_f16_nt_describe()). */
+typedef struct gemm_f16_launch_info {
+    int32_t cta_group;        /* 1 or 2 */
+    int32_t consumers;        /* 1 or 2 */
+    int32_t block_n;          /* tile width: 256 or 64 */
+    int32_t split_k;          /* K slices S (1 = no split-K; > 1 adds the reduction kernel) */
+    int64_t clusters;         /* persistent clusters in the grid (CTAs = clusters * cta_group) */
+    int64_t work_items;       /* tiles, half tiles or K slices dealt to the clusters */
+    int64_t workspace_bytes;  /* split-K partials, 0 without split-K */
+} gemm_f16_launch_info;
+
+/*
+ * The configuration gemm_f16_nt_ex() (with_workspace 0) or gemm_f16_nt_ws()
+ * with a large enough workspace (with_workspace 1) would launch for these
+ * arguments on the current device, without launching anything: the choices
+ * described under gemm_f16_options, resolved.  Makes the same per-device
+ * set-up as the first GEMM call.  Not on the pages.  Returns GEMM_OK and
+ * fills *out (all zero when M, N or K is 0: then nothing, or only a fill of D
+ * with zeros, is launched), or the errors of gemm_f16_nt_workspace_size(),
+ * and GEMM_ERR_INVALID_ARG for a null `out` or with_workspace not 0 or 1.
+ */
+int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts, int32_t with_workspace,
+                         gemm_f16_launch_info *out);
+
 /*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a wait inside a kernel ran out
@@ -198,8 +237,8 @@ const char *gemm_f16_status_string(int status);
 
 /* One unit of work of a persistent cluster (see gemm_f16_nt_schedule()). */
 typedef struct gemm_f16_work_item {
-    int64_t m_idx, n_idx;     /* the tile: rows m_idx * 128*cta_group*consumers, columns n_idx * 256 */
-    int64_t n_off, n_len;     /* columns n_off .. n_off + n_len of that tile (256, or a 128 half) */
+    int64_t m_idx, n_idx;     /* the tile: rows m_idx * 128*cta_group*consumers, columns n_idx * block_n */
+    int64_t n_off, n_len;     /* columns n_off .. n_off + n_len of that tile (block_n, or a half) */
     int64_t slice;            /* K slice under split-K, else 0 */
     int64_t kt_begin, kt_end; /* 64-wide K tiles [kt_begin, kt_end) */
 } gemm_f16_work_item;
@@ -207,7 +246,9 @@ typedef struct gemm_f16_work_item {
 /*
  * The persistent scheduler, as a pure host query (no CUDA call); the kernel
  * runs the same code.  D is cut into tiles of (128 * cta_group * consumers)
- * rows x 256 columns (consumers 0 means 1), ordered in groups of
+ * rows x block_n columns (consumers 0 means 1; block_n 0 means 256, and 64,
+ * the narrow tiles of gemm_f16_options, needs cta_group 0 or 1, which then
+ * means 1, and one consumer), ordered in groups of
  * `raster_group` M-tiles (0 = the shape-derived default described under
  * gemm_f16_options): M fastest inside a group, then N, then the next group
  * (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters
@@ -217,11 +258,12 @@ typedef struct gemm_f16_work_item {
  * 148 CTAs leave 6.9 tiles per CTA, i.e. a partly idle last wave).  With
  * split_k = 1 (what gemm_f16_nt_ws() does given enough workspace) and few
  * tiles, K is instead cut into slices: item t*S + s is slice s of tile t.
+ * Narrow tiles are never split, along N or K.
  * Cluster `cluster_id` takes work items cluster_id, cluster_id + P, ...
  * Returns 1 and fills *out with the iter-th item of that cluster, 0 if the
  * cluster has no iter-th item, or GEMM_ERR_INVALID_ARG for bad arguments.
  */
-int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers,
+int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers, int32_t block_n,
                          int32_t raster_group, int32_t split_k, int64_t num_clusters, int64_t cluster_id, int64_t iter,
                          gemm_f16_work_item *out);
 
@@ -229,19 +271,22 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
  * Where CTA `rank` of a work item reads and writes, as a pure host query (no
  * CUDA call); the kernel uses the same function.  TIRx notes V8, "Operand
  * Partition" and "Output Ownership": with m_base = m_idx * 128 * cta_group *
- * consumers and n_base = n_idx * 256 + n_off, the CTA loads A rows a_row =
+ * consumers and n_base = n_idx * block_n + n_off, the CTA loads A rows a_row =
  * m_base + 128 * rank (128 rows; consumer c's block lies c * 128 * cta_group
  * rows further, TIRx notes V9) and B rows b_row = n_base + (n_len / cta_group)
  * * rank (n_len / cta_group rows, shared by the consumers), and writes D rows
  * d_row = a_row (128 rows per consumer) over the n_len columns starting at
- * d_col = n_base ("Epilogue Column Address": no rank term).  n_len is 256 (whole tile, n_off 0) or 128 (half tile, n_off 0 or
- * 128).  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not 0/1/2,
- * consumers not 0/1/2 or 2 without a pair, rank out of range, bad
- * n_off/n_len, negative or too large indices, null outputs).
+ * d_col = n_base ("Epilogue Column Address": no rank term).  block_n is 0
+ * (meaning 256) or 256: n_len is 256 (whole tile, n_off 0) or 128 (half tile,
+ * n_off 0 or 128); or 64 (narrow tiles, cta_group 0 or 1, one consumer):
+ * n_len 64, n_off 0.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not
+ * 0/1/2, consumers not 0/1/2 or 2 without a pair, block_n not 0/64/256 or 64
+ * with a pair or two consumers, rank out of range, bad n_off/n_len, negative
+ * or too large indices, null outputs).
  */
-int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int64_t m_idx, int64_t n_idx, int64_t n_off,
-                           int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row, int64_t *d_row,
-                           int64_t *d_col);
+int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int64_t m_idx, int64_t n_idx,
+                           int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
+                           int64_t *d_row, int64_t *d_col);
 
 /*
  * The stage/phase bookkeeping of one SMEM or TMEM ring, run on the host with

@@ -7,6 +7,7 @@
   the kernel runs — against the pages' worked examples (tests/golden) and
   against exhaustive properties (bijection, ownership).
 """
+import ctypes
 import os
 import random
 import re
@@ -78,7 +79,8 @@ def test_argument_errors_are_returned_before_any_launch():
     assert lib.gemm_f16_nt_ws(None, None, None, 0, 128, 64, None, 0, None, None) == OK
     for bad in (g.Options(cta_group=3), g.Options(max_clusters=-1), g.Options(raster_group=-2),
                 g.Options(debug_flags=2), g.Options(timeout_ns=-5), g.Options(overlap_launch=2),
-                g.Options(consumers=3), g.Options(cta_group=1, consumers=2)):
+                g.Options(consumers=3), g.Options(cta_group=1, consumers=2), g.Options(block_n=128),
+                g.Options(block_n=32), g.Options(block_n=64, cta_group=2), g.Options(block_n=64, consumers=2)):
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
 
@@ -90,6 +92,22 @@ def test_no_device_reported_without_gpu():
     assert lib.gemm_f16_nt(0x10000, 0x20000, 0x30000, 128, 128, 64, None) == NO_DEVICE
     assert lib.gemm_f16_nt_workspace_size(256, 256, 4096, None) == NO_DEVICE
     assert lib.gemm_f16_nt_workspace_size(256, 12, 4096, None) == UNSUPPORTED
+    info = g.LaunchInfo()
+    assert lib.gemm_f16_nt_describe(128, 128, 64, None, 0, ctypes.byref(info)) == NO_DEVICE
+
+
+def test_describe_validates_before_touching_a_device():
+    lib = g.load()
+    info = g.LaunchInfo()
+    assert lib.gemm_f16_nt_describe(-1, 8, 8, None, 0, ctypes.byref(info)) == INVALID
+    assert lib.gemm_f16_nt_describe(128, 12, 64, None, 0, ctypes.byref(info)) == UNSUPPORTED
+    assert lib.gemm_f16_nt_describe(128, 128, 64, None, 2, ctypes.byref(info)) == INVALID
+    assert lib.gemm_f16_nt_describe(128, 128, 64, None, 0, None) == INVALID
+    assert lib.gemm_f16_nt_describe(128, 128, 64, ctypes.byref(g.Options(block_n=64, cta_group=2)), 0,
+                                    ctypes.byref(info)) == INVALID
+    # an empty product launches no GEMM: all zero, no device needed
+    assert g.describe(0, 128, 64) == dict(cta_group=0, consumers=0, block_n=0, split_k=0, clusters=0, work_items=0,
+                                          workspace_bytes=0)
 
 
 def test_status_strings():
@@ -209,6 +227,48 @@ def test_schedule_splits_the_last_wave_of_4096():
     # split_k does not change a shape with this many tiles
     assert all(g.schedule(4096, 4096, 2, 8, 76, c, it, split_k=1) == w for c, it, w in items)
     assert sum(1 for c, it, w in items if it == 3) == 56
+
+
+@pytest.mark.parametrize("M,N,K,clusters", [
+    (128, 128, 64, 152), (256, 256, 512, 152), (1024, 1024, 512, 152), (300, 520, 256, 7), (1, 8, 8, 1),
+    (4096, 4096, 4096, 152), (1000, 7000, 512, 13),
+])
+def test_narrow_schedule_covers_every_output_once(M, N, K, clusters):
+    """Narrow tiles (block_n 64): every 128 x 64 tile is one work item, never split along N or K,
+    dealt round-robin over the clusters, also when split-K is asked for."""
+    num_m, num_n = -(-M // 128), -(-N // 64)
+    k_tiles = -(-K // 64)
+    cover = {}
+    for c in range(clusters):
+        it = 0
+        while (w := g.schedule(M, N, 1, 0, clusters, c, it, K=K, block_n=64, split_k=1)) is not None:
+            m_idx, n_idx, n_off, n_len, sl, kb, ke = w
+            assert (n_off, n_len, sl, kb, ke) == (0, 64, 0, 0, k_tiles)
+            assert 0 <= m_idx < num_m and 0 <= n_idx < num_n
+            assert (m_idx, n_idx) not in cover
+            cover[(m_idx, n_idx)] = c
+            it += 1
+        assert it == len(range(c, num_m * num_n, clusters))
+    assert len(cover) == num_m * num_n
+    # cta_group 0 means 1 for narrow tiles; a pair or two consumers are refused
+    assert g.schedule(M, N, 0, 0, clusters, 0, 0, K=K, block_n=64) == g.schedule(M, N, 1, 0, clusters, 0, 0, K=K,
+                                                                                   block_n=64)
+    for cg, consumers in ((2, 1), (2, 2)):
+        with pytest.raises(g.GemmError):
+            g.schedule(M, N, cg, 0, clusters, 0, 0, K=K, consumers=consumers, block_n=64)
+    with pytest.raises(g.GemmError):
+        g.schedule(M, N, 1, 0, clusters, 0, 0, K=K, block_n=128)
+
+
+def test_narrow_cta_origin():
+    # a 128 x 64 tile: A rows and D rows from m_idx * 128, B rows and D columns from n_idx * 64
+    assert g.cta_origin(1, 3, 5, 0, n_len=64, block_n=64) == dict(a_row=384, b_row=320, d_row=384, d_col=320)
+    assert g.cta_origin(0, 0, 1, 0, n_len=64, block_n=64) == dict(a_row=0, b_row=64, d_row=0, d_col=64)
+    for bad in (dict(n_len=256), dict(n_len=32), dict(n_len=64, n_off=32)):
+        with pytest.raises(g.GemmError):
+            g.cta_origin(1, 0, 0, 0, block_n=64, **{"n_off": 0, **bad})
+    with pytest.raises(g.GemmError):
+        g.cta_origin(2, 0, 0, 0, n_len=64, block_n=64)
 
 
 def test_cta_origin_matches_the_pages_operand_partition():

@@ -1,0 +1,57 @@
+"""Which kernel configuration a call resolves to on a GB300 (gemm_f16_nt_describe).
+
+The choices are host logic, but they depend on how many CTAs and CTA pairs are
+co-resident on the device, so they are checked here, on the GPU, for the five
+workloads and the boundaries between configurations.  Each configuration's
+results are checked against the oracle elsewhere; these tests pin which one
+runs.
+"""
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+def test_small_problems_take_narrow_tiles(gpu_lib):
+    c1 = gpu_lib.describe(128, 128, 64)
+    assert (c1["cta_group"], c1["block_n"], c1["split_k"], c1["clusters"], c1["work_items"]) == (1, 64, 1, 2, 2)
+    c2 = gpu_lib.describe(256, 256, 512)
+    assert (c2["cta_group"], c2["block_n"], c2["split_k"], c2["clusters"], c2["work_items"]) == (1, 64, 1, 8, 8)
+    # one wave of 128 x 64 tiles, any K, without a workspace
+    for M, N, K in ((1024, 1024, 1024), (1024, 1024, 4096), (256, 256, 4096), (128, 4096, 2048)):
+        c = gpu_lib.describe(M, N, K)
+        assert c["block_n"] == 64 and c["work_items"] == -(-M // 128) * -(-N // 64), (M, N, K)
+        assert c["clusters"] == c["work_items"] and c["workspace_bytes"] == 0
+
+
+def test_more_than_one_wave_keeps_256_wide_tiles(gpu_lib):
+    wide = gpu_lib.describe(2048, 1024, 512)  # 256 narrow tiles: more than one wave
+    assert (wide["cta_group"], wide["block_n"]) == (1, 256)
+    big = gpu_lib.describe(4096, 4096, 4096)
+    assert (big["cta_group"], big["consumers"], big["block_n"], big["split_k"]) == (2, 1, 256, 1)
+    P, T = big["clusters"], 256
+    r = T % P
+    assert big["work_items"] == (T + r if 0 < 2 * r <= P else T)
+    assert big["clusters"] >= 70  # GB300: 152 SMs, 76 co-resident pairs
+
+
+def test_split_k_wins_only_with_at_least_8_slices(gpu_lib):
+    deep = gpu_lib.describe(256, 256, 4096, with_workspace=True)
+    assert (deep["cta_group"], deep["block_n"], deep["split_k"]) == (2, 256, 8)
+    assert deep["workspace_bytes"] == 8 * 256 * 256 * 4 == gpu_lib.workspace_size(256, 256, 4096)
+    shallow = gpu_lib.describe(1024, 1024, 4096, with_workspace=True)  # 4 slices: narrow tiles instead
+    assert shallow["block_n"] == 64 and shallow["split_k"] == 1 and gpu_lib.workspace_size(1024, 1024, 4096) == 0
+
+
+def test_explicit_options_are_obeyed(gpu_lib):
+    single = gpu_lib.describe(128, 128, 64, gpu_lib.Options(cta_group=1))
+    assert (single["cta_group"], single["block_n"]) == (1, 256)
+    pair = gpu_lib.describe(128, 128, 64, gpu_lib.Options(cta_group=2))
+    assert (pair["cta_group"], pair["block_n"]) == (2, 256)
+    two = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(consumers=2))
+    assert (two["cta_group"], two["consumers"], two["block_n"]) == (2, 2, 256)
+    narrow = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(block_n=64))
+    assert (narrow["cta_group"], narrow["block_n"], narrow["work_items"]) == (1, 64, 32 * 64)
+    capped = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(max_clusters=5))
+    assert capped["clusters"] == 5

@@ -95,7 +95,7 @@ def test_static_scratch_without_split_k(gpu_lib):
 
 def test_static_scratch_refuses_what_does_not_fit(gpu_lib):
     lib = gpu_lib.load()
-    M, N, K = 768, 1536, 4096  # 18 tiles, 4 K slices: 4 x 768 x 1536 x 4 B = 18 MiB of scratch
+    M, N, K = 768, 768, 4096  # 9 pair tiles, 8 K slices: 8 x 768 x 768 x 4 B = 18 MiB of scratch
     need = lib.gemm_f16_nt_workspace_size(M, N, K, None)
     if need <= STATIC_BYTES:
         pytest.skip(f"on this device the shape needs only {need} bytes")
