@@ -172,10 +172,10 @@ def oracle_rows_tflops(A, B, rows: int, threads: int):
     return 2.0 * rows * B.shape[0] * A.shape[1] / dt / 1e12, dt
 
 
-def cpu_baseline(A, B, target_s: float = 12.0) -> dict:
-    threads = os.cpu_count() or 1
-    # two-point calibration: each call decodes all of B once (fixed cost), then
-    # costs the same per row of D
+def oracle_rows_calibrated(A, B, threads: int, target_s: float):
+    """Time the oracle on as many full rows of D as take about target_s.  Two-point
+    calibration first: each call decodes all of B once (a fixed cost), then costs the same
+    per row.  Returns (rows, TFLOP/s, seconds, per-row seconds, fixed seconds)."""
     r1, r2 = min(A.shape[0], threads), min(A.shape[0], 4 * threads)
     _, t1 = oracle_rows_tflops(A, B, r1, threads)
     _, t2 = oracle_rows_tflops(A, B, r2, threads)
@@ -184,9 +184,40 @@ def cpu_baseline(A, B, target_s: float = 12.0) -> dict:
     rows = int((target_s - fixed) / per_row)
     rows = min(A.shape[0], max(r2, (rows // threads) * threads))
     v, dt = oracle_rows_tflops(A, B, rows, threads)
+    return rows, v, dt, per_row, fixed
+
+
+def cpu_baseline(A, B, target_s: float = 12.0) -> dict:
+    threads = os.cpu_count() or 1
+    rows, v, dt, _, _ = oracle_rows_calibrated(A, B, threads, target_s)
     return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"rows 0..{rows - 1} of D for {WORKLOAD} ({rows}x{B.shape[0]} outputs, K={A.shape[1]}), "
                       f"{dt:.1f} s on {threads} host threads"}
+
+
+def oracle_workload_timing(w, A, B, target_s: float = 1.5) -> dict:
+    """The oracle as it stands on one workload, in seconds and GFLOP/s: one host thread on the
+    whole product for the two small shapes, all host threads on a bounded number of full rows of
+    D for the large ones (then also the full product's time, scaled from the rows)."""
+    import oracle
+
+    small = w.flop < 1e9
+    threads = 1 if small else (os.cpu_count() or 1)
+    if small:
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle.gemm_f16_nt(A, B, threads=1)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= 0.2:
+                break
+        per = dt / reps
+        return {"threads": 1, "seconds": per, "gflops": w.flop / per / 1e9,
+                "sample": f"the whole product, {reps} calls"}
+    rows, tf, dt, _, _ = oracle_rows_calibrated(A, B, threads, target_s)
+    return {"threads": threads, "seconds": dt, "gflops": tf * 1e3, "full_product_seconds": dt * w.M / rows,
+            "sample": f"rows 0..{rows - 1} of D ({rows} of {w.M}); the full product's time scaled linearly "
+                      f"from the sample"}
 
 
 def run_reference(args) -> None:
@@ -230,9 +261,11 @@ def run_reference(args) -> None:
 
 # ------------------------------------------------------ all five workloads --
 
-def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float = 0.4) -> list[dict]:
+def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float = 0.4,
+                          oracle_timing: bool = False) -> list[dict]:
     """Each synthetic shape once: TFLOP/s, fraction of the tensor peak, and HBM GB/s of the
     compulsory bytes (the figure that matters for the small, latency-bound shapes).
+    With `oracle_timing` (the cpu_baseline leg) the oracle is also timed on each shape.
 
     Inputs rotate over enough device copies that one pass through them exceeds
     the 129 MB L2 (one copy when a single problem already does), so every
@@ -316,6 +349,8 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
             else:
                 res["cublas_tflops"] = tf
                 res["cublas_ms_median"] = pct["ms_median"]
+        if oracle_timing:
+            res["oracle"] = oracle_workload_timing(w, A, B)
         out.append(res)
         del Ar, Br, Dr
         torch.cuda.empty_cache()
@@ -484,7 +519,7 @@ def run_ours(args) -> None:
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(A, B)
         if world == 1 and not args.no_workloads:
-            line["workloads"] = measure_all_workloads(g, dev, peak, A, B)
+            line["workloads"] = measure_all_workloads(g, dev, peak, A, B, oracle_timing=not args.no_cpu_baseline)
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
