@@ -44,7 +44,7 @@ WORKLOAD = si.HEADLINE
 ROTATE = 4
 NOMINAL_PEAK_TFLOPS = 2250.0          # GB300 dense fp16/bf16 tensor, nominal
 FALLBACK_PEAK_TFLOPS = 1900.0         # one earlier cuBLAS bf16 measurement on a GB300
-KERNEL_NAME = "gemm_f16_nt_kernel<2>"
+KERNEL_NAME = "gemm_f16_nt_kernel<2, 1, 256>"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_gemm_f16_nt_kernel_square_4096.json")
 
 

@@ -18,9 +18,10 @@
  *     library never frees, keeps or reallocates them and allocates no device
  *     memory per call.  D must not overlap A or B.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
- *     stream).  Compute calls are asynchronous: they validate, enqueue one
- *     kernel on `stream` and return; D is ready when the stream reaches that
- *     point.
+ *     stream).  Compute calls are asynchronous: they validate, enqueue their
+ *     kernel on `stream` (two with split-K, the GEMM and the reduction; a fill
+ *     of D with zeros when K is 0) and return; D is ready when the stream
+ *     reaches that point.
  *   - Errors are negative gemm_status_t values.  An argument error is reported
  *     before anything is enqueued and leaves D untouched.  A failure inside a
  *     running kernel (a bounded wait that ran out) is reported by
