@@ -156,8 +156,7 @@ class ClockSampler:
         reasons = sorted({names[i] for p in inside for i in range(4) if p[4 + i].lower().startswith("active")})
         power = [num(p[2]) for p in inside if num(p[2]) is not None]
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(inside[0][1]),
-                "reasons": reasons, "power_w_max": max(power) if power else None,
-                "power_w_median": statistics.median(power) if power else None, "samples": len(inside),
+                "reasons": reasons, "power_w_max": max(power) if power else None, "samples": len(inside),
                 "note": note}
 
 
@@ -459,11 +458,11 @@ def run_ours(args) -> None:
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_tflops(flop, args.steps, world, elapsed_ms)
     per_gpu_tflops = flop / (ms_per_step * 1e-3) / 1e12
-    if clocks and clocks.get("sm_mhz") and clocks.get("power_w_median"):
-        # under the power cap the clock follows the power: work per clock and per joule
-        # are what a kernel decides
+    if clocks and clocks.get("sm_mhz"):
+        # under the power cap the clock follows the power: the work done per clock is what
+        # the kernel decides (nvidia-smi's power reading averages over about a second, too
+        # long for a per-joule figure over this timed region)
         clocks["tflops_per_ghz"] = per_gpu_tflops / (clocks["sm_mhz"] / 1000.0)
-        clocks["gflop_per_joule"] = per_gpu_tflops * 1000.0 / clocks["power_w_median"]
 
     # cuBLAS (torch.matmul) on the same rotation, as a reference point
     cublas = None
