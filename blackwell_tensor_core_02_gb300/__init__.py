@@ -147,7 +147,12 @@ def _workspace_for(nbytes: int, device, stream):
     key = (device.index if device.index is not None else torch.cuda.current_device(), stream)
     buf = _workspaces.get(key)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
+        # Allocate on the stream that uses the buffer: torch's caching allocator then hands
+        # this memory (or the smaller buffer it replaces) to later allocations only in that
+        # stream's order, after the GEMMs already queued there.
+        s = torch.cuda.ExternalStream(stream, device=device) if stream else torch.cuda.default_stream(device)
+        with torch.cuda.stream(s):
+            buf = torch.empty(max(nbytes, 1 << 20), dtype=torch.uint8, device=device)
         _workspaces[key] = buf
     return buf
 

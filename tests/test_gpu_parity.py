@@ -156,6 +156,26 @@ def test_split_k_full(gpu_lib, M, N, K, cg):
     assert_close(gpu_lib.gemm_f16_nt(dA, dB, options=o).cpu().numpy(), ref, "binding")
 
 
+def test_binding_workspace_on_a_side_stream(gpu_lib):
+    # The binding's cached split-K workspace belongs to the stream the call runs on; a larger
+    # problem on the same stream replaces it while the first GEMM may still be queued.
+    side = torch.cuda.Stream()
+    shapes = [(256, 256, 4096), (512, 512, 4096)]  # 2 MiB, then 8 MiB of partials
+    outs = []
+    for i, (M, N, K) in enumerate(shapes):
+        assert gpu_lib.workspace_size(M, N, K) > 0
+        A, B = si.custom(M, N, K, seed=700 + i).operands()
+        dA, dB = to_dev(A), to_dev(B)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            D = gpu_lib.gemm_f16_nt(dA, dB, stream=side)
+        outs.append((A, B, D))
+    side.synchronize()
+    assert gpu_lib.last_device_status(side.cuda_stream)[0] == 0
+    for A, B, D in outs:
+        assert_close(D.cpu().numpy(), oracle.gemm_f16_nt(A, B), f"side stream {A.shape[0]}x{B.shape[0]}")
+
+
 def test_guard_bands_and_full_overwrite(gpu_lib):
     # D sits inside a larger buffer filled with a NaN sentinel: every element of
     # D must be written, and nothing before or after it.
