@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -48,14 +49,23 @@ KERNEL_NAME = "gemm_f16_nt_kernel<2, 1, 256>"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_gemm_f16_nt_kernel_square_4096.json")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources: the ncu traffic figure is only valid for the kernel it was taken on."""
+def source_code_only(text: str) -> str:
+    """C/C++/CUDA source with comments removed and whitespace collapsed (the sources hold no
+    comment markers inside string literals)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(csrc: str | None = None) -> str:
+    """Hash of the CUDA sources' code (comments and layout ignored): the ncu traffic figure is
+    only valid for the kernel it was taken on."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "blackwell_tensor_core_02_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "blackwell_tensor_core_02_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+            with open(os.path.join(csrc, name), encoding="utf-8") as f:
+                h.update(name.encode() + b"\0" + source_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -44,6 +44,11 @@
 // drain consumer 0 and warps 8-11 consumer 1.  Its epilogue writes D from
 // registers (the SMEM goes to four 48 KiB stages).
 //
+// Narrow tiles (BN = 64, CG = 1, NC = 1): for problems whose 128 x 64 tiles fit
+// one wave of CTAs.  Same roles; an 8-stage ring of 24 KiB stages holds a K of
+// 512 at once, TMEM is 128 columns (two 64-column accumulators), and the
+// epilogue writes D from registers.  Not on the pages, which fix the tile.
+//
 // Split-K (NC = 1): with very few tiles, item t*S + s runs K slice s of tile
 // t and its epilogue writes the fp32 partial sum of that slice to a workspace
 // [S][M][N]; splitk_reduce_kernel then adds the S partials in fp32 and rounds
