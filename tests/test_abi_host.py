@@ -318,16 +318,20 @@ def test_pipeline_state_matches_the_pages_table():
         g.pipeline_trace(0, 0, 1)
 
 
-def _simulate_ring(depth, producer_phase, steps, seed):
-    """Model one SMEM ring with parity barriers, driven by the library's PipelineState traces.
+def _simulate_ring(depth, producer_phase, steps, seed, traces=None):
+    """Model one SMEM ring with parity barriers, driven by the library's PipelineState traces
+    (or by the given (producer, consumer) traces).
 
     try_wait(bar, p) passes when the barrier's phase bit differs from p
     ("GEMM I", the phase-flip table).  A fill completes full[s]'s phase; a
     consume completes empty[s]'s phase.  Returns the consumed sequence, or None
     on deadlock.
     """
-    prod = g.pipeline_trace(depth, producer_phase, steps)
-    cons = g.pipeline_trace(depth, 0, steps)
+    if traces is None:
+        prod = g.pipeline_trace(depth, producer_phase, steps)
+        cons = g.pipeline_trace(depth, 0, steps)
+    else:
+        prod, cons = traces
     full, empty = [0] * depth, [0] * depth
     slot = [None] * depth
     i = j = 0
@@ -357,3 +361,23 @@ def test_opposite_initial_phases_model():
             assert _simulate_ring(depth, 1, 50, seed) == list(range(50))
     # the pages' "subtlest bug": both ends at phase 0 deadlock on the fresh barrier
     assert _simulate_ring(4, 0, 50, 0) is None
+
+
+def test_forgotten_phase_toggle_corrupts_silently():
+    """The pages' other ring bug ("GEMM I", the phase-flip table): a PipelineState that wraps
+    its stage but never flips its phase.  Planted in the model, not in a kernel.  After the
+    first lap a wait compares against a phase bit that a later fill or drain may already have
+    flipped back, so depending on the interleaving the ring either stalls or, worse, runs to
+    the end with the consumer reading slots that hold other fills than the ones it expects
+    (e.g. fills 0-3 twice, never 4-7).  No interleaving delivers the right data."""
+    depth, steps = 4, 40
+    stuck = lambda phase: [(i % depth, phase) for i in range(steps)]  # noqa: E731
+    silent = 0
+    for seed in range(40):
+        out = _simulate_ring(depth, 1, steps, seed, traces=(stuck(1), stuck(0)))
+        assert out != list(range(steps))
+        silent += out is not None
+    assert silent > 0, "some interleavings finish with wrong data and nothing to notice it by"
+    # the library's traces, same seeds: always in order
+    for seed in range(40):
+        assert _simulate_ring(depth, 1, steps, seed) == list(range(steps))
