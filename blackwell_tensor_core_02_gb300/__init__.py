@@ -25,7 +25,7 @@ __all__ = [
 STATUS = {
     0: "GEMM_OK", -1: "GEMM_ERR_INVALID_ARG", -2: "GEMM_ERR_UNSUPPORTED_SHAPE", -3: "GEMM_ERR_MISALIGNED",
     -4: "GEMM_ERR_NO_DEVICE", -5: "GEMM_ERR_ARCH", -6: "GEMM_ERR_LAUNCH", -7: "GEMM_ERR_DEVICE_TIMEOUT",
-    -8: "GEMM_ERR_CUDA", -9: "GEMM_ERR_SCRATCH_LIMIT",
+    -8: "GEMM_ERR_CUDA", -9: "GEMM_ERR_SCRATCH_LIMIT", -10: "GEMM_ERR_DEVICE_BOUNDS",
 }
 
 
@@ -58,43 +58,59 @@ _lock = threading.Lock()
 _lib: ctypes.CDLL | None = None
 
 
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    """Argument and result types of every C entry point."""
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    i64p, i32p = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
+    lib.gemm_f16_nt.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    lib.gemm_f16_nt.restype = ctypes.c_int
+    lib.gemm_f16_nt_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+    lib.gemm_f16_nt_ex.restype = ctypes.c_int
+    lib.gemm_f16_nt_supported.argtypes = [i64, i64, i64]
+    lib.gemm_f16_nt_supported.restype = ctypes.c_int
+    lib.gemm_f16_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+    lib.gemm_f16_last_device_status.restype = ctypes.c_int
+    lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
+    lib.gemm_f16_status_string.restype = ctypes.c_char_p
+    lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i64, i64, i64,
+                                         ctypes.POINTER(WorkItem)]
+    lib.gemm_f16_nt_schedule.restype = ctypes.c_int
+    lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
+    lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
+    lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, vp, ctypes.POINTER(Options)]
+    lib.gemm_f16_nt_ws.restype = ctypes.c_int
+    lib.gemm_f16_nt_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Options)]
+    lib.gemm_f16_nt_workspace_size.restype = ctypes.c_int64
+    lib.gemm_f16_nt_static_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
+    lib.gemm_f16_nt_static_ws.restype = ctypes.c_int
+    lib.gemm_f16_nt_describe.argtypes = [i64, i64, i64, ctypes.POINTER(Options), i32, ctypes.POINTER(LaunchInfo)]
+    lib.gemm_f16_nt_describe.restype = ctypes.c_int
+    lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
+    lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
+    return lib
+
+
 def load() -> ctypes.CDLL:
     """Build (if stale) and load the CUDA library; raise if that is impossible."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.build()
-        lib = ctypes.CDLL(path)
-        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-        i64p, i32p = ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int32)
-        lib.gemm_f16_nt.argtypes = [vp, vp, vp, i64, i64, i64, vp]
-        lib.gemm_f16_nt.restype = ctypes.c_int
-        lib.gemm_f16_nt_ex.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
-        lib.gemm_f16_nt_ex.restype = ctypes.c_int
-        lib.gemm_f16_nt_supported.argtypes = [i64, i64, i64]
-        lib.gemm_f16_nt_supported.restype = ctypes.c_int
-        lib.gemm_f16_last_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
-        lib.gemm_f16_last_device_status.restype = ctypes.c_int
-        lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
-        lib.gemm_f16_status_string.restype = ctypes.c_char_p
-        lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i64, i64, i64,
-                                             ctypes.POINTER(WorkItem)]
-        lib.gemm_f16_nt_schedule.restype = ctypes.c_int
-        lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
-        lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
-        lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, vp, ctypes.POINTER(Options)]
-        lib.gemm_f16_nt_ws.restype = ctypes.c_int
-        lib.gemm_f16_nt_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Options)]
-        lib.gemm_f16_nt_workspace_size.restype = ctypes.c_int64
-        lib.gemm_f16_nt_static_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, ctypes.POINTER(Options)]
-        lib.gemm_f16_nt_static_ws.restype = ctypes.c_int
-        lib.gemm_f16_nt_describe.argtypes = [i64, i64, i64, ctypes.POINTER(Options), i32, ctypes.POINTER(LaunchInfo)]
-        lib.gemm_f16_nt_describe.restype = ctypes.c_int
-        lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
-        lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
-        _lib = lib
-        return lib
+        _lib = _declare(ctypes.CDLL(_build.build()))
+        return _lib
+
+
+_checked: ctypes.CDLL | None = None
+
+
+def load_checked() -> ctypes.CDLL:
+    """The checked build of the same library (device range checks compiled in; for tests).
+    It is a separate shared object with its own device code and status word."""
+    global _checked
+    with _lock:
+        if _checked is None:
+            _checked = _declare(ctypes.CDLL(_build.build(checked=True)))
+        return _checked
 
 
 def status_string(code: int) -> str:

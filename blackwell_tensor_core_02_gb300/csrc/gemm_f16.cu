@@ -524,6 +524,8 @@ const char *gemm_f16_status_string(int status) {
         case GEMM_ERR_LAUNCH: return "GEMM_ERR_LAUNCH: kernel launch failed";
         case GEMM_ERR_DEVICE_TIMEOUT: return "GEMM_ERR_DEVICE_TIMEOUT: a wait inside the kernel ran out";
         case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA runtime or driver error";
+        case GEMM_ERR_DEVICE_BOUNDS:
+            return "GEMM_ERR_DEVICE_BOUNDS: a range check inside the kernel failed (checked build)";
         case GEMM_ERR_SCRATCH_LIMIT:
             return "GEMM_ERR_SCRATCH_LIMIT: the split-K scratch this problem needs exceeds the library's fixed "
                    "16 MiB scratch array (use gemm_f16_nt_ws with a larger workspace)";

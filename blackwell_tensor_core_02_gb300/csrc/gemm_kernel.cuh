@@ -69,8 +69,20 @@ namespace gemm_f16 {
 __device__ int g_status;              // first error code of any CTA (0 = none)
 __device__ unsigned long long g_info; // where it happened (role, CTA, tile seq)
 
-enum : int { kStatusTimeout = -7 };
+enum : int { kStatusTimeout = -7, kStatusBounds = -10 };
 enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
+
+// The checked build (-DGEMM_F16_DEVICE_CHECKS=1, a second library the tests
+// load beside the production one) tests, before each access, that the work
+// item, ring stage, TMEM columns, epilogue chunk and staging buffer are in
+// range.  A failed check records kStatusBounds with (role, check, CTA, tile
+// sequence) in the status word and raises the CTA's abort flag, so the CTA
+// ends through the same path as a timed-out wait; it never traps.  In the
+// production build every check compiles to nothing.
+#ifndef GEMM_F16_DEVICE_CHECKS
+#define GEMM_F16_DEVICE_CHECKS 0
+#endif
+enum : uint32_t { kCheckItem = 1, kCheckStage = 2, kCheckTmem = 3, kCheckChunk = 4, kCheckStaging = 5 };
 
 // BN is the tile width: 256, or 64 for the narrow single-CTA tiles of small
 // problems (more CTAs, and a ring deep enough to hold a K of 512 at once).
@@ -143,6 +155,30 @@ __device__ __forceinline__ void record_failure(uint32_t role, uint32_t seq) {
         g_info = (static_cast<unsigned long long>(role) << 56) |
                  (static_cast<unsigned long long>(blockIdx.x & 0xFFFFFFu) << 32) | seq;
     }
+}
+
+__device__ __forceinline__ bool in_bounds(bool ok, volatile int *abort_flag, uint32_t role, uint32_t check,
+                                          uint32_t seq) {
+#if GEMM_F16_DEVICE_CHECKS
+    if (!ok) {
+        if (atomicCAS(&g_status, 0, kStatusBounds) == 0) {
+            g_info = (static_cast<unsigned long long>(role) << 56) | (static_cast<unsigned long long>(check) << 48) |
+                     (static_cast<unsigned long long>(blockIdx.x & 0xFFFFu) << 32) | seq;
+        }
+        *abort_flag = 1;
+        return false;
+    }
+#else
+    (void)abort_flag, (void)role, (void)check, (void)seq;
+#endif
+    return ok || !GEMM_F16_DEVICE_CHECKS;
+}
+
+// A work item the scheduler hands out: a tile inside the grid, a K range
+// inside K, columns inside the tile.
+__device__ __forceinline__ bool item_ok(const WorkItem &w, int32_t num_m, int32_t num_n, int32_t k_tiles, int32_t bn) {
+    return w.m_idx >= 0 && w.m_idx < num_m && w.n_idx >= 0 && w.n_idx < num_n && w.kt_begin >= 0 &&
+           w.kt_begin < w.kt_end && w.kt_end <= k_tiles && w.n_off >= 0 && w.n_len > 0 && w.n_off + w.n_len <= bn;
 }
 
 // Bounded wait by one thread.  Returns false if the wait ran out (the failure
@@ -272,11 +308,18 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
             for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
                 const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
                                            p.k_tiles, p.slices, C::BLOCK_N);
+                if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag,
+                               kRoleProducer, kCheckItem, seq)) {
+                    ok = false;
+                    break;
+                }
                 const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
                 const bool half = w.n_len < C::BLOCK_N;
                 const CUtensorMap *mapB = half ? &tmBh : &tmB;
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
-                    if (!wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
+                    if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleProducer, kCheckStage,
+                                   seq) ||
+                        !wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
                                       kRoleProducer, seq)) {
                         ok = false;
                         break;
@@ -320,7 +363,11 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
                 const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
                                            p.k_tiles, p.slices, C::BLOCK_N);
                 const uint32_t idesc = w.n_len < C::BLOCK_N ? idesc_half : idesc_full;
-                if (!wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
+                if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag, kRoleMma,
+                               kCheckItem, seq) ||
+                    !in_bounds(acc.stage >= 0 && (acc.stage + 1) * NC * C::BLOCK_N <= C::TMEM_COLS, abort_flag,
+                               kRoleMma, kCheckTmem, seq) ||
+                    !wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
                                   seq)) {
                     ok = false;
                     break;
@@ -328,7 +375,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
                 ptx::tcgen05_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * NC * C::BLOCK_N);
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
-                    if (!wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
+                    if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleMma, kCheckStage, seq) ||
+                        !wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
                                       seq)) {
                         ok = false;
                         break;
@@ -382,6 +430,17 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
+            if (GEMM_F16_DEVICE_CHECKS) {
+                bool fine = in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag,
+                                      kRoleEpilogue, kCheckItem, seq);
+                fine = fine && in_bounds((acc.stage * NC + consumer) * C::BLOCK_N + w.n_len <= C::TMEM_COLS,
+                                         abort_flag, kRoleEpilogue, kCheckTmem, seq);
+                fine = fine && in_bounds(chunks >= 1 && chunks <= C::BLOCK_N / C::EPI_N, abort_flag, kRoleEpilogue,
+                                         kCheckChunk, seq);
+                fine = fine && in_bounds(C::EPI_DIRECT || buf < static_cast<uint32_t>(C::EPI_BUFS), abort_flag,
+                                         kRoleEpilogue, kCheckStaging, seq);
+                if (!fine) break;
+            }
             ptx::tcgen05_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>((acc.stage * NC + consumer) * C::BLOCK_N);

@@ -48,7 +48,8 @@ typedef enum gemm_status {
     GEMM_ERR_LAUNCH = -6,            /* the kernel launch itself failed         */
     GEMM_ERR_DEVICE_TIMEOUT = -7,    /* a bounded wait inside the kernel ran out */
     GEMM_ERR_CUDA = -8,              /* another CUDA runtime/driver error        */
-    GEMM_ERR_SCRATCH_LIMIT = -9      /* gemm_f16_nt_static_ws: scratch too small  */
+    GEMM_ERR_SCRATCH_LIMIT = -9,     /* gemm_f16_nt_static_ws: scratch too small  */
+    GEMM_ERR_DEVICE_BOUNDS = -10     /* checked build only: a device range check failed */
 } gemm_status_t;
 
 /*
@@ -225,10 +226,15 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
 /*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a wait inside a kernel ran out
- * (the kernel then skipped its remaining work and exited; D is incomplete).
- * If `info` is not NULL it receives where the first failure happened:
- * bits 56-63 role (1 producer, 2 MMA issuer, 3 epilogue), 32-55 CTA index,
- * 0-31 the tile's sequence number in that CTA.  Returns GEMM_ERR_CUDA if the
+ * (the kernel then skipped its remaining work and exited; D is incomplete),
+ * or, from the checked build of the library (compiled with
+ * -DGEMM_F16_DEVICE_CHECKS=1 for tests), GEMM_ERR_DEVICE_BOUNDS if a range
+ * check inside a kernel failed.  If `info` is not NULL it receives where the
+ * first failure happened: bits 56-63 role (1 producer, 2 MMA issuer, 3
+ * epilogue), 0-31 the tile's sequence number in that CTA, and 32-55 the CTA
+ * index for a timeout, or 48-55 the check (1 work item, 2 ring stage, 3 TMEM
+ * columns, 4 epilogue chunk, 5 staging buffer) and 32-47 the CTA index for a
+ * failed range check.  Returns GEMM_ERR_CUDA if the
  * synchronisation itself reports an error.
  */
 int gemm_f16_last_device_status(void *stream, uint64_t *info);

@@ -41,11 +41,11 @@ def declared_functions():
 
 
 def test_library_exports_every_declared_function():
-    lib = g.load()
     names = declared_functions()
     assert len(names) >= 8
-    for name in names:
-        assert hasattr(lib, name), f"{name} declared in include/gemm_f16.h but not exported"
+    for lib in (g.load(), g.load_checked()):  # the production build and the checked build
+        for name in names:
+            assert hasattr(lib, name), f"{name} declared in include/gemm_f16.h but not exported"
 
 
 def test_supported_shapes():

@@ -32,7 +32,7 @@ def _cases(n=36, seed=2026):
         entry = ["nt", "ws", "static"][int(rng.integers(0, 3))]
         out.append((i, M, N, K, variant, clusters, entry))
     # make sure split-K (few tiles, long K) shows up with each workspace entry point
-    out.append((n, 256, 264, 2600, (0, 0), 0, "ws"))
+    out.append((n, 256, 264, 2600, (2, 1), 0, "ws"))  # the default would take narrow tiles here
     out.append((n + 1, 500, 512, 2048, (1, 1), 0, "static"))
     # narrow tiles, forced, with the K-loop both inside and beyond the 8-stage ring
     rng = np.random.default_rng(seed + 1)
