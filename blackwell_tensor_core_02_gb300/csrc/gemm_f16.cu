@@ -139,6 +139,11 @@ int encode_partial_map(CUtensorMap *map, void *ptr, int64_t slices, int64_t M, i
     return r == CUDA_SUCCESS ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+bool overlaps(const void *p, int64_t p_bytes, const void *q, int64_t q_bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return a < b + static_cast<uintptr_t>(q_bytes) && b < a + static_cast<uintptr_t>(p_bytes);
+}
+
 bool shape_ok(int64_t M, int64_t N, int64_t K) {
     return M >= 0 && N >= 0 && K >= 0 && M <= kDimLimit && N <= kDimLimit && K <= kDimLimit && N % 8 == 0 &&
            K % 8 == 0;
@@ -378,6 +383,10 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     if ((reinterpret_cast<uintptr_t>(D) & 15u) || (K > 0 && ((reinterpret_cast<uintptr_t>(A) & 15u) ||
                                                              (reinterpret_cast<uintptr_t>(B) & 15u)))) {
         return GEMM_ERR_MISALIGNED;
+    }
+    // D is written while A and B are still being read: their byte ranges must not meet
+    if (K > 0 && (overlaps(D, M * N * 2, A, M * K * 2) || overlaps(D, M * N * 2, B, N * K * 2))) {
+        return GEMM_ERR_INVALID_ARG;
     }
     int dev = -1;
     DeviceInfo *info = nullptr;

@@ -16,7 +16,8 @@
  * Conventions shared by every call below:
  *   - Pointers named A, B, D are DEVICE pointers owned by the caller.  The
  *     library never frees, keeps or reallocates them and allocates no device
- *     memory per call.  D must not overlap A or B.
+ *     memory per call.  D must not overlap A or B (a call where it does is
+ *     refused with GEMM_ERR_INVALID_ARG).
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Compute calls are asynchronous: they validate, enqueue their
  *     kernel on `stream` (two with split-K, the GEMM and the reduction; a fill

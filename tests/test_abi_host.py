@@ -70,6 +70,10 @@ def test_argument_errors_are_returned_before_any_launch():
     assert lib.gemm_f16_nt(a + 2, b, d, 128, 128, 64, None) == MISALIGNED
     assert lib.gemm_f16_nt(a, b + 8, d, 128, 128, 64, None) == MISALIGNED
     assert lib.gemm_f16_nt(a, b, d + 4, 128, 128, 64, None) == MISALIGNED
+    # D may not overlap A or B (A spans 16 KiB from a; B 16 KiB from b)
+    assert lib.gemm_f16_nt(a, b, a + 0x3ff0, 128, 128, 64, None) == INVALID
+    assert lib.gemm_f16_nt(a, b, b - 0x7ff0, 128, 128, 64, None) == INVALID
+    assert lib.gemm_f16_nt(a, a, d, 128, 128, 64, None) != INVALID  # A and B may share memory
     # empty products are accepted and launch nothing, even with null operands
     assert lib.gemm_f16_nt(None, None, None, 0, 128, 64, None) == OK
     assert lib.gemm_f16_nt(None, None, None, 128, 0, 64, None) == OK
