@@ -6,8 +6,12 @@ narrow 128 x 64 tiles), a cap on the number of
 persistent clusters (so that tail splits and multi-tile CTAs occur at small
 sizes) and an entry point (no workspace, caller workspace, the library's fixed
 scratch).  Every element must meet |gpu - oracle| <= 2^-9 |oracle| + 1e-3.
+
+GEMM_FUZZ_CASES and GEMM_FUZZ_SEED (environment) change the number of cases of
+the first series and the seed, for longer sweeps; the defaults are 36 and 2026.
 """
 import ctypes
+import os
 
 import numpy as np
 import pytest
@@ -46,7 +50,9 @@ def _cases(n=36, seed=2026):
     return out
 
 
-@pytest.mark.parametrize("i,M,N,K,variant,clusters,entry", _cases(), ids=lambda v: str(v) if isinstance(v, int) else None)
+@pytest.mark.parametrize("i,M,N,K,variant,clusters,entry",
+                         _cases(int(os.environ.get("GEMM_FUZZ_CASES", "36")), int(os.environ.get("GEMM_FUZZ_SEED", "2026"))),
+                         ids=lambda v: str(v) if isinstance(v, int) else None)
 def test_random_case(gpu_lib, i, M, N, K, variant, clusters, entry):
     lib = gpu_lib.load()
     A, B = si.custom(M, N, K, seed=1000 + i).operands()
