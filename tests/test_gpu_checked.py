@@ -1,7 +1,7 @@
 """The checked build: the same library compiled with its device range checks.
 
-compute-sanitizer is closed on this GPU pool, so the kernel carries its own
-range checks, compiled in only for this build (-DGEMM_F16_DEVICE_CHECKS=1):
+Instead of an external memory checker, the kernel carries its own range
+checks, compiled in only for the checked library (-DGEMM_F16_DEVICE_CHECKS=1):
 every work item the scheduler hands out, every ring stage, the TMEM columns of
 each accumulator, the epilogue's chunk count and staging buffer.  A failed
 check would end the kernel with GEMM_ERR_DEVICE_BOUNDS in the status word
