@@ -17,6 +17,10 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr int64_t kDefaultTimeoutNs = 4000000000LL;
 constexpr int64_t kDimLimit = (int64_t(1) << 31) - 1;
+// Largest M, N or K a GEMM accepts: the kernel forms tile coordinates (a
+// tile's first row or column plus up to 512) in 32-bit integers, and a TMA
+// store must never start at a coordinate that wrapped negative.
+constexpr int64_t kShapeLimit = kDimLimit - 1023;
 
 struct DeviceInfo {
     bool ready = false;
@@ -145,7 +149,7 @@ bool overlaps(const void *p, int64_t p_bytes, const void *q, int64_t q_bytes) {
 }
 
 bool shape_ok(int64_t M, int64_t N, int64_t K) {
-    return M >= 0 && N >= 0 && K >= 0 && M <= kDimLimit && N <= kDimLimit && K <= kDimLimit && N % 8 == 0 &&
+    return M >= 0 && N >= 0 && K >= 0 && M <= kShapeLimit && N <= kShapeLimit && K <= kShapeLimit && N % 8 == 0 &&
            K % 8 == 0;
 }
 
@@ -526,7 +530,7 @@ const char *gemm_f16_status_string(int status) {
         case GEMM_OK: return "GEMM_OK";
         case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: null pointer, negative size or bad option";
         case GEMM_ERR_UNSUPPORTED_SHAPE:
-            return "GEMM_ERR_UNSUPPORTED_SHAPE: N and K must be multiples of 8 and below 2^31";
+            return "GEMM_ERR_UNSUPPORTED_SHAPE: N and K must be multiples of 8, and M, N, K at most 2^31 - 1024";
         case GEMM_ERR_MISALIGNED: return "GEMM_ERR_MISALIGNED: A, B and D must be 16-byte aligned";
         case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no usable CUDA device";
         case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: the current device is not sm_103 (GB300)";

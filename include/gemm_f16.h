@@ -116,7 +116,9 @@ typedef struct gemm_f16_options {
  * 1 if gemm_f16_nt() accepts this shape, 0 if not.  Pure host logic, no CUDA
  * call.  Accepted: M >= 0, N >= 0, K >= 0, N % 8 == 0 and K % 8 == 0 (rows of
  * B and D are then whole 16-byte units, as the tensor-memory-accelerator copy
- * engine requires), and M, N, K < 2^31.  M, N and K need not be multiples of
+ * engine requires), and M, N, K <= 2^31 - 1024 (tile coordinates are 32-bit
+ * integers; the margin keeps a last tile's rows and columns from wrapping).
+ * M, N and K need not be multiples of
  * the tile: edge tiles read zeros past the ends of A and B and write only the
  * in-range part of D.  M == 0 or N == 0 is an empty product (nothing is
  * launched); K == 0 writes D = 0.

@@ -50,8 +50,10 @@ def test_library_exports_every_declared_function():
 
 def test_supported_shapes():
     ok = [(128, 128, 64), (4096, 4096, 4096), (8192, 28672, 4096), (1, 8, 8), (0, 8, 8), (5, 0, 0),
-          (129, 264, 520), (2 ** 31 - 1, 8, 8)]
-    bad = [(128, 12, 64), (128, 128, 60), (-1, 8, 8), (8, 8, -8), (2 ** 31, 8, 8), (8, 2 ** 31, 8)]
+          (129, 264, 520), (2 ** 31 - 1024, 8, 8), (8, 2 ** 31 - 1024, 8), (8, 8, 2 ** 31 - 1024)]
+    # up to 2^31 - 1024: past that a last tile's coordinates would wrap in 32 bits
+    bad = [(128, 12, 64), (128, 128, 60), (-1, 8, 8), (8, 8, -8), (2 ** 31, 8, 8), (8, 2 ** 31, 8),
+           (2 ** 31 - 1023, 8, 8), (2 ** 31 - 1, 8, 8), (8, 2 ** 31 - 1016, 8), (8, 8, 2 ** 31 - 1016)]
     for s in ok:
         assert g.gemm_f16_nt_supported(*s), s
     for s in bad:
