@@ -242,6 +242,33 @@ def test_back_to_back_dependent_calls(gpu_lib, overlap):
         assert_close(D2.cpu().numpy(), oracle.gemm_f16_nt(D1h, C), "second (reads the first)")
 
 
+def test_dependent_chain_with_overlap_matches_plain_launches(gpu_lib):
+    # A longer chain on CTA-pair kernels: D2 = (A·Bᵀ)·Cᵀ, twenty times over with fresh data.
+    # Under the overlapped launch the second GEMM prefetches its first k-tiles of D1 into L2
+    # while the first GEMM may still be writing D1; plain launches (overlap_launch = -1)
+    # give the reference.  The kernels compute identically either way, so any stale read
+    # would show as a bit difference.
+    M, N, K, N2 = 2048, 2048, 1024, 1024
+    on, off = gpu_lib.Options(overlap_launch=1), gpu_lib.Options(overlap_launch=-1)
+    assert gpu_lib.describe(M, N, K, on)["cta_group"] == 2 and gpu_lib.describe(M, N2, N, on)["cta_group"] == 2
+    rng = torch.Generator(device="cuda").manual_seed(123)
+    outs, refs = [], []
+    for _ in range(20):
+        dA = (torch.rand((M, K), generator=rng, device="cuda") - 0.5).half()
+        dB = (torch.rand((N, K), generator=rng, device="cuda") - 0.5).half()
+        dC = ((torch.rand((N2, N), generator=rng, device="cuda") - 0.5) * 0.125).half()
+        D1 = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+        gpu_lib.gemm_f16_nt(dA, dB, D1, options=on)
+        outs.append(gpu_lib.gemm_f16_nt(D1, dC, options=on))
+        R1 = gpu_lib.gemm_f16_nt(dA, dB, options=off)
+        refs.append(gpu_lib.gemm_f16_nt(R1, dC, options=off))
+    torch.cuda.synchronize()
+    assert gpu_lib.last_device_status()[0] == 0
+    for i, (o, r) in enumerate(zip(outs, refs)):
+        assert not torch.isnan(o).any(), f"chain {i}: NaN from a stale read of D1"
+        assert torch.equal(o.view(torch.int16), r.view(torch.int16)), f"chain {i} differs"
+
+
 def test_concurrent_host_threads(gpu_lib):
     # Four host threads, each on its own stream, call the library at once
     # (device set-up is guarded; tensor maps are built per call).
