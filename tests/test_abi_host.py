@@ -48,6 +48,43 @@ def test_library_exports_every_declared_function():
             assert hasattr(lib, name), f"{name} declared in include/gemm_f16.h but not exported"
 
 
+def test_header_is_c99_and_the_binding_matches_its_layouts():
+    """include/gemm_f16.h compiles as strict C99, a C program links against the library and
+    calls it, and the ctypes mirrors in the Python binding have the C compiler's sizes and
+    field offsets for every struct of the ABI."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    structs = {"gemm_f16_options": g.Options, "gemm_f16_launch_info": g.LaunchInfo,
+               "gemm_f16_work_item": g.WorkItem}
+    lines = ['#include "gemm_f16.h"', "#include <stddef.h>", "#include <stdio.h>", "int main(void) {",
+             '    printf("supported %d\\n", gemm_f16_nt_supported(128, 128, 64));']
+    for cname, py in structs.items():
+        lines.append(f'    printf("{cname} size %d\\n", (int)sizeof({cname}));')
+        for field, _ in py._fields_:
+            lines.append(f'    printf("{cname} {field} %d\\n", (int)offsetof({cname}, {field}));')
+    lines += ["    return 0;", "}"]
+    lib = g.load()  # builds the library if needed
+    out_dir = os.path.join(ROOT, "blackwell_tensor_core_02_gb300", "_build", "abi_c_check")
+    os.makedirs(out_dir, exist_ok=True)
+    src, exe = os.path.join(out_dir, "abi.c"), os.path.join(out_dir, "abi")
+    with open(src, "w") as f:
+        f.write("\n".join(lines) + "\n")
+    lib_dir = os.path.dirname(lib._name)
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    src, "-L", lib_dir, "-lgemm_f16", f"-Wl,-rpath,{lib_dir}", "-o", exe], check=True)
+    got = dict(line.rsplit(" ", 1) for line in subprocess.run([exe], check=True, capture_output=True,
+                                                              text=True).stdout.splitlines())
+    assert got["supported"] == "1"
+    for cname, py in structs.items():
+        assert int(got[f"{cname} size"]) == ctypes.sizeof(py), cname
+        for field, _ in py._fields_:
+            assert int(got[f"{cname} {field}"]) == getattr(py, field).offset, (cname, field)
+
+
 def test_supported_shapes():
     ok = [(128, 128, 64), (4096, 4096, 4096), (8192, 28672, 4096), (1, 8, 8), (0, 8, 8), (5, 0, 0),
           (129, 264, 520), (2 ** 31 - 1024, 8, 8), (8, 2 ** 31 - 1024, 8), (8, 8, 2 ** 31 - 1024)]
