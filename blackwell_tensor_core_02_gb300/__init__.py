@@ -43,15 +43,16 @@ class WorkItem(ctypes.Structure):
 class LaunchInfo(ctypes.Structure):
     """Mirror of ``gemm_f16_launch_info``."""
     _fields_ = [("cta_group", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32),
-                ("split_k", ctypes.c_int32), ("clusters", ctypes.c_int64), ("work_items", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("split_k", ctypes.c_int32), ("block_m", ctypes.c_int32), ("stages", ctypes.c_int32),
+                ("clusters", ctypes.c_int64), ("work_items", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
 
 
 class Options(ctypes.Structure):
     """Mirror of ``gemm_f16_options`` (zero fields mean defaults)."""
     _fields_ = [("cta_group", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
-                ("overlap_launch", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32)]
+                ("overlap_launch", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32),
+                ("block_m", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -72,10 +73,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_f16_last_device_status.restype = ctypes.c_int
     lib.gemm_f16_status_string.argtypes = [ctypes.c_int]
     lib.gemm_f16_status_string.restype = ctypes.c_char_p
-    lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i64, i64, i64,
+    lib.gemm_f16_nt_schedule.argtypes = [i64, i64, i64, i32, i32, i32, i32, i32, i32, i64, i64, i64,
                                          ctypes.POINTER(WorkItem)]
     lib.gemm_f16_nt_schedule.restype = ctypes.c_int
-    lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
+    lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
     lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
     lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, vp, ctypes.POINTER(Options)]
     lib.gemm_f16_nt_ws.restype = ctypes.c_int
@@ -323,22 +324,23 @@ def last_device_status(stream=None) -> tuple[int, int]:
 
 
 def schedule(M: int, N: int, cta_group: int, raster_group: int, num_clusters: int, cluster_id: int,
-             it: int, K: int = 4096, consumers: int = 1, split_k: int = 0, block_n: int = 256):
+             it: int, K: int = 4096, consumers: int = 1, split_k: int = 0, block_n: int = 256,
+             block_m: int = 128):
     """The iter-th work item of one cluster as (m_idx, n_idx, n_off, n_len, slice, kt_begin, kt_end),
     or None when it has no more."""
     w = WorkItem()
-    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, block_n, raster_group, split_k, num_clusters,
-                                     cluster_id, it, ctypes.byref(w))
+    rc = load().gemm_f16_nt_schedule(M, N, K, cta_group, consumers, block_n, block_m, raster_group, split_k,
+                                     num_clusters, cluster_id, it, ctypes.byref(w))
     if rc < 0:
         raise GemmError(rc, "gemm_f16_nt_schedule")
     return tuple(getattr(w, f) for f, _ in WorkItem._fields_) if rc == 1 else None
 
 
 def cta_origin(cta_group: int, m_idx: int, n_idx: int, rank: int, n_off: int = 0, n_len: int = 256,
-               consumers: int = 1, block_n: int = 256) -> dict:
+               consumers: int = 1, block_n: int = 256, block_m: int = 128) -> dict:
     """Rows/columns CTA `rank` of a work item loads and writes (see the C header)."""
     out = [ctypes.c_int64() for _ in range(4)]
-    rc = load().gemm_f16_nt_cta_origin(cta_group, consumers, block_n, m_idx, n_idx, n_off, n_len, rank,
+    rc = load().gemm_f16_nt_cta_origin(cta_group, consumers, block_n, block_m, m_idx, n_idx, n_off, n_len, rank,
                                        *[ctypes.byref(o) for o in out])
     if rc != 0:
         raise GemmError(rc, "gemm_f16_nt_cta_origin")

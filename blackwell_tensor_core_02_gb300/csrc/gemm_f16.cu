@@ -26,20 +26,20 @@ struct DeviceInfo {
     bool ready = false;
     int status = GEMM_OK;
     int sm_count = 0;
-    int max_clusters[4] = {0, 0, 0, 0};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2
-                                         // consumers, [3] narrow single-CTA tiles
+    int max_clusters[5] = {0, 0, 0, 0, 0};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2
+                                            // consumers, [3] narrow single-CTA tiles, [4] tiny tiles
 };
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int CG, int NC, int BN>
+template <int CG, int NC, int BN, int BM>
 cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr, bool overlap = false) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(Cfg<CG, NC, BN>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<CG, NC, BN>::SMEM_ALLOC;
+    cfg.blockDim = dim3(Cfg<CG, NC, BN, BM>::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<CG, NC, BN, BM>::SMEM_ALLOC;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CG;
@@ -58,15 +58,16 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttri
     return cfg;
 }
 
-template <int CG, int NC, int BN>
+template <int CG, int NC, int BN, int BM = 128>
 int prepare_kernel(int *max_clusters) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<CG, NC, BN>::SMEM_ALLOC);
+    using C = Cfg<CG, NC, BN, BM>;
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC, BN, BM>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<CG, NC, BN>(dim3(CG, 1, 1), nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<CG, NC, BN, BM>(dim3(CG, 1, 1), nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC, BN>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC, BN, BM>, &cfg);
     if (e != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
     *max_clusters = n;
     return GEMM_OK;
@@ -98,6 +99,7 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
             if (d.status == GEMM_OK) d.status = prepare_kernel<2, 1, 256>(&d.max_clusters[1]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2, 256>(&d.max_clusters[2]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64>(&d.max_clusters[3]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64>(&d.max_clusters[4]);
         }
         if (d.status == GEMM_OK && g_encode == nullptr) {
             void *fn = nullptr;
@@ -157,6 +159,7 @@ struct Opts {
     int32_t cta_group = 0;  // 0: chosen from the shape (resolve_config)
     int32_t consumers = 1;
     int32_t block_n = 0;    // tile width 256 or 64; 0: chosen from the shape (resolve_config)
+    int32_t block_m = 0;    // rows per CTA 128 or 64 (64 only with block_n 64); 0: chosen likewise
     int32_t max_clusters = 0;
     int32_t raster_group = 0;
     int64_t timeout_ns = kDefaultTimeoutNs;
@@ -173,6 +176,8 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
         if (opts->cta_group != 0) o->cta_group = opts->cta_group;
         if (opts->block_n != 0 && opts->block_n != 64 && opts->block_n != 256) return GEMM_ERR_INVALID_ARG;
         o->block_n = opts->block_n;
+        if (opts->block_m != 0 && opts->block_m != 64 && opts->block_m != 128) return GEMM_ERR_INVALID_ARG;
+        o->block_m = opts->block_m;
         if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
             (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
             return GEMM_ERR_INVALID_ARG;
@@ -184,6 +189,10 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     }
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o->consumers == 2 && o->cta_group == 1) return GEMM_ERR_INVALID_ARG;
+    if (o->block_m == 64) {
+        if (o->block_n == 256) return GEMM_ERR_INVALID_ARG;
+        o->block_n = 64;  // 64-row tiles are 64 wide
+    }
     if (o->block_n == 64 && (o->cta_group == 2 || o->consumers == 2)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
 }
@@ -205,6 +214,15 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
 //   With a workspace (allow_splitk), a split-K of at least 8 slices over CTA
 //   pairs beats them (512x512x4096 9.8 vs 11.4, 256x256x4096 9.2 vs 11.6); 4
 //   slices do not (1024x1024x4096 14.9 vs 12.1).
+// - Narrow tiles whose 64 x 64 halves fill at most two thirds of a wave go
+//   one step further, to 64-row tiles: twice the CTAs again, each with half
+//   the MMA work per K tile.  Measured on GB300 (graph-timed, us, 64 vs 128
+//   rows, tiles of 64 x 64 in brackets): 128x128x64 2.27 vs 2.53 (4),
+//   512x512x512 3.47 vs 3.76 (64), 256x256x4096 10.3 vs 11.8 (16),
+//   576x576x1024 5.00 vs 5.62 (81), 640x640x512 3.87 vs 3.93 (100); with more
+//   the 128-row tiles win (128x4096x512 4.01 vs 3.80 and 512x1024x512 3.99
+//   vs 3.77 (128), 768x768x512 4.14 vs 4.07 (144)), past one wave by far
+//   (1024x1024x512 5.21 vs 4.28).
 void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool allow_splitk, Opts *o) {
     const int64_t k_tiles = (K + 63) / 64;
     if (o->block_n == 0) {
@@ -228,8 +246,14 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
     }
     if (o->block_n == 64) {
         o->cta_group = 1;
+        if (o->block_m == 0) {
+            int64_t ctas = dev.max_clusters[4];
+            if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
+            o->block_m = 3 * ((M + 63) / 64) * ((N + 63) / 64) <= 2 * ctas ? 64 : 128;
+        }
         return;
     }
+    o->block_m = 128;
     if (o->cta_group != 0) return;
     if (o->consumers == 2) {
         o->cta_group = 2;
@@ -249,10 +273,10 @@ struct Plan {
     int64_t workspace_bytes;   // split-K partials, 0 without split-K
 };
 
-template <int CG, int NC, int BN>
+template <int CG, int NC, int BN, int BM = 128>
 int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o, bool allow_splitk,
               Plan *out) {
-    using C = Cfg<CG, NC, BN>;
+    using C = Cfg<CG, NC, BN, BM>;
     Params &p = out->p;
     p = Params{};
     p.M = static_cast<int32_t>(M);
@@ -267,7 +291,7 @@ int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts
     p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
     p.debug_flags = o.debug_flags;
     p.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
-    int64_t clusters = dev.max_clusters[C::NARROW ? 3 : (CG == 1 ? 0 : NC)];
+    int64_t clusters = dev.max_clusters[C::KIND];
     if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
     p.slices = (allow_splitk && NC == 1 && !C::NARROW)
                    ? splitk_slices(p.num_tiles, static_cast<int32_t>(clusters), p.k_tiles)
@@ -313,16 +337,16 @@ cudaError_t launch_reduce(const cudaLaunchConfig_t *cfg, int slices, const float
     }
 }
 
-template <int CG, int NC, int BN>
+template <int CG, int NC, int BN, int BM = 128>
 int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
            const DeviceInfo &dev, const Opts &o, void *workspace, int64_t workspace_bytes) {
-    using C = Cfg<CG, NC, BN>;
+    using C = Cfg<CG, NC, BN, BM>;
     Plan plan;
-    int st = make_plan<CG, NC, BN>(M, N, K, dev, o, workspace != nullptr, &plan);
+    int st = make_plan<CG, NC, BN, BM>(M, N, K, dev, o, workspace != nullptr, &plan);
     if (st != GEMM_OK) return st;
     if (plan.p.slices > 1 && (workspace_bytes < plan.workspace_bytes ||
                               (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)) {
-        st = make_plan<CG, NC, BN>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
+        st = make_plan<CG, NC, BN, BM>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
         if (st != GEMM_OK) return st;
     }
     Params &p = plan.p;
@@ -341,8 +365,8 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
     }
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg =
-        launch_config<CG, NC, BN>(dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1), stream, attr, o.overlap);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC, BN>, tmA, tmB, tmBh, tmD, tmP, p);
+        launch_config<CG, NC, BN, BM>(dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1), stream, attr, o.overlap);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC, BN, BM>, tmA, tmB, tmBh, tmD, tmP, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
@@ -399,6 +423,7 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_fill(D, M, N, s);
     resolve_config(M, N, K, *info, workspace != nullptr, &o);
+    if (o.block_n == 64 && o.block_m == 64) return launch<1, 1, 64, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.block_n == 64) return launch<1, 1, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.cta_group == 2 && o.consumers == 2) return launch<2, 2, 256>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.cta_group == 2) return launch<2, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
@@ -479,19 +504,29 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
     const bool ws = with_workspace != 0;
     resolve_config(M, N, K, *info, ws, &o);
     Plan plan;
-    if (o.block_n == 64) {
+    int stages = 0;
+    if (o.block_n == 64 && o.block_m == 64) {
+        st = make_plan<1, 1, 64, 64>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64>::STAGES;
+    } else if (o.block_n == 64) {
         st = make_plan<1, 1, 64>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64>::STAGES;
     } else if (o.cta_group == 2 && o.consumers == 2) {
         st = make_plan<2, 2, 256>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<2, 2, 256>::STAGES;
     } else if (o.cta_group == 2) {
         st = make_plan<2, 1, 256>(M, N, K, *info, o, ws, &plan);
+        stages = Cfg<2, 1, 256>::STAGES;
     } else {
         st = make_plan<1, 1, 256>(M, N, K, *info, o, ws, &plan);
+        stages = Cfg<1, 1, 256>::STAGES;
     }
     if (st != GEMM_OK) return st;
     out->cta_group = o.cta_group;
     out->consumers = o.consumers;
     out->block_n = o.block_n;
+    out->block_m = o.block_m;
+    out->stages = stages;
     out->split_k = plan.p.slices;
     out->clusters = plan.clusters;
     out->work_items = plan.p.num_items;
@@ -547,20 +582,22 @@ const char *gemm_f16_status_string(int status) {
 }
 
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers, int32_t block_n,
-                         int32_t raster_group, int32_t split_k, int64_t num_clusters, int64_t cluster_id, int64_t iter,
-                         gemm_f16_work_item *out) {
-    if (block_n == 0) block_n = 256;
+                         int32_t block_m, int32_t raster_group, int32_t split_k, int64_t num_clusters,
+                         int64_t cluster_id, int64_t iter, gemm_f16_work_item *out) {
+    if (block_m == 0) block_m = 128;
+    if (block_n == 0) block_n = block_m == 64 ? 64 : 256;
     if (cta_group == 0) cta_group = block_n == 64 ? 1 : 2;
     if (consumers == 0) consumers = 1;
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
         (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
-        (block_n == 64 && (cta_group != 1 || consumers != 1)) || raster_group < 0 ||
+        (block_n == 64 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
+        (block_m == 64 && block_n != 64) || raster_group < 0 ||
         (split_k != 0 && split_k != 1) || K < 0 ||
         K > kDimLimit || M <= 0 || N <= 0 || M > kDimLimit || N > kDimLimit || num_clusters <= 0 ||
         num_clusters > kDimLimit || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !out) {
         return GEMM_ERR_INVALID_ARG;
     }
-    const int64_t tile_m = 128 * cta_group * consumers, tile_n = block_n;
+    const int64_t tile_m = int64_t(block_m) * cta_group * consumers, tile_n = block_n;
     const int64_t num_m = (M + tile_m - 1) / tile_m, num_n = (N + tile_n - 1) / tile_n;
     const int64_t tiles = num_m * num_n;
     if (tiles > kDimLimit / 16) return GEMM_ERR_INVALID_ARG;
@@ -594,18 +631,20 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
     return 1;
 }
 
-int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int64_t m_idx, int64_t n_idx,
-                           int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
+int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int32_t block_m, int64_t m_idx,
+                           int64_t n_idx, int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
                            int64_t *d_row, int64_t *d_col) {
-    if (block_n == 0) block_n = 256;
+    if (block_m == 0) block_m = 128;
+    if (block_n == 0) block_n = block_m == 64 ? 64 : 256;
     if (cta_group == 0) cta_group = block_n == 64 ? 1 : 2;
     if (consumers == 0) consumers = 1;
     const bool lens_ok = block_n == 64 ? (n_len == 64 && n_off == 0)
                                        : ((n_len == 256 && n_off == 0) || (n_len == 128 && (n_off == 0 || n_off == 128)));
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
         (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
-        (block_n == 64 && (cta_group != 1 || consumers != 1)) || rank < 0 || rank >= cta_group || m_idx < 0 ||
-        n_idx < 0 || m_idx * 128 * cta_group * consumers > kDimLimit || n_idx * block_n > kDimLimit || !lens_ok ||
+        (block_n == 64 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
+        (block_m == 64 && block_n != 64) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
+        m_idx * block_m * cta_group * consumers > kDimLimit || n_idx * block_n > kDimLimit || !lens_ok ||
         !a_row || !b_row || !d_row || !d_col) {
         return GEMM_ERR_INVALID_ARG;
     }
@@ -614,7 +653,7 @@ int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n
     w.n_idx = static_cast<int32_t>(n_idx);
     w.n_off = static_cast<int32_t>(n_off);
     w.n_len = static_cast<int32_t>(n_len);
-    const CtaOrigin o = cta_origin(w, cta_group, rank, consumers, block_n);
+    const CtaOrigin o = cta_origin(w, cta_group, rank, consumers, block_n, block_m);
     *a_row = o.a_row;
     *b_row = o.b_row;
     *d_row = o.d_row;

@@ -49,6 +49,12 @@
 // 512 at once, TMEM is 128 columns (two 64-column accumulators), and the
 // epilogue writes D from registers.  Not on the pages, which fix the tile.
 //
+// Tiny tiles (BM = 64, BN = 64): for problems whose 64 x 64 tiles fill at most
+// two thirds of a wave, the same again with MMAs of M = 64 and a 12-stage ring of
+// 16 KiB stages.  An M = 64 accumulator takes lanes 0-15 of each 32-lane
+// quarter of TMEM (row r in lane 32 * (r / 16) + r % 16), so each epilogue
+// warp reads its quarter as usual and stores 16 rows from its lanes 0-15.
+//
 // Split-K (NC = 1): with very few tiles, item t*S + s runs K slice s of tile
 // t and its epilogue writes the fp32 partial sum of that slice to a workspace
 // [S][M][N]; splitk_reduce_kernel then adds the S partials in fp32 and rounds
@@ -86,13 +92,20 @@ enum : uint32_t { kCheckItem = 1, kCheckStage = 2, kCheckTmem = 3, kCheckChunk =
 
 // BN is the tile width: 256, or 64 for the narrow single-CTA tiles of small
 // problems (more CTAs, and a ring deep enough to hold a K of 512 at once).
-template <int CG, int NC, int BN = 256>
+// BM is the rows of D per CTA and consumer: 128, or 64 for the tiny tiles
+// (64 x 64) of the smallest problems.
+template <int CG, int NC, int BN = 256, int BM = 128>
 struct Cfg {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(NC == 1 || (NC == 2 && CG == 2), "two consumers need a CTA pair");
     static_assert(BN == 256 || (BN == 64 && CG == 1 && NC == 1), "narrow tiles are single-CTA, one consumer");
+    static_assert(BM == 128 || (BM == 64 && BN == 64), "64-row tiles are narrow");
     static constexpr bool NARROW = BN != 256;
-    static constexpr int BLOCK_M = 128;                 // rows of D per CTA and consumer
+    static constexpr bool TINY = BM == 64;
+    // co-resident cluster count slot of this configuration in the host's
+    // per-device table
+    static constexpr int KIND = TINY ? 4 : (NARROW ? 3 : (CG == 1 ? 0 : NC));
+    static constexpr int BLOCK_M = BM;                  // rows of D per CTA and consumer
     static constexpr int BLOCK_N = BN;                  // columns of D per tile (MMA N)
     static constexpr int BLOCK_K = 64;                  // one 128-byte swizzle row of fp16
     static constexpr int MMA_M = BLOCK_M * CG;          // M of one tcgen05.mma (one consumer)
@@ -102,7 +115,7 @@ struct Cfg {
     static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
     static constexpr int A_STAGE = A_BLOCK * NC;
     static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
-    static constexpr int STAGES = NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4));
+    static constexpr int STAGES = TINY ? 12 : (NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)));
     static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
     static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
@@ -112,6 +125,7 @@ struct Cfg {
     static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
     static constexpr bool EPI_DIRECT = NC == 2 || NARROW;  // store D from registers instead of via SMEM + TMA
     static constexpr int EPI_N = 64;                    // columns per epilogue chunk
+    static constexpr int WARP_ROWS = BLOCK_M / 4;       // rows of D per epilogue warp (TMEM lanes 0 .. -1)
     static constexpr int EPI_BUFS = EPI_DIRECT ? 0 : 2;
     static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
@@ -212,12 +226,12 @@ __device__ __forceinline__ void to_f16x2(const uint32_t (&in)[32], uint32_t *out
     }
 }
 
-template <int CG, int NC, int BN>
-__global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
+template <int CG, int NC, int BN, int BM>
+__global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
                        const __grid_constant__ CUtensorMap tmP, const Params p) {
-    using C = Cfg<CG, NC, BN>;
+    using C = Cfg<CG, NC, BN, BM>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -283,7 +297,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
     if (warp == 0 && lane == 0 && cluster < p.num_items) {
         const WorkItem w = work_of(cluster, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
                                    p.slices, C::BLOCK_N);
-        const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
+        const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
         const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
         const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
         for (int kt = w.kt_begin; kt < kt_end; ++kt) {
@@ -313,7 +327,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
+                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
                 const bool half = w.n_len < C::BLOCK_N;
                 const CUtensorMap *mapB = half ? &tmBh : &tmB;
                 for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
@@ -410,7 +424,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
         __syncwarp();
     } else if (warp >= C::EPI_WARP0) {
         // -------------------------------------------------------- epilogue
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 = rows of this warp
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 hold the rows of this warp
         const int consumer = (warp - C::EPI_WARP0) / 4;
         const uint32_t stage_base = sD + static_cast<uint32_t>(quarter * C::EPI_BUFS * C::EPI_BUF);
         PipelineState acc(C::ACC_BUFS, 0u);
@@ -419,9 +433,9 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
         for (int item = cluster; item < p.num_items; item += num_clusters, ++seq) {
             const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
                                        p.k_tiles, p.slices, C::BLOCK_N);
-            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N);
+            const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
             const int chunks = w.n_len / C::EPI_N;
-            const int32_t row0 = o.d_row + consumer * C::MMA_M + quarter * 32;
+            const int32_t row0 = o.d_row + consumer * C::MMA_M + quarter * C::WARP_ROWS;
             const int32_t col0 = o.d_col;
             bool ok = true;
             if (lane == 0) {
@@ -546,15 +560,16 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN>::THREADS, 1)
                         buf ^= 1u;
                     }
                 } else {
-                    // Two-consumer variant: row `lane` of this warp, 64 columns
-                    // = eight 16-byte stores straight from registers (N % 8 == 0,
-                    // so a 16-byte unit is all in range or all out).
+                    // Two-consumer and narrow variants: row `lane` of this
+                    // warp, 64 columns = eight 16-byte stores straight from
+                    // registers (N % 8 == 0, so a 16-byte unit is all in range
+                    // or all out).  With 64-row tiles only lanes 0-15 hold rows.
                     uint32_t h[32];
                     to_f16x2(lo, h);
                     to_f16x2(hi, h + 16);
                     const int32_t row = row0 + lane;
                     const int32_t col = col0 + c * C::EPI_N;
-                    if (row < p.M) {
+                    if (lane < C::WARP_ROWS && row < p.M) {
                         uint16_t *dst = p.D + static_cast<int64_t>(row) * p.N + col;
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {

@@ -93,7 +93,8 @@ struct WorkItem {
 // split_from on are the two halves of tiles split_from, split_from + 1, ...
 // With slices > 1 (split-K; nothing is then split along N) item t*slices + s
 // is K slice s of tile t: K tiles [s*k_tiles/slices, (s+1)*k_tiles/slices).
-// Tiles are bn columns wide (256, or 64 for the narrow small-problem tiles).
+// Tiles are bn columns wide (256, or 64 for the narrow and tiny tiles of
+// small problems).
 GEMM_HD WorkItem work_of(int32_t item, int32_t num_m, int32_t num_n, int32_t group, int32_t split_from,
                          int32_t k_tiles = 0, int32_t slices = 1, int32_t bn = 256) {
     if (slices > 1) {
@@ -156,11 +157,11 @@ GEMM_HD int32_t split_point(int32_t num_tiles, int32_t clusters) {
 
 // Where one CTA of a work item reads and writes (TIRx notes V8, "Operand
 // Partition", "Output Ownership", "Epilogue Column Address").  An item covers
-// (128 * cg * nc) rows x n_len columns of D, nc being the number of MMA
-// consumers (TIRx notes V9: two consumers stack their 128*cg rows along M),
-// in a grid of tiles bn columns wide.
-// CTA `rank` loads, for consumer c, A rows a_row + c*128*cg .. +128 and the
-// shared B rows b_row .. +n_len/cg, and writes D rows d_row + c*128*cg .. +128
+// (bm * cg * nc) rows x n_len columns of D, nc being the number of MMA
+// consumers (TIRx notes V9: two consumers stack their bm*cg rows along M),
+// in a grid of tiles bn columns wide; bm is 128, or 64 for the tiny tiles.
+// CTA `rank` loads, for consumer c, A rows a_row + c*bm*cg .. +bm and the
+// shared B rows b_row .. +n_len/cg, and writes D rows d_row + c*bm*cg .. +bm
 // over all n_len columns from d_col: the rank selects the A rows and the
 // output rows, and only the slice of B it loads, never the output columns.
 struct CtaOrigin {
@@ -170,11 +171,12 @@ struct CtaOrigin {
     int32_t d_col;
 };
 
-GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank, int32_t nc = 1, int32_t bn = 256) {
+GEMM_HD CtaOrigin cta_origin(WorkItem w, int32_t cg, int32_t rank, int32_t nc = 1, int32_t bn = 256,
+                             int32_t bm = 128) {
     CtaOrigin o;
-    const int32_t m_base = w.m_idx * 128 * cg * nc;
+    const int32_t m_base = w.m_idx * bm * cg * nc;
     const int32_t n_base = w.n_idx * bn + w.n_off;
-    o.a_row = m_base + rank * 128;
+    o.a_row = m_base + rank * bm;
     o.b_row = n_base + rank * (w.n_len / cg);
     o.d_row = o.a_row;
     o.d_col = n_base;

@@ -64,7 +64,8 @@ typedef enum gemm_status {
  *                 the pair tiles would occupy at most half the co-resident
  *                 pairs (small, latency-bound problems), else 2.  With both
  *                 cta_group and block_n at 0, small problems may instead take
- *                 the narrow tiles of block_n 64.
+ *                 the narrow tiles of block_n 64 (and the smallest the tiny
+ *                 tiles of block_m 64).
  *   max_clusters  cap on the persistent grid, in clusters (CTA pairs for
  *                 cta_group 2); 0 = as many as are co-resident on the device.
  *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes
@@ -100,6 +101,14 @@ typedef enum gemm_status {
  *                 tiles of 64 and the 128 x 64 tiles fit one wave of
  *                 co-resident CTAs, else 256.  Other values:
  *                 GEMM_ERR_INVALID_ARG.
+ *   block_m       rows of D per CTA.  128: the tiles above.  64 (needs
+ *                 block_n 0 or 64, which then means 64): single CTAs with
+ *                 64 x 64 tiles, MMAs of M = 64 and a 12-stage ring; for the
+ *                 smallest problems.  Not on the pages.  0 (default): with
+ *                 block_n resolved to 64, 64 when the 64 x 64 tiles number at
+ *                 most two thirds of the co-resident CTAs, else 128.  Other
+ *                 values:
+ *                 GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;
@@ -110,6 +119,7 @@ typedef struct gemm_f16_options {
     int32_t overlap_launch;
     int32_t consumers;
     int32_t block_n;
+    int32_t block_m;
 } gemm_f16_options;
 
 /*
@@ -208,6 +218,8 @@ typedef struct gemm_f16_launch_info {
     int32_t consumers;        /* 1 or 2 */
     int32_t block_n;          /* tile width: 256 or 64 */
     int32_t split_k;          /* K slices S (1 = no split-K; > 1 adds the reduction kernel) */
+    int32_t block_m;          /* rows of D per CTA and consumer: 128 or 64 */
+    int32_t stages;           /* depth of the shared-memory operand ring */
     int64_t clusters;         /* persistent clusters in the grid (CTAs = clusters * cta_group) */
     int64_t work_items;       /* tiles, half tiles or K slices dealt to the clusters */
     int64_t workspace_bytes;  /* split-K partials, 0 without split-K */
@@ -247,7 +259,7 @@ const char *gemm_f16_status_string(int status);
 
 /* One unit of work of a persistent cluster (see gemm_f16_nt_schedule()). */
 typedef struct gemm_f16_work_item {
-    int64_t m_idx, n_idx;     /* the tile: rows m_idx * 128*cta_group*consumers, columns n_idx * block_n */
+    int64_t m_idx, n_idx;     /* the tile: rows m_idx * block_m*cta_group*consumers, columns n_idx * block_n */
     int64_t n_off, n_len;     /* columns n_off .. n_off + n_len of that tile (block_n, or a half) */
     int64_t slice;            /* K slice under split-K, else 0 */
     int64_t kt_begin, kt_end; /* 64-wide K tiles [kt_begin, kt_end) */
@@ -255,10 +267,11 @@ typedef struct gemm_f16_work_item {
 
 /*
  * The persistent scheduler, as a pure host query (no CUDA call); the kernel
- * runs the same code.  D is cut into tiles of (128 * cta_group * consumers)
- * rows x block_n columns (consumers 0 means 1; block_n 0 means 256, and 64,
- * the narrow tiles of gemm_f16_options, needs cta_group 0 or 1, which then
- * means 1, and one consumer), ordered in groups of
+ * runs the same code.  D is cut into tiles of (block_m * cta_group *
+ * consumers) rows x block_n columns (consumers 0 means 1; block_m 0 means 128,
+ * and 64, the tiny tiles of gemm_f16_options, needs block_n 0 or 64; block_n 0
+ * means 64 with block_m 64, else 256; block_n 64, the narrow tiles, needs
+ * cta_group 0 or 1, which then means 1, and one consumer), ordered in groups of
  * `raster_group` M-tiles (0 = the shape-derived default described under
  * gemm_f16_options): M fastest inside a group, then N, then the next group
  * (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters
@@ -268,34 +281,36 @@ typedef struct gemm_f16_work_item {
  * 148 CTAs leave 6.9 tiles per CTA, i.e. a partly idle last wave).  With
  * split_k = 1 (what gemm_f16_nt_ws() does given enough workspace) and few
  * tiles, K is instead cut into slices: item t*S + s is slice s of tile t.
- * Narrow tiles are never split, along N or K.
+ * Narrow and tiny tiles are never split, along N or K.
  * Cluster `cluster_id` takes work items cluster_id, cluster_id + P, ...
  * Returns 1 and fills *out with the iter-th item of that cluster, 0 if the
  * cluster has no iter-th item, or GEMM_ERR_INVALID_ARG for bad arguments.
  */
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers, int32_t block_n,
-                         int32_t raster_group, int32_t split_k, int64_t num_clusters, int64_t cluster_id, int64_t iter,
-                         gemm_f16_work_item *out);
+                         int32_t block_m, int32_t raster_group, int32_t split_k, int64_t num_clusters,
+                         int64_t cluster_id, int64_t iter, gemm_f16_work_item *out);
 
 /*
  * Where CTA `rank` of a work item reads and writes, as a pure host query (no
  * CUDA call); the kernel uses the same function.  TIRx notes V8, "Operand
- * Partition" and "Output Ownership": with m_base = m_idx * 128 * cta_group *
- * consumers and n_base = n_idx * block_n + n_off, the CTA loads A rows a_row =
- * m_base + 128 * rank (128 rows; consumer c's block lies c * 128 * cta_group
- * rows further, TIRx notes V9) and B rows b_row = n_base + (n_len / cta_group)
- * * rank (n_len / cta_group rows, shared by the consumers), and writes D rows
- * d_row = a_row (128 rows per consumer) over the n_len columns starting at
- * d_col = n_base ("Epilogue Column Address": no rank term).  block_n is 0
- * (meaning 256) or 256: n_len is 256 (whole tile, n_off 0) or 128 (half tile,
- * n_off 0 or 128); or 64 (narrow tiles, cta_group 0 or 1, one consumer):
- * n_len 64, n_off 0.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not
+ * Partition" and "Output Ownership": with bm = block_m (0 meaning 128), m_base =
+ * m_idx * bm * cta_group * consumers and n_base = n_idx * block_n + n_off, the
+ * CTA loads A rows a_row = m_base + bm * rank (bm rows; consumer c's block
+ * lies c * bm * cta_group rows further, TIRx notes V9) and B rows b_row =
+ * n_base + (n_len / cta_group) * rank (n_len / cta_group rows, shared by the
+ * consumers), and writes D rows d_row = a_row (bm rows per consumer) over the
+ * n_len columns starting at d_col = n_base ("Epilogue Column Address": no rank
+ * term).  block_n is 0 (meaning 256, or 64 with block_m 64) or 256: n_len is
+ * 256 (whole tile, n_off 0) or 128 (half tile, n_off 0 or 128); or 64 (narrow
+ * tiles, cta_group 0 or 1, one consumer): n_len 64, n_off 0.  block_m 64
+ * needs block_n 64.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not
  * 0/1/2, consumers not 0/1/2 or 2 without a pair, block_n not 0/64/256 or 64
- * with a pair or two consumers, rank out of range, bad n_off/n_len, negative
- * or too large indices, null outputs).
+ * with a pair or two consumers, block_m not 0/64/128 or 64 with block_n 256,
+ * rank out of range, bad n_off/n_len, negative or too large indices, null
+ * outputs).
  */
-int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int64_t m_idx, int64_t n_idx,
-                           int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
+int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int32_t block_m, int64_t m_idx,
+                           int64_t n_idx, int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
                            int64_t *d_row, int64_t *d_col);
 
 /*

@@ -123,7 +123,9 @@ def test_argument_errors_are_returned_before_any_launch():
     for bad in (g.Options(cta_group=3), g.Options(max_clusters=-1), g.Options(raster_group=-2),
                 g.Options(debug_flags=2), g.Options(timeout_ns=-5), g.Options(overlap_launch=2),
                 g.Options(consumers=3), g.Options(cta_group=1, consumers=2), g.Options(block_n=128),
-                g.Options(block_n=32), g.Options(block_n=64, cta_group=2), g.Options(block_n=64, consumers=2)):
+                g.Options(block_n=32), g.Options(block_n=64, cta_group=2), g.Options(block_n=64, consumers=2),
+                g.Options(block_m=32), g.Options(block_m=256), g.Options(block_m=64, block_n=256),
+                g.Options(block_m=64, cta_group=2), g.Options(block_m=64, consumers=2)):
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
 
@@ -149,8 +151,8 @@ def test_describe_validates_before_touching_a_device():
     assert lib.gemm_f16_nt_describe(128, 128, 64, ctypes.byref(g.Options(block_n=64, cta_group=2)), 0,
                                     ctypes.byref(info)) == INVALID
     # an empty product launches no GEMM: all zero, no device needed
-    assert g.describe(0, 128, 64) == dict(cta_group=0, consumers=0, block_n=0, split_k=0, clusters=0, work_items=0,
-                                          workspace_bytes=0)
+    assert g.describe(0, 128, 64) == dict(cta_group=0, consumers=0, block_n=0, split_k=0, block_m=0, stages=0,
+                                          clusters=0, work_items=0, workspace_bytes=0)
 
 
 def test_status_strings():
@@ -301,6 +303,56 @@ def test_narrow_schedule_covers_every_output_once(M, N, K, clusters):
             g.schedule(M, N, cg, 0, clusters, 0, 0, K=K, consumers=consumers, block_n=64)
     with pytest.raises(g.GemmError):
         g.schedule(M, N, 1, 0, clusters, 0, 0, K=K, block_n=128)
+
+
+@pytest.mark.parametrize("M,N,K,clusters", [
+    (128, 128, 64, 152), (256, 256, 512, 152), (512, 512, 512, 152), (300, 520, 256, 7), (1, 8, 8, 1),
+    (1000, 7000, 512, 13),
+])
+def test_tiny_schedule_covers_every_output_once(M, N, K, clusters):
+    """Tiny tiles (block_m 64, block_n 64): every 64 x 64 tile is one work item, never split along
+    N or K, dealt round-robin over the clusters."""
+    num_m, num_n = -(-M // 64), -(-N // 64)
+    k_tiles = -(-K // 64)
+    cover = {}
+    for c in range(clusters):
+        it = 0
+        while (w := g.schedule(M, N, 1, 0, clusters, c, it, K=K, block_n=64, block_m=64, split_k=1)) is not None:
+            m_idx, n_idx, n_off, n_len, sl, kb, ke = w
+            assert (n_off, n_len, sl, kb, ke) == (0, 64, 0, 0, k_tiles)
+            assert 0 <= m_idx < num_m and 0 <= n_idx < num_n
+            assert (m_idx, n_idx) not in cover
+            cover[(m_idx, n_idx)] = c
+            it += 1
+        assert it == len(range(c, num_m * num_n, clusters))
+    assert len(cover) == num_m * num_n
+    # block_n 0 means 64 with block_m 64; block_m 64 needs narrow single-CTA tiles
+    assert g.schedule(M, N, 0, 0, clusters, 0, 0, K=K, block_n=0, block_m=64) == \
+        g.schedule(M, N, 1, 0, clusters, 0, 0, K=K, block_n=64, block_m=64)
+    for kw in (dict(block_n=256), dict(block_n=64, block_m=32), dict(block_n=64, block_m=256)):
+        with pytest.raises(g.GemmError):
+            g.schedule(M, N, 1, 0, clusters, 0, 0, K=K, **{"block_m": 64, **kw})
+    with pytest.raises(g.GemmError):
+        g.schedule(M, N, 2, 0, clusters, 0, 0, K=K, block_n=64, block_m=64)
+
+
+def test_tiny_cta_origin():
+    # a 64 x 64 tile: A rows and D rows from m_idx * 64, B rows and D columns from n_idx * 64
+    assert g.cta_origin(1, 3, 5, 0, n_len=64, block_n=64, block_m=64) == dict(a_row=192, b_row=320, d_row=192,
+                                                                               d_col=320)
+    assert g.cta_origin(0, 7, 0, 0, n_len=64, block_n=0, block_m=64) == dict(a_row=448, b_row=0, d_row=448, d_col=0)
+    # over a 320 x 192 grid the written 64 x 64 blocks tile D exactly once
+    cover = np.zeros((5, 3), dtype=int)
+    for m_idx in range(5):
+        for n_idx in range(3):
+            o = g.cta_origin(1, m_idx, n_idx, 0, n_len=64, block_n=64, block_m=64)
+            assert o["a_row"] == o["d_row"] and o["b_row"] == o["d_col"]
+            cover[o["d_row"] // 64, o["d_col"] // 64] += 1
+    assert np.all(cover == 1)
+    for kw in (dict(block_n=256, n_len=256), dict(block_n=64, n_len=64, cta_group=2), dict(block_m=96)):
+        args = {"cta_group": 1, "n_len": 64, "block_n": 64, "block_m": 64, **kw}
+        with pytest.raises(g.GemmError):
+            g.cta_origin(args.pop("cta_group"), 0, 0, 0, **args)
 
 
 def test_narrow_cta_origin():

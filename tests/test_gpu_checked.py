@@ -23,9 +23,10 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (M, N, K, cta_group, consumers, block_n, max_clusters, workspace)
-    (128, 128, 64, 0, 0, 0, 0, False),       # default: narrow tiles
+    # (M, N, K, cta_group, consumers, block_n, max_clusters, workspace[, block_m])
+    (128, 128, 64, 0, 0, 0, 0, False),       # default: tiny tiles
     (256, 256, 512, 0, 0, 0, 0, False),
+    (700, 600, 1000, 1, 1, 64, 5, False, 64),  # tiny tiles, many per CTA, K beyond the ring
     (1000, 520, 1000, 2, 1, 256, 3, False),  # pairs, many tiles per cluster, ragged
     (1000, 520, 1000, 1, 1, 256, 5, False),  # single CTAs
     (1000, 520, 1000, 2, 2, 256, 2, False),  # two consumers
@@ -50,11 +51,13 @@ def _call(lib, dA, dB, M, N, K, o, ws):
     return D, status, info.value
 
 
-@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(str(v) for v in c[:3]) + f"-cg{c[3]}-nc{c[4]}-bn{c[5]}")
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(str(v) for v in c[:3]) + f"-cg{c[3]}-nc{c[4]}-bn{c[5]}"
+                         + (f"-bm{c[8]}" if len(c) > 8 else ""))
 def test_checked_build_runs_clean_and_matches(gpu_lib, case):
-    M, N, K, cg, nc, bn, clusters, use_ws = case
+    M, N, K, cg, nc, bn, clusters, use_ws = case[:8]
     checked, prod = gpu_lib.load_checked(), gpu_lib.load()
-    o = gpu_lib.Options(cta_group=cg, consumers=nc, block_n=bn, max_clusters=clusters)
+    o = gpu_lib.Options(cta_group=cg, consumers=nc, block_n=bn, max_clusters=clusters,
+                        block_m=case[8] if len(case) > 8 else 0)
     A, B = si.custom(M, N, K, seed=M + 2 * N + 3 * K).operands()
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     ws = None

@@ -13,15 +13,36 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-def test_small_problems_take_narrow_tiles(gpu_lib):
+def _resident_tiny_ctas(gpu_lib):
+    # a grid of 64 x 64 tiles far beyond one wave launches every co-resident CTA
+    return gpu_lib.describe(4096, 4096, 64, gpu_lib.Options(block_m=64))["clusters"]
+
+
+def test_smallest_problems_take_tiny_tiles(gpu_lib):
     c1 = gpu_lib.describe(128, 128, 64)
-    assert (c1["cta_group"], c1["block_n"], c1["split_k"], c1["clusters"], c1["work_items"]) == (1, 64, 1, 2, 2)
+    assert (c1["cta_group"], c1["block_n"], c1["block_m"], c1["split_k"], c1["clusters"], c1["work_items"],
+            c1["stages"]) == (1, 64, 64, 1, 4, 4, 12)
     c2 = gpu_lib.describe(256, 256, 512)
-    assert (c2["cta_group"], c2["block_n"], c2["split_k"], c2["clusters"], c2["work_items"]) == (1, 64, 1, 8, 8)
-    # one wave of 128 x 64 tiles, any K, without a workspace
-    for M, N, K in ((1024, 1024, 1024), (1024, 1024, 4096), (256, 256, 4096), (128, 4096, 2048)):
+    assert (c2["cta_group"], c2["block_n"], c2["block_m"], c2["split_k"], c2["clusters"],
+            c2["work_items"]) == (1, 64, 64, 1, 16, 16)
+    # 64 x 64 tiles up to two thirds of the co-resident CTAs, any K, without a workspace
+    P = _resident_tiny_ctas(gpu_lib)
+    assert P >= 140  # GB300: 152 SMs, one tiny-tile CTA each
+    for M, N, K in ((256, 256, 4096), (512, 512, 512), (64 * (2 * P // 3), 64, 1024), (576, 576, 1024),
+                    (200, 1000, 72)):
         c = gpu_lib.describe(M, N, K)
-        assert c["block_n"] == 64 and c["work_items"] == -(-M // 128) * -(-N // 64), (M, N, K)
+        tiles = -(-M // 64) * -(-N // 64)
+        assert (c["block_n"], c["block_m"], c["work_items"], c["clusters"]) == (64, 64, tiles, tiles), (M, N, K)
+        assert c["workspace_bytes"] == 0
+
+
+def test_small_problems_take_narrow_tiles(gpu_lib):
+    P = _resident_tiny_ctas(gpu_lib)
+    # one wave of 128 x 64 tiles, but more than two thirds of a wave of 64 x 64 tiles
+    for M, N, K in ((1024, 1024, 1024), (1024, 1024, 4096), (128, 4096, 2048), (64 * (2 * P // 3 + 1), 64, 1024)):
+        c = gpu_lib.describe(M, N, K)
+        assert (c["block_n"], c["block_m"], c["stages"]) == (64, 128, 8), (M, N, K)
+        assert c["work_items"] == -(-M // 128) * -(-N // 64), (M, N, K)
         assert c["clusters"] == c["work_items"] and c["workspace_bytes"] == 0
 
 
@@ -29,7 +50,8 @@ def test_more_than_one_wave_keeps_256_wide_tiles(gpu_lib):
     wide = gpu_lib.describe(2048, 1024, 512)  # 256 narrow tiles: more than one wave
     assert (wide["cta_group"], wide["block_n"]) == (1, 256)
     big = gpu_lib.describe(4096, 4096, 4096)
-    assert (big["cta_group"], big["consumers"], big["block_n"], big["split_k"]) == (2, 1, 256, 1)
+    assert (big["cta_group"], big["consumers"], big["block_n"], big["block_m"], big["split_k"],
+            big["stages"]) == (2, 1, 256, 128, 1, 6)
     P, T = big["clusters"], 256
     r = T % P
     assert big["work_items"] == (T + r if 0 < 2 * r <= P else T)
@@ -42,6 +64,8 @@ def test_split_k_wins_only_with_at_least_8_slices(gpu_lib):
     assert deep["workspace_bytes"] == 8 * 256 * 256 * 4 == gpu_lib.workspace_size(256, 256, 4096)
     shallow = gpu_lib.describe(1024, 1024, 4096, with_workspace=True)  # 4 slices: narrow tiles instead
     assert shallow["block_n"] == 64 and shallow["split_k"] == 1 and gpu_lib.workspace_size(1024, 1024, 4096) == 0
+    tiny = gpu_lib.describe(256, 256, 1024, with_workspace=True)  # split-K would give 2 slices: tiny tiles
+    assert (tiny["block_m"], tiny["split_k"]) == (64, 1)
 
 
 def test_explicit_options_are_obeyed(gpu_lib):
@@ -52,6 +76,10 @@ def test_explicit_options_are_obeyed(gpu_lib):
     two = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(consumers=2))
     assert (two["cta_group"], two["consumers"], two["block_n"]) == (2, 2, 256)
     narrow = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(block_n=64))
-    assert (narrow["cta_group"], narrow["block_n"], narrow["work_items"]) == (1, 64, 32 * 64)
+    assert (narrow["cta_group"], narrow["block_n"], narrow["block_m"], narrow["work_items"]) == (1, 64, 128, 32 * 64)
+    forced = gpu_lib.describe(128, 128, 64, gpu_lib.Options(block_m=128))
+    assert (forced["block_n"], forced["block_m"], forced["work_items"]) == (64, 128, 2)
+    tiny = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(block_m=64))
+    assert (tiny["cta_group"], tiny["block_n"], tiny["block_m"], tiny["work_items"]) == (1, 64, 64, 64 * 64)
     capped = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(max_clusters=5))
     assert capped["clusters"] == 5

@@ -1,8 +1,8 @@
 """Randomised GPU parity: seeded random shapes, variants and entry points against the oracle.
 
 Each case draws M (any), N and K (multiples of 8, the supported set), a kernel
-variant (default, CTA pair, single CTA, two consumers; a second series the
-narrow 128 x 64 tiles), a cap on the number of
+variant (default, CTA pair, single CTA, two consumers; further series the
+narrow 128 x 64 and the tiny 64 x 64 tiles), a cap on the number of
 persistent clusters (so that tail splits and multi-tile CTAs occur at small
 sizes) and an entry point (no workspace, caller workspace, the library's fixed
 scratch).  Every element must meet |gpu - oracle| <= 2^-9 |oracle| + 1e-3.
@@ -38,15 +38,18 @@ def _cases(n=36, seed=2026):
     # make sure split-K (few tiles, long K) shows up with each workspace entry point
     out.append((n, 256, 264, 2600, (2, 1), 0, "ws"))  # the default would take narrow tiles here
     out.append((n + 1, 500, 512, 2048, (1, 1), 0, "static"))
-    # narrow tiles, forced, with the K-loop both inside and beyond the 8-stage ring
-    rng = np.random.default_rng(seed + 1)
-    for i in range(n + 2, n + 14):
-        M = int(rng.integers(1, 700))
-        N = int(rng.integers(1, 100)) * 8
-        K = int(rng.integers(1, 130)) * 8
-        clusters = int(rng.choice([0, 0, 1, 3, 7]))
-        entry = ["nt", "ws", "static"][int(rng.integers(0, 3))]
-        out.append((i, M, N, K, (1, 1, 64), clusters, entry))
+    # narrow and tiny tiles, forced, with the K-loop both inside and beyond
+    # the 8- and 12-stage rings
+    for series, variant in ((1, (1, 1, 64, 128)), (2, (1, 1, 64, 64))):
+        rng = np.random.default_rng(seed + series)
+        first = n + 2 + 12 * (series - 1)
+        for i in range(first, first + 12):
+            M = int(rng.integers(1, 700))
+            N = int(rng.integers(1, 100)) * 8
+            K = int(rng.integers(1, 130)) * 8
+            clusters = int(rng.choice([0, 0, 1, 3, 7]))
+            entry = ["nt", "ws", "static"][int(rng.integers(0, 3))]
+            out.append((i, M, N, K, variant, clusters, entry))
     return out
 
 
@@ -60,7 +63,7 @@ def test_random_case(gpu_lib, i, M, N, K, variant, clusters, entry):
     dB = torch.from_numpy(B).cuda()
     D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
     o = gpu_lib.Options(cta_group=variant[0], consumers=variant[1], max_clusters=clusters,
-                        block_n=variant[2] if len(variant) > 2 else 0)
+                        block_n=variant[2] if len(variant) > 2 else 0, block_m=variant[3] if len(variant) > 3 else 0)
     stream = torch.cuda.current_stream().cuda_stream
     if entry == "nt":
         rc = gpu_lib.gemm_f16_nt_ptr(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), M, N, K, stream, o)

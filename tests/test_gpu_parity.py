@@ -48,16 +48,17 @@ def assert_close(gpu_f16, ref_bits, what=""):
                              f"gpu={got[i]!r} oracle={ref[i]!r}")
 
 
-# (cta_group, consumers, block_n): the CTA pair with one MMA consumer (the
-# default), a single CTA, the pair with two consumers sharing each B stage, and
-# the narrow 128 x 64 single-CTA tiles of small problems.
-VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64)]
-VIDS = ["pair", "single", "pair-2consumers", "narrow"]
+# (cta_group, consumers, block_n[, block_m]): the CTA pair with one MMA
+# consumer (the default), a single CTA, the pair with two consumers sharing
+# each B stage, the narrow 128 x 64 single-CTA tiles of small problems, and the
+# tiny 64 x 64 tiles (MMAs of M = 64) of the smallest.
+VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64, 128), (1, 1, 64, 64)]
+VIDS = ["pair", "single", "pair-2consumers", "narrow", "tiny"]
 
 
 def opts(g, variant=(0, 0), max_clusters=0):
     return g.Options(cta_group=variant[0], max_clusters=max_clusters, consumers=variant[1],
-                     block_n=variant[2] if len(variant) > 2 else 0)
+                     block_n=variant[2] if len(variant) > 2 else 0, block_m=variant[3] if len(variant) > 3 else 0)
 
 
 # ----------------------------------------------------------- full compares --
@@ -96,11 +97,12 @@ def test_ragged_shapes_full(gpu_lib, M, N, K, v):
 
 
 @pytest.mark.parametrize("v,clusters", [((2, 1), 1), ((2, 1), 3), ((1, 1), 1), ((1, 1), 5), ((2, 2), 1), ((2, 2), 3),
-                                        ((1, 1, 64), 1), ((1, 1, 64), 6)])
+                                        ((1, 1, 64), 1), ((1, 1, 64), 6), ((1, 1, 64, 64), 1),
+                                        ((1, 1, 64, 64), 7)])
 def test_few_persistent_clusters_run_many_tiles(gpu_lib, v, clusters):
-    # 1024 x 1024 x 320: 16 (pair), 32 (single CTA) or 8 (two consumers)
-    # tiles, so each persistent CTA runs several tiles and both rings wrap many
-    # times across tiles.
+    # 1024 x 1024 x 320: 16 (pair), 32 (single CTA), 8 (two consumers), 128
+    # (narrow) or 256 (tiny) tiles, so each persistent CTA runs several tiles
+    # and both rings wrap many times across tiles.
     w = si.custom(1024, 1024, 320, seed=77)
     A, B = w.operands()
     assert_close(run(gpu_lib, A, B, opts(gpu_lib, v, clusters)), oracle.gemm_f16_nt(A, B),
