@@ -8,7 +8,9 @@ sizes) and an entry point (no workspace, caller workspace, the library's fixed
 scratch).  Every element must meet |gpu - oracle| <= 2^-9 |oracle| + 1e-3.
 
 GEMM_FUZZ_CASES and GEMM_FUZZ_SEED (environment) change the number of cases of
-the first series and the seed, for longer sweeps; the defaults are 36 and 2026.
+the first series and the seed, and GEMM_FUZZ_SERIES_CASES the number of cases of
+each of the narrow and tiny series, for longer sweeps; the defaults are 36, 2026
+and 12.
 """
 import ctypes
 import os
@@ -24,7 +26,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
-def _cases(n=36, seed=2026):
+def _cases(n=36, seed=2026, per_series=12):
     rng = np.random.default_rng(seed)
     out = []
     for i in range(n):
@@ -42,8 +44,8 @@ def _cases(n=36, seed=2026):
     # the 8- and 12-stage rings
     for series, variant in ((1, (1, 1, 64, 128)), (2, (1, 1, 64, 64))):
         rng = np.random.default_rng(seed + series)
-        first = n + 2 + 12 * (series - 1)
-        for i in range(first, first + 12):
+        first = n + 2 + per_series * (series - 1)
+        for i in range(first, first + per_series):
             M = int(rng.integers(1, 700))
             N = int(rng.integers(1, 100)) * 8
             K = int(rng.integers(1, 130)) * 8
@@ -54,7 +56,8 @@ def _cases(n=36, seed=2026):
 
 
 @pytest.mark.parametrize("i,M,N,K,variant,clusters,entry",
-                         _cases(int(os.environ.get("GEMM_FUZZ_CASES", "36")), int(os.environ.get("GEMM_FUZZ_SEED", "2026"))),
+                         _cases(int(os.environ.get("GEMM_FUZZ_CASES", "36")), int(os.environ.get("GEMM_FUZZ_SEED", "2026")),
+                                int(os.environ.get("GEMM_FUZZ_SERIES_CASES", "12"))),
                          ids=lambda v: str(v) if isinstance(v, int) else None)
 def test_random_case(gpu_lib, i, M, N, K, variant, clusters, entry):
     lib = gpu_lib.load()
