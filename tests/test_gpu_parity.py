@@ -85,6 +85,57 @@ def test_identity_operands_are_exact(gpu_lib, v):
     assert np.array_equal(D.view(np.uint16), A.view(np.uint16))
 
 
+def _range_edge_operands(seed):
+    """Row and column groups whose products put D in every fp16 range.
+
+    A rows 0-63: +256·u, rows 64-127: −256·u (u in [0.5, 1)), rows 128-191:
+    ±2⁻¹²·u, rows 192-255: ±u.  B columns 0-95: +256·v, columns 96-191:
+    ±2⁻¹²·v.  With K = 320 the big rows times the big columns sum to at least
+    5·10⁶ (±Inf in fp16), the tiny rows times the tiny columns to about 2⁻²¹
+    (fp16 subnormals, below 2⁻¹⁴), and every other block stays finite.
+    """
+    rng = np.random.default_rng(seed)
+    K = 320
+    u = rng.uniform(0.5, 1.0, size=(256, K))
+    sign = np.where(rng.random((256, K)) < 0.5, -1.0, 1.0)
+    A = np.empty((256, K))
+    A[0:64] = 256.0 * u[0:64]
+    A[64:128] = -256.0 * u[64:128]
+    A[128:192] = 2.0 ** -12 * u[128:192] * sign[128:192]
+    A[192:256] = u[192:256] * sign[192:256]
+    v = rng.uniform(0.5, 1.0, size=(192, K))
+    vsign = np.where(rng.random((192, K)) < 0.5, -1.0, 1.0)
+    B = np.empty((192, K))
+    B[0:96] = 256.0 * v[0:96]
+    B[96:192] = 2.0 ** -12 * v[96:192] * vsign[96:192]
+    return A.astype(np.float16), B.astype(np.float16)
+
+
+@pytest.mark.parametrize("v", VARIANTS + [(0, 0)], ids=VIDS + ["default"])
+def test_range_edges_overflow_and_subnormals(gpu_lib, v):
+    A, B = _range_edge_operands(5)
+    got = run(gpu_lib, A, B, opts(gpu_lib, v))
+    ref_bits = oracle.gemm_f16_nt(A, B)
+    ref = ref_bits.view(np.float16).astype(np.float64)
+    g64 = got.astype(np.float64)
+    inf = np.isinf(ref)
+    assert inf[0:128, 0:96].all() and not inf[128:].any(), "the operands do not reach the intended ranges"
+    # overflow: the same infinity, bit for bit
+    assert np.array_equal(got.view(np.uint16)[inf], ref_bits[inf]), f"{v}: infinities differ"
+    # subnormal results of the tiny block (all products tiny, so fp32 accumulation error is far
+    # below a subnormal step): within one step (2^-24), so a flush to zero would fail.  Elsewhere
+    # a subnormal can arise from cancelling large products and only the usual bound applies.
+    sub = np.zeros_like(inf)
+    sub[128:192, 96:192] = (np.abs(ref[128:192, 96:192]) < 2.0 ** -14) & (ref[128:192, 96:192] != 0)
+    assert sub[128:192, 96:192].mean() > 0.9, "the tiny block does not land in the subnormal range"
+    assert np.all(np.abs(g64[sub] - ref[sub]) <= 2.0 ** -24), f"{v}: subnormal results off by more than one step"
+    # everything finite within the usual bound
+    fin = ~inf
+    assert np.all(np.isfinite(g64[fin])), f"{v}: a finite result came out infinite"
+    err = np.abs(g64[fin] - ref[fin])
+    assert np.all(err <= RTOL * np.abs(ref[fin]) + ATOL), f"{v}: finite results outside tolerance"
+
+
 RAGGED = [(1, 8, 8), (200, 136, 72), (129, 264, 520), (383, 1032, 1000), (1000, 8, 64), (640, 776, 8)]
 
 
