@@ -13,7 +13,8 @@
 //              elected lane issues every tcgen05.mma, "GEMM I", "Why one
 //              elected thread issues the MMA").
 //   warps 2-5  epilogue: each warp owns one 32-lane quarter of TMEM (warp w
-//              may only touch lanes 32*(w%4) .. +31), i.e. 32 rows of the tile.
+//              may only touch lanes 32*(w%4) .. +31), i.e. 32 rows of the tile
+//              (16 with 64-row tiles).
 //
 // Two producer-consumer rings ("GEMM III", "Four barriers"; TIRx notes V7):
 //   SMEM ring:  empty[s] (mma2tma) -> TMA -> full[s] (tma2mma) -> MMA -> empty[s]
@@ -125,7 +126,8 @@ struct Cfg {
     static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
     static constexpr bool EPI_DIRECT = NC == 2 || NARROW;  // store D from registers instead of via SMEM + TMA
     static constexpr int EPI_N = 64;                    // columns per epilogue chunk
-    static constexpr int WARP_ROWS = BLOCK_M / 4;       // rows of D per epilogue warp (TMEM lanes 0 .. -1)
+    static constexpr int WARP_ROWS = BLOCK_M / 4;       // rows of D per epilogue warp: the first WARP_ROWS
+                                                        // lanes of its TMEM quarter
     static constexpr int EPI_BUFS = EPI_DIRECT ? 0 : 2;
     static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
