@@ -124,11 +124,17 @@ struct Cfg {
     static_assert(TMEM_COLS == 512 || TMEM_COLS == 128, "a power of two of at least 32 columns");
     static constexpr int EPI_WARPS = 4 * NC;
     static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
-    static constexpr bool EPI_DIRECT = NC == 2 || NARROW;  // store D from registers instead of via SMEM + TMA
+    static constexpr bool EPI_DIRECT = NC == 2;         // store D from registers (one row per lane)
+    static constexpr bool EPI_TMA = !NARROW && NC == 1; // stage in SMEM, store D (or split-K partials) by TMA
+    // Narrow and tiny tiles stage each warp's rows in SMEM and read them back
+    // so that a warp's store covers whole 128-byte rows of D (coalesced
+    // st.global): a row per lane would send 16-byte pieces of 16 or 32
+    // different rows per store instruction.
+    static constexpr bool EPI_COALESCED = NARROW;
     static constexpr int EPI_N = 64;                    // columns per epilogue chunk
     static constexpr int WARP_ROWS = BLOCK_M / 4;       // rows of D per epilogue warp: the first WARP_ROWS
                                                         // lanes of its TMEM quarter
-    static constexpr int EPI_BUFS = EPI_DIRECT ? 0 : 2;
+    static constexpr int EPI_BUFS = EPI_TMA ? 2 : (EPI_COALESCED ? 1 : 0);
     static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     // Shared-memory layout (offsets from a 1024-byte aligned base; identical
@@ -290,26 +296,11 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
     // Everything above touches only this CTA's own resources, so with a
     // programmatic launch it overlaps the tail of the previous kernel of the
-    // stream.  A, B and D are first read and written below, after the wait.
-    // Before it, the producer only asks L2 to fetch the A and B boxes of its
-    // first ring fill: L2 is where every later load reads them, and a line
-    // the previous kernel still writes is updated there, so the prefetch
-    // changes no value; it moves the HBM latency of the first k-tiles under
-    // the previous kernel's tail.
-    if (warp == 0 && lane == 0 && cluster < p.num_items) {
-        const WorkItem w = work_of(cluster, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
-                                   p.slices, C::BLOCK_N);
-        const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
-        const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
-        const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
-        for (int kt = w.kt_begin; kt < kt_end; ++kt) {
-#pragma unroll
-            for (int c = 0; c < NC; ++c) ptx::tma_prefetch_l2_2d(&tmA, kt * C::BLOCK_K, o.a_row + c * C::MMA_M);
-            ptx::tma_prefetch_l2_2d(mapB, kt * C::BLOCK_K, o.b_row);
-        }
-    }
+    // stream; so does what each role does below before its own
+    // griddepcontrol.wait (the producer's before its first TMA load, the
+    // epilogue's before its first write of D; the MMA issuer touches no
+    // global memory).  A, B and D are read and written only after it.
     if (threadIdx.x == 0) ptx::griddep_launch_dependents();
-    ptx::griddep_wait();
 
     if (warp == 0) {
         // ---------------------------------------------------- TMA producer
@@ -321,9 +312,33 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
             PipelineState ring(C::STAGES, (p.debug_flags & kDebugProducerPhase0) ? 0u : 1u);
             uint32_t seq = 0;
             bool ok = true;
-            for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
-                const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
-                                           p.k_tiles, p.slices, C::BLOCK_N);
+            bool dependency_met = false;  // griddepcontrol.wait has returned
+            int item = cluster;
+            WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
+                                 p.slices, C::BLOCK_N);
+            if (item < p.num_items) {
+                // Before the wait, only ask L2 for the A and B boxes of the
+                // first ring fill: L2 is where every later load reads them,
+                // and a line the previous kernel still writes is updated
+                // there, so the prefetch changes no value; it moves the HBM
+                // latency of the first k-tiles under the previous kernel's
+                // tail.
+                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
+                const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
+                const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
+                for (int kt = w.kt_begin; kt < kt_end; ++kt) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        ptx::tma_prefetch_l2_2d(&tmA, kt * C::BLOCK_K, o.a_row + c * C::MMA_M);
+                    }
+                    ptx::tma_prefetch_l2_2d(mapB, kt * C::BLOCK_K, o.b_row);
+                }
+            }
+            for (; ok && item < p.num_items; item += num_clusters, ++seq) {
+                if (seq > 0) {
+                    w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
+                                p.slices, C::BLOCK_N);
+                }
                 if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag,
                                kRoleProducer, kCheckItem, seq)) {
                     ok = false;
@@ -342,6 +357,12 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
                     }
                     const uint32_t full = bar_full + 8 * ring.stage;
                     if (leader) ptx::mbar_arrive_expect_tx(full, half ? C::TX_HALF : C::TX_BYTES);
+                    if (!dependency_met) {
+                        // the first load of A or B: the previous kernel of
+                        // the stream must be complete and its writes visible
+                        ptx::griddep_wait();
+                        dependency_met = true;
+                    }
                     const int32_t k0 = kt * C::BLOCK_K;
                     if constexpr (CG == 2) {
                         const uint32_t full_leader = ptx::mapa(full, 0);
@@ -446,6 +467,12 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
             }
             ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
             if (!ok) break;
+            if (seq == 0) {
+                // before this warp's first write of D (or of the split-K
+                // workspace): the previous kernel of the stream must be done
+                // with it
+                ptx::griddep_wait();
+            }
             if (GEMM_F16_DEVICE_CHECKS) {
                 bool fine = in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag,
                                       kRoleEpilogue, kCheckItem, seq);
@@ -453,7 +480,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
                                          abort_flag, kRoleEpilogue, kCheckTmem, seq);
                 fine = fine && in_bounds(chunks >= 1 && chunks <= C::BLOCK_N / C::EPI_N, abort_flag, kRoleEpilogue,
                                          kCheckChunk, seq);
-                fine = fine && in_bounds(C::EPI_DIRECT || buf < static_cast<uint32_t>(C::EPI_BUFS), abort_flag,
+                fine = fine && in_bounds(!C::EPI_TMA || buf < static_cast<uint32_t>(C::EPI_BUFS), abort_flag,
                                          kRoleEpilogue, kCheckStaging, seq);
                 if (!fine) break;
             }
@@ -473,7 +500,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
                     }
                 }
             };
-            if constexpr (!C::EPI_DIRECT) {
+            if constexpr (C::EPI_TMA) {
                 if (p.slices == 1) {
                     // fp16 D through TMA stores.  All chunks are read from TMEM
                     // and rounded to packed fp16 first (128 registers), so the
@@ -534,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
                 ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
                 ptx::tmem_wait_ld();
                 if (c == chunks - 1) release_tmem();
-                if constexpr (!C::EPI_DIRECT) {
+                if constexpr (C::EPI_TMA) {
                     // Split-K: this slice's fp32 partial sums go to the
                     // workspace [slice][M][N] as two 32 x 32 fp32 boxes per
                     // chunk (128-byte rows, the same swizzled staging as the
@@ -561,11 +588,46 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
                         }
                         buf ^= 1u;
                     }
+                } else if constexpr (C::EPI_COALESCED) {
+                    // Narrow and tiny tiles: lane r holds row r of this warp's
+                    // WARP_ROWS rows.  Each row goes to the warp's staging
+                    // buffer (128 bytes, 16-byte unit j at j ^ (r % 8), which
+                    // keeps both passes free of bank conflicts); the warp then
+                    // reads it back four rows per instruction, lane l taking
+                    // unit l % 8 of row l / 8, so every st.global of the warp
+                    // writes four whole 128-byte rows of D.  N % 8 == 0, so a
+                    // 16-byte unit is all in range or all out.
+                    uint32_t h[32];
+                    to_f16x2(lo, h);
+                    to_f16x2(hi, h + 16);
+                    const uint32_t buf_base = stage_base;
+                    if (lane < C::WARP_ROWS) {
+                        const uint32_t row_addr = buf_base + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
+                            ptx::st_shared_v4(row_addr + unit * 16u, h[4 * j], h[4 * j + 1], h[4 * j + 2],
+                                              h[4 * j + 3]);
+                        }
+                    }
+                    __syncwarp();
+                    const int32_t col = col0 + c * C::EPI_N + 8 * (lane & 7);
+#pragma unroll
+                    for (int i = 0; i < C::WARP_ROWS / 4; ++i) {
+                        const int32_t r = 4 * i + (lane >> 3);
+                        const uint32_t unit = static_cast<uint32_t>(lane & 7) ^ static_cast<uint32_t>(r & 7);
+                        const uint4 v = ptx::ld_shared_v4(buf_base + static_cast<uint32_t>(r) * 128u + unit * 16u);
+                        const int32_t row = row0 + r;
+                        if (row < p.M && col < p.N) {
+                            ptx::st_global_v4(p.D + static_cast<int64_t>(row) * p.N + col, v.x, v.y, v.z, v.w);
+                        }
+                    }
+                    __syncwarp();  // the buffer is rewritten by the next chunk or work item
                 } else {
-                    // Two-consumer and narrow variants: row `lane` of this
-                    // warp, 64 columns = eight 16-byte stores straight from
-                    // registers (N % 8 == 0, so a 16-byte unit is all in range
-                    // or all out).  With 64-row tiles only lanes 0-15 hold rows.
+                    // Two-consumer variant: row `lane` of this warp, 64
+                    // columns = eight 16-byte stores straight from registers
+                    // (N % 8 == 0, so a 16-byte unit is all in range or all
+                    // out).
                     uint32_t h[32];
                     to_f16x2(lo, h);
                     to_f16x2(hi, h + 16);
