@@ -45,7 +45,7 @@ WORKLOAD = si.HEADLINE
 ROTATE = 4
 NOMINAL_PEAK_TFLOPS = 2250.0          # GB300 dense fp16/bf16 tensor, nominal
 FALLBACK_PEAK_TFLOPS = 1900.0         # one earlier cuBLAS bf16 measurement on a GB300
-KERNEL_NAME = "gemm_f16_nt_kernel<2, 1, 256, 128>"
+KERNEL_NAME = "gemm_f16_nt_kernel<2, 1, 256, 128, 1>"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_gemm_f16_nt_kernel_square_4096.json")
 
 
@@ -337,7 +337,8 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
         per_graph = int(min(400, max(10, budget_s / replays / max(w.flop / 1.5e15, 3e-6))))
         cfg = g.describe(w.M, w.N, w.K)
         res = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "steps": per_graph * replays,
-               "kernel": {k: cfg[k] for k in ("cta_group", "block_n", "block_m", "split_k", "clusters", "work_items")},
+               "kernel": {k: cfg[k] for k in ("cta_group", "block_n", "block_m", "split_k", "cluster_k", "clusters",
+                                              "work_items")},
                "parity_vs_oracle": parity,
                "rotated_copies": rot,
                "timing": f"CUDA graph of {per_graph} launches, replayed {replays} times; "

@@ -44,7 +44,8 @@ class LaunchInfo(ctypes.Structure):
     """Mirror of ``gemm_f16_launch_info``."""
     _fields_ = [("cta_group", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32),
                 ("split_k", ctypes.c_int32), ("block_m", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("clusters", ctypes.c_int64), ("work_items", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64)]
+                ("clusters", ctypes.c_int64), ("work_items", ctypes.c_int64), ("workspace_bytes", ctypes.c_int64),
+                ("cluster_k", ctypes.c_int32)]
 
 
 class Options(ctypes.Structure):
@@ -52,7 +53,7 @@ class Options(ctypes.Structure):
     _fields_ = [("cta_group", ctypes.c_int32), ("max_clusters", ctypes.c_int32),
                 ("raster_group", ctypes.c_int32), ("debug_flags", ctypes.c_int32), ("timeout_ns", ctypes.c_int64),
                 ("overlap_launch", ctypes.c_int32), ("consumers", ctypes.c_int32), ("block_n", ctypes.c_int32),
-                ("block_m", ctypes.c_int32)]
+                ("block_m", ctypes.c_int32), ("cluster_k", ctypes.c_int32)]
 
 
 _lock = threading.Lock()

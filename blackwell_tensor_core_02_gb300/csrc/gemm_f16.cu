@@ -26,23 +26,25 @@ struct DeviceInfo {
     bool ready = false;
     int status = GEMM_OK;
     int sm_count = 0;
-    int max_clusters[5] = {0, 0, 0, 0, 0};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2
-                                            // consumers, [3] narrow single-CTA tiles, [4] tiny tiles
+    int max_clusters[8] = {};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2 consumers,
+                               // [3] narrow single-CTA tiles, [4] tiny tiles, [5] [6] [7] tiny tiles with
+                               // K split across clusters of 2, 4 and 8 CTAs
 };
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int CG, int NC, int BN, int BM>
+template <int CG, int NC, int BN, int BM, int KS = 1>
 cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttribute *attr, bool overlap = false) {
+    using C = Cfg<CG, NC, BN, BM, KS>;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(Cfg<CG, NC, BN, BM>::THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Cfg<CG, NC, BN, BM>::SMEM_ALLOC;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM_ALLOC;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.x = C::CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
@@ -58,16 +60,16 @@ cudaLaunchConfig_t launch_config(dim3 grid, cudaStream_t stream, cudaLaunchAttri
     return cfg;
 }
 
-template <int CG, int NC, int BN, int BM = 128>
+template <int CG, int NC, int BN, int BM = 128, int KS = 1>
 int prepare_kernel(int *max_clusters) {
-    using C = Cfg<CG, NC, BN, BM>;
-    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC, BN, BM>,
+    using C = Cfg<CG, NC, BN, BM, KS>;
+    cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC, BN, BM, KS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg = launch_config<CG, NC, BN, BM>(dim3(CG, 1, 1), nullptr, attr);
+    cudaLaunchConfig_t cfg = launch_config<CG, NC, BN, BM, KS>(dim3(C::CLUSTER, 1, 1), nullptr, attr);
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC, BN, BM>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, gemm_f16_nt_kernel<CG, NC, BN, BM, KS>, &cfg);
     if (e != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
     *max_clusters = n;
     return GEMM_OK;
@@ -100,6 +102,9 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
             if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2, 256>(&d.max_clusters[2]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64>(&d.max_clusters[3]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64>(&d.max_clusters[4]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64, 2>(&d.max_clusters[5]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64, 4>(&d.max_clusters[6]);
+            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64, 8>(&d.max_clusters[7]);
         }
         if (d.status == GEMM_OK && g_encode == nullptr) {
             void *fn = nullptr;
@@ -160,6 +165,7 @@ struct Opts {
     int32_t consumers = 1;
     int32_t block_n = 0;    // tile width 256 or 64; 0: chosen from the shape (resolve_config)
     int32_t block_m = 0;    // rows per CTA 128 or 64 (64 only with block_n 64); 0: chosen likewise
+    int32_t cluster_k = 0;  // tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 chosen likewise
     int32_t max_clusters = 0;
     int32_t raster_group = 0;
     int64_t timeout_ns = kDefaultTimeoutNs;
@@ -178,6 +184,11 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
         o->block_n = opts->block_n;
         if (opts->block_m != 0 && opts->block_m != 64 && opts->block_m != 128) return GEMM_ERR_INVALID_ARG;
         o->block_m = opts->block_m;
+        if (opts->cluster_k != 0 && opts->cluster_k != 1 && opts->cluster_k != 2 && opts->cluster_k != 4 &&
+            opts->cluster_k != 8) {
+            return GEMM_ERR_INVALID_ARG;
+        }
+        o->cluster_k = opts->cluster_k;
         if (opts->max_clusters < 0 || opts->raster_group < 0 || opts->timeout_ns < 0 ||
             (opts->debug_flags & ~static_cast<int32_t>(kDebugProducerPhase0)) != 0) {
             return GEMM_ERR_INVALID_ARG;
@@ -189,12 +200,63 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     }
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o->consumers == 2 && o->cta_group == 1) return GEMM_ERR_INVALID_ARG;
+    if (o->cluster_k > 1) {
+        if (o->block_m == 128) return GEMM_ERR_INVALID_ARG;
+        o->block_m = 64;  // the K split runs on tiny tiles
+    }
     if (o->block_m == 64) {
         if (o->block_n == 256) return GEMM_ERR_INVALID_ARG;
         o->block_n = 64;  // 64-row tiles are 64 wide
     }
     if (o->block_n == 64 && (o->cta_group == 2 || o->consumers == 2)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
+}
+
+// The K split of tiny tiles across a cluster (cluster_k).  Each cluster owns
+// one 64 x 64 tile and each of its KS CTAs one K slice, so a CTA streams 1/KS
+// of the tile's operands: small problems with a long K are bound by how fast
+// one SM's loads arrive, not by the tensor pipe.  The slices' fp32 sums meet
+// in shared memory through the copy engine and are added in the same kernel
+// (no workspace, no second launch), which costs about a microsecond more
+// than the tiles alone.  Measured on GB300 (graph-timed, us, KS = 1 / 2 / 4 /
+// 8): 256x256x128 2.14 / 3.06, 256x256x512 2.86 / 3.35 / 3.14 / 6.80 (16
+// clusters of 8 do not all fit at once: two waves), 256x256x1024 4.10 /
+// 3.91 / 3.46, 256x256x4096 10.08 / 7.16 / 5.16 / 8.82, 128x128x4096 10.10 /
+// 7.01 / 5.00 / 3.84, 128x1024x1024 4.24 / 3.97 / 4.26, 384x384x2048 6.19 /
+// 5.20 / 5.17, 512x512x512 2.90 / 4.25, 512x512x4096 10.21 / 8.45 / 12.68.
+// So the split pays from 16 K tiles of 64 on, with at least 4 per CTA, while
+// the grid leaves half of the SMs to the next kernel's set-up (tiles * KS at
+// most half the co-resident CTAs); with at least 24 K tiles per CTA a whole
+// wave of clusters still pays.  Automatic: the largest KS of 8, 4, 2 that
+// meets this; a grid capped by max_clusters keeps the persistent tiles.
+// Forced: at most the number of K tiles.
+int32_t tiny_cluster_k(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o) {
+    const int64_t k_tiles = (K + 63) / 64;
+    const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
+    int32_t ks = o.cluster_k;
+    if (ks == 0) {
+        if (o.max_clusters > 0 || k_tiles < 16) return 1;
+        const int32_t options[3] = {8, 4, 2};
+        const int slot[3] = {7, 6, 5};
+        for (int i = 0; i < 3; ++i) {
+            const int64_t per_cta = k_tiles / options[i];
+            if (per_cta < 4 || tiles > dev.max_clusters[slot[i]]) continue;  // all clusters in one wave
+            if (2 * tiles * options[i] <= dev.max_clusters[4] || per_cta >= 24) return options[i];
+        }
+        return 1;
+    }
+    while (ks > 1 && ks > k_tiles) ks /= 2;  // every CTA needs a K tile
+    return ks;
+}
+
+// Whether a problem left to the defaults would take the tiny tiles with a K
+// split (which then wins over split-K through a workspace).
+bool tiny_cluster_k_applies(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o) {
+    if (o.block_m == 128 || o.cluster_k == 1) return false;
+    int64_t ctas = dev.max_clusters[4];
+    if (o.max_clusters > 0 && o.max_clusters < ctas) ctas = o.max_clusters;
+    if (o.block_m == 0 && 3 * ((M + 63) / 64) * ((N + 63) / 64) > 2 * ctas) return false;
+    return tiny_cluster_k(M, N, K, dev, o) > 1;
 }
 
 // The default CTA group and tile width.
@@ -231,7 +293,7 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
             int64_t ctas = dev.max_clusters[3];
             if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
             narrow = ((M + 127) / 128) * ((N + 63) / 64) <= ctas;
-            if (narrow && allow_splitk) {
+            if (narrow && allow_splitk && !tiny_cluster_k_applies(M, N, K, dev, *o)) {
                 int64_t pairs = dev.max_clusters[1];
                 if (o->max_clusters > 0 && o->max_clusters < pairs) pairs = o->max_clusters;
                 const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
@@ -251,8 +313,10 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
             if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
             o->block_m = 3 * ((M + 63) / 64) * ((N + 63) / 64) <= 2 * ctas ? 64 : 128;
         }
+        o->cluster_k = o->block_m == 64 ? tiny_cluster_k(M, N, K, dev, *o) : 1;
         return;
     }
+    o->cluster_k = 1;
     o->block_m = 128;
     if (o->cta_group != 0) return;
     if (o->consumers == 2) {
@@ -273,10 +337,10 @@ struct Plan {
     int64_t workspace_bytes;   // split-K partials, 0 without split-K
 };
 
-template <int CG, int NC, int BN, int BM = 128>
+template <int CG, int NC, int BN, int BM = 128, int KS = 1>
 int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o, bool allow_splitk,
               Plan *out) {
-    using C = Cfg<CG, NC, BN, BM>;
+    using C = Cfg<CG, NC, BN, BM, KS>;
     Params &p = out->p;
     p = Params{};
     p.M = static_cast<int32_t>(M);
@@ -291,6 +355,16 @@ int make_plan(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts
     p.raster_group = o.raster_group > 0 ? o.raster_group : auto_raster_group(p.num_m_tiles, K, C::TILE_M);
     p.debug_flags = o.debug_flags;
     p.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
+    if constexpr (C::KSPLIT) {
+        // one cluster per tile, CTA s of the cluster on K slice s: item
+        // t * KS + s, the numbering of split-K, one item per CTA
+        p.slices = KS;
+        p.split_from = p.num_tiles;
+        p.num_items = p.num_tiles * KS;
+        out->workspace_bytes = 0;
+        out->clusters = p.num_tiles;
+        return GEMM_OK;
+    }
     int64_t clusters = dev.max_clusters[C::KIND];
     if (o.max_clusters > 0 && o.max_clusters < clusters) clusters = o.max_clusters;
     p.slices = (allow_splitk && NC == 1 && !C::NARROW)
@@ -337,16 +411,16 @@ cudaError_t launch_reduce(const cudaLaunchConfig_t *cfg, int slices, const float
     }
 }
 
-template <int CG, int NC, int BN, int BM = 128>
+template <int CG, int NC, int BN, int BM = 128, int KS = 1>
 int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, cudaStream_t stream,
            const DeviceInfo &dev, const Opts &o, void *workspace, int64_t workspace_bytes) {
-    using C = Cfg<CG, NC, BN, BM>;
+    using C = Cfg<CG, NC, BN, BM, KS>;
     Plan plan;
-    int st = make_plan<CG, NC, BN, BM>(M, N, K, dev, o, workspace != nullptr, &plan);
+    int st = make_plan<CG, NC, BN, BM, KS>(M, N, K, dev, o, workspace != nullptr, &plan);
     if (st != GEMM_OK) return st;
-    if (plan.p.slices > 1 && (workspace_bytes < plan.workspace_bytes ||
-                              (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)) {
-        st = make_plan<CG, NC, BN, BM>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
+    if (plan.p.slices > 1 && !C::KSPLIT &&
+        (workspace_bytes < plan.workspace_bytes || (reinterpret_cast<uintptr_t>(workspace) & 15u) != 0)) {
+        st = make_plan<CG, NC, BN, BM, KS>(M, N, K, dev, o, false, &plan);  // workspace too small: no split-K
         if (st != GEMM_OK) return st;
     }
     Params &p = plan.p;
@@ -356,22 +430,22 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
         return GEMM_ERR_CUDA;
     }
     p.D = reinterpret_cast<uint16_t *>(D);
-    p.partial = p.slices > 1 ? reinterpret_cast<float *>(workspace) : nullptr;
+    p.partial = p.slices > 1 && !C::KSPLIT ? reinterpret_cast<float *>(workspace) : nullptr;
     CUtensorMap tmP;
-    if (p.slices > 1) {
+    if (p.slices > 1 && !C::KSPLIT) {
         if (encode_partial_map(&tmP, workspace, p.slices, M, N) != GEMM_OK) return GEMM_ERR_CUDA;
     } else {
         tmP = tmD;  // unused without split-K
     }
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        launch_config<CG, NC, BN, BM>(dim3(static_cast<unsigned>(plan.clusters * CG), 1, 1), stream, attr, o.overlap);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC, BN, BM>, tmA, tmB, tmBh, tmD, tmP, p);
+    cudaLaunchConfig_t cfg = launch_config<CG, NC, BN, BM, KS>(
+        dim3(static_cast<unsigned>(plan.clusters * C::CLUSTER), 1, 1), stream, attr, o.overlap);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_f16_nt_kernel<CG, NC, BN, BM, KS>, tmA, tmB, tmBh, tmD, tmP, p);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return GEMM_ERR_LAUNCH;
     }
-    if (p.slices > 1) {
+    if (p.slices > 1 && !C::KSPLIT) {
         // second pass: add the slices' partials and round once (its CTAs may
         // start early; griddepcontrol.wait orders it after the GEMM)
         const int64_t units = M * N / 4;
@@ -423,7 +497,14 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_fill(D, M, N, s);
     resolve_config(M, N, K, *info, workspace != nullptr, &o);
-    if (o.block_n == 64 && o.block_m == 64) return launch<1, 1, 64, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+    if (o.block_n == 64 && o.block_m == 64) {
+        switch (o.cluster_k) {
+            case 2: return launch<1, 1, 64, 64, 2>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+            case 4: return launch<1, 1, 64, 64, 4>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+            case 8: return launch<1, 1, 64, 64, 8>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+            default: return launch<1, 1, 64, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+        }
+    }
     if (o.block_n == 64) return launch<1, 1, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.cta_group == 2 && o.consumers == 2) return launch<2, 2, 256>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.cta_group == 2) return launch<2, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
@@ -505,7 +586,16 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
     resolve_config(M, N, K, *info, ws, &o);
     Plan plan;
     int stages = 0;
-    if (o.block_n == 64 && o.block_m == 64) {
+    if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 2) {
+        st = make_plan<1, 1, 64, 64, 2>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64, 2>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 4) {
+        st = make_plan<1, 1, 64, 64, 4>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64, 4>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 8) {
+        st = make_plan<1, 1, 64, 64, 8>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64, 8>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64) {
         st = make_plan<1, 1, 64, 64>(M, N, K, *info, o, false, &plan);
         stages = Cfg<1, 1, 64, 64>::STAGES;
     } else if (o.block_n == 64) {
@@ -527,7 +617,8 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
     out->block_n = o.block_n;
     out->block_m = o.block_m;
     out->stages = stages;
-    out->split_k = plan.p.slices;
+    out->cluster_k = o.cluster_k > 1 ? o.cluster_k : 1;
+    out->split_k = o.cluster_k > 1 ? 1 : plan.p.slices;
     out->clusters = plan.clusters;
     out->work_items = plan.p.num_items;
     out->workspace_bytes = plan.workspace_bytes;
@@ -592,7 +683,8 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
         (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
         (block_n == 64 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
         (block_m == 64 && block_n != 64) || raster_group < 0 ||
-        (split_k != 0 && split_k != 1) || K < 0 ||
+        (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8) ||
+        (split_k > 1 && block_m != 64) || K < 0 ||
         K > kDimLimit || M <= 0 || N <= 0 || M > kDimLimit || N > kDimLimit || num_clusters <= 0 ||
         num_clusters > kDimLimit || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !out) {
         return GEMM_ERR_INVALID_ARG;
@@ -604,9 +696,14 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
     const int32_t k_tiles = static_cast<int32_t>((K + 63) / 64);
     if (raster_group == 0) raster_group = auto_raster_group(static_cast<int32_t>(num_m), K, static_cast<int32_t>(tile_m));
     const bool narrow = block_n == 64;
-    const int32_t slices = (split_k && consumers == 1 && !narrow)
-                               ? splitk_slices(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters), k_tiles)
-                               : 1;
+    int32_t slices = 1;
+    if (split_k > 1) {
+        // tiny tiles with K split across clusters of split_k CTAs (cluster_k)
+        slices = split_k;
+        while (slices > 1 && slices > k_tiles) slices /= 2;
+    } else if (split_k && consumers == 1 && !narrow) {
+        slices = splitk_slices(static_cast<int32_t>(tiles), static_cast<int32_t>(num_clusters), k_tiles);
+    }
     int32_t split_from;
     int64_t items;
     if (slices > 1) {

@@ -89,23 +89,36 @@ enum : uint32_t { kRoleProducer = 1, kRoleMma = 2, kRoleEpilogue = 3 };
 #ifndef GEMM_F16_DEVICE_CHECKS
 #define GEMM_F16_DEVICE_CHECKS 0
 #endif
-enum : uint32_t { kCheckItem = 1, kCheckStage = 2, kCheckTmem = 3, kCheckChunk = 4, kCheckStaging = 5 };
+enum : uint32_t {
+    kCheckItem = 1,
+    kCheckStage = 2,
+    kCheckTmem = 3,
+    kCheckChunk = 4,
+    kCheckStaging = 5,
+    kCheckReduceRow = 6
+};
 
 // BN is the tile width: 256, or 64 for the narrow single-CTA tiles of small
 // problems (more CTAs, and a ring deep enough to hold a K of 512 at once).
 // BM is the rows of D per CTA and consumer: 128, or 64 for the tiny tiles
-// (64 x 64) of the smallest problems.
-template <int CG, int NC, int BN = 256, int BM = 128>
+// (64 x 64) of the smallest problems.  KS > 1 (tiny tiles only) splits K
+// across a cluster of KS CTAs that add their partial sums through
+// distributed shared memory.
+template <int CG, int NC, int BN = 256, int BM = 128, int KS = 1>
 struct Cfg {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(NC == 1 || (NC == 2 && CG == 2), "two consumers need a CTA pair");
     static_assert(BN == 256 || (BN == 64 && CG == 1 && NC == 1), "narrow tiles are single-CTA, one consumer");
     static_assert(BM == 128 || (BM == 64 && BN == 64), "64-row tiles are narrow");
+    static_assert(KS == 1 || ((KS == 2 || KS == 4 || KS == 8) && BM == 64), "a K split over 2, 4 or 8 tiny CTAs");
     static constexpr bool NARROW = BN != 256;
     static constexpr bool TINY = BM == 64;
+    static constexpr bool KSPLIT = KS > 1;
+    static constexpr int CLUSTER = CG * KS;             // CTAs per cluster
     // co-resident cluster count slot of this configuration in the host's
     // per-device table
-    static constexpr int KIND = TINY ? 4 : (NARROW ? 3 : (CG == 1 ? 0 : NC));
+    static constexpr int KIND = KSPLIT ? (KS == 2 ? 5 : (KS == 4 ? 6 : 7))
+                                       : (TINY ? 4 : (NARROW ? 3 : (CG == 1 ? 0 : NC)));
     static constexpr int BLOCK_M = BM;                  // rows of D per CTA and consumer
     static constexpr int BLOCK_N = BN;                  // columns of D per tile (MMA N)
     static constexpr int BLOCK_K = 64;                  // one 128-byte swizzle row of fp16
@@ -142,13 +155,22 @@ struct Cfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_D = OFF_B + STAGES * B_STAGE;
-    static constexpr int OFF_BAR = OFF_D + EPI_WARPS * EPI_BUFS * EPI_BUF;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;  // + drain
+    // K split: the CTA's own fp32 sums, all BLOCK_M rows, staged for the copies to their owners
+    static constexpr int OFF_SRC = OFF_D + EPI_WARPS * EPI_BUFS * EPI_BUF;
+    static constexpr int OFF_BAR = OFF_SRC + (KSPLIT ? BLOCK_M * BLOCK_N * 4 : 0);
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (KSPLIT ? 1 : 0);  // + drain (+ recv)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;         // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;            // alignment slack
     static_assert(SMEM_ALLOC <= 232448, "exceeds the 227 KiB per-block shared memory limit");
     static_assert(A_BLOCK % 1024 == 0 && B_STAGE % 1024 == 0 && EPI_BUF % 1024 == 0, "1 KiB swizzle atoms");
+    // with a K split, the staging buffers receive the cluster's fp32 partial
+    // sums of this CTA's rows: KS slices x (BLOCK_M / KS) rows x BLOCK_N fp32
+    static constexpr int KS_ROWS = BLOCK_M / KS;        // rows of the tile this CTA adds up and stores
+    static constexpr uint32_t KS_RECV_BYTES = BLOCK_M * BLOCK_N * 4;  // all slices of those rows
+    static_assert(!KSPLIT || (EPI_COALESCED && BLOCK_M * BLOCK_N * 4 <= EPI_WARPS * EPI_BUFS * EPI_BUF &&
+                              KS_ROWS % 8 == 0),
+                  "the cluster's partial sums of a CTA's rows fit its staging buffers");
 };
 
 struct Params {
@@ -205,14 +227,19 @@ __device__ __forceinline__ bool item_ok(const WorkItem &w, int32_t num_m, int32_
 
 // Bounded wait by one thread.  Returns false if the wait ran out (the failure
 // is recorded and the CTA's abort flag raised) or, when `honor_abort`, as soon
-// as another role of this CTA has aborted.
+// as another role of this CTA has aborted.  kCluster: acquire at cluster scope
+// (the arrivals come from other CTAs of the cluster).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                              uint64_t timeout_ns, uint32_t role, uint32_t seq,
                                              bool honor_abort = true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [](uint32_t b, uint32_t ph) {
+        return kCluster ? ptx::mbar_try_wait_cluster(b, ph) : ptx::mbar_try_wait(b, ph);
+    };
+    if (try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (honor_abort && *abort_flag) return false;
             if (ptx::globaltimer_ns() - t0 > timeout_ns) {
@@ -234,12 +261,12 @@ __device__ __forceinline__ void to_f16x2(const uint32_t (&in)[32], uint32_t *out
     }
 }
 
-template <int CG, int NC, int BN, int BM>
-__global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
+template <int CG, int NC, int BN, int BM, int KS = 1>
+__global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
     gemm_f16_nt_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmD,
                        const __grid_constant__ CUtensorMap tmP, const Params p) {
-    using C = Cfg<CG, NC, BN, BM>;
+    using C = Cfg<CG, NC, BN, BM, KS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -260,6 +287,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
     const uint32_t bar_tfull = bar_empty + 8 * C::STAGES;     // [ACC_BUFS]
     const uint32_t bar_tempty = bar_tfull + 8 * C::ACC_BUFS;  // [ACC_BUFS]
     const uint32_t bar_drain = bar_tempty + 8 * C::ACC_BUFS;
+    const uint32_t bar_recv = bar_drain + 8;  // K split: the cluster's partial rows have arrived
+    const uint32_t krank = C::KSPLIT ? ptx::cluster_ctarank() : 0u;  // K slice of this CTA
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -279,6 +308,12 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
             ptx::mbar_init(bar_tempty + 8 * a, C::EPI_WARPS * CG);
         }
         ptx::mbar_init(bar_drain, 1);
+        if constexpr (C::KSPLIT) {
+            // the cluster's copies of this CTA's rows complete KS_RECV_BYTES
+            // of transactions on it; its one arrival is made here
+            ptx::mbar_init(bar_recv, 1);
+            ptx::mbar_arrive_expect_tx(bar_recv, C::KS_RECV_BYTES);
+        }
         *abort_flag = 0;
         ptx::fence_mbarrier_init();
     }
@@ -287,8 +322,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
         ptx::tmem_relinquish<CG>();
     }
     ptx::tcgen05_fence_before();
-    if constexpr (CG == 2) {
-        ptx::cluster_sync();
+    if constexpr (C::CLUSTER > 1) {
+        ptx::cluster_sync();  // also: every barrier of the cluster initialised before any remote arrival
     } else {
         __syncthreads();
     }
@@ -588,6 +623,44 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
                         }
                         buf ^= 1u;
                     }
+                } else if constexpr (C::KSPLIT) {
+                    // K split across the cluster: CTA s adds up and stores
+                    // rows [s * KS_ROWS, (s + 1) * KS_ROWS) of the tile.
+                    // Lane r writes its row R's fp32 sums over this CTA's K
+                    // slice to row R of the CTA's source buffer (256 bytes,
+                    // 16-byte unit u at u ^ (R % 8): no bank conflicts); then
+                    // one lane copies the warp's rows, by the copy engine, to
+                    // slots krank * KS_ROWS + R % KS_ROWS of each owner's
+                    // staging buffers (the same swizzle, as KS_ROWS is a
+                    // multiple of 8), counted in bytes on its receive barrier.
+                    const uint32_t src = base + C::OFF_SRC;
+                    if (lane < C::WARP_ROWS) {
+                        const uint32_t R = static_cast<uint32_t>(quarter * C::WARP_ROWS + lane);
+                        const uint32_t row_addr = src + R * 256u;
+                        const uint32_t sw = R & 7u;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ sw) * 16u), lo[4 * j],
+                                              lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
+                            ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(8 + j) ^ sw) * 16u), hi[4 * j],
+                                              hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                        }
+                    }
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        // rows [r0, r0 + WARP_ROWS) of the tile, cut at owner boundaries
+                        const uint32_t r0 = static_cast<uint32_t>(quarter * C::WARP_ROWS);
+                        for (uint32_t R = r0; R < r0 + C::WARP_ROWS;) {
+                            const uint32_t owner = R / C::KS_ROWS;
+                            uint32_t end = (owner + 1) * C::KS_ROWS;
+                            if (end > r0 + C::WARP_ROWS) end = r0 + C::WARP_ROWS;
+                            const uint32_t slot = krank * C::KS_ROWS + R % C::KS_ROWS;
+                            ptx::bulk_copy_to_cluster(ptx::mapa(sD + slot * 256u, owner), src + R * 256u,
+                                                      (end - R) * 256u, ptx::mapa(bar_recv, owner));
+                            R = end;
+                        }
+                    }
                 } else if constexpr (C::EPI_COALESCED) {
                     // Narrow and tiny tiles: lane r holds row r of this warp's
                     // WARP_ROWS rows.  Each row goes to the warp's staging
@@ -653,9 +726,76 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM>::THREADS, 1)
         __syncwarp();
     }
 
-    // ---- teardown: both CTAs done with TMEM and with each other's SMEM
+    if constexpr (C::KSPLIT) {
+        // ---- K split: add the cluster's partial sums of this CTA's rows and
+        // store them.  Every thread arrives on the cluster barrier once its
+        // role is done, the epilogue's once all copies into this CTA have
+        // landed, and waits on it only before exit: when it completes, every
+        // copy of the cluster has landed, so no CTA leaves while a copy still
+        // reads or writes its shared memory.  The adding in between reads
+        // only this CTA's own shared memory.
+        ptx::tcgen05_fence_before();
+        if (warp < C::EPI_WARP0) ptx::cluster_arrive();
+        if (warp >= C::EPI_WARP0) {
+            // all KS slices of this CTA's rows are in: KS_RECV_BYTES of copies
+            const bool ok = wait_bounded<true>(bar_recv, 0, abort_flag, p.timeout_ns, kRoleEpilogue, 0xFFFFFFFEu);
+            ptx::cluster_arrive();
+            ptx::griddep_wait();  // returns at once when this warp has waited already
+            const WorkItem w = work_of(cluster, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
+                                       p.k_tiles, p.slices, C::BLOCK_N);
+            const CtaOrigin o = cta_origin(w, CG, 0, NC, C::BLOCK_N, C::BLOCK_M);
+            // per 8-column chunk of a row: add the KS slices in slice order
+            // (fp32), round once to fp16, store 16 bytes; eight consecutive
+            // threads cover one 128-byte row of D
+            for (int u = static_cast<int>(threadIdx.x) - 32 * C::EPI_WARP0; ok && u < C::KS_ROWS * 8;
+                 u += 32 * C::EPI_WARPS) {
+                const int r = u / 8;   // row among this CTA's rows
+                const int ch = u % 8;  // 8-column chunk
+                if (!in_bounds(krank < static_cast<uint32_t>(KS) && r < C::KS_ROWS, abort_flag, kRoleEpilogue,
+                               kCheckReduceRow, 0)) {
+                    break;
+                }
+                const uint32_t sw = static_cast<uint32_t>(r) & 7u;  // slot % 8 for every slice
+                float4 x, y;
+#pragma unroll
+                for (int j = 0; j < KS; ++j) {
+                    const uint32_t row_addr = sD + static_cast<uint32_t>(j * C::KS_ROWS + r) * 256u;
+                    const uint4 a = ptx::ld_shared_v4(row_addr + ((static_cast<uint32_t>(2 * ch) ^ sw) * 16u));
+                    const uint4 b = ptx::ld_shared_v4(row_addr + ((static_cast<uint32_t>(2 * ch + 1) ^ sw) * 16u));
+                    const float4 fa = make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),
+                                                  __uint_as_float(a.w));
+                    const float4 fb = make_float4(__uint_as_float(b.x), __uint_as_float(b.y), __uint_as_float(b.z),
+                                                  __uint_as_float(b.w));
+                    if (j == 0) {
+                        x = fa, y = fb;
+                    } else {
+                        x.x += fa.x, x.y += fa.y, x.z += fa.z, x.w += fa.w;
+                        y.x += fb.x, y.y += fb.y, y.z += fb.z, y.w += fb.w;
+                    }
+                }
+                const int32_t row = o.d_row + static_cast<int32_t>(krank) * C::KS_ROWS + r;
+                const int32_t col = o.d_col + 8 * ch;
+                if (row < p.M && col < p.N) {
+                    const __half2 h0 = __floats2half2_rn(x.x, x.y), h1 = __floats2half2_rn(x.z, x.w);
+                    const __half2 h2 = __floats2half2_rn(y.x, y.y), h3 = __floats2half2_rn(y.z, y.w);
+                    ptx::st_global_v4(p.D + static_cast<int64_t>(row) * p.N + col,
+                                      *reinterpret_cast<const uint32_t *>(&h0), *reinterpret_cast<const uint32_t *>(&h1),
+                                      *reinterpret_cast<const uint32_t *>(&h2), *reinterpret_cast<const uint32_t *>(&h3));
+                }
+            }
+        }
+        ptx::cluster_wait();
+        if (warp == 1) {
+            ptx::tcgen05_fence_after();
+            ptx::tmem_dealloc<CG>(tmem_base, C::TMEM_COLS);
+        }
+        return;
+    }
+
+    // ---- teardown: the cluster's CTAs done with TMEM and with each other's
+    // SMEM
     ptx::tcgen05_fence_before();
-    if constexpr (CG == 2) {
+    if constexpr (C::CLUSTER > 1) {
         ptx::cluster_sync();
     } else {
         __syncthreads();

@@ -109,6 +109,20 @@ typedef enum gemm_status {
  *                 most two thirds of the co-resident CTAs, else 128.  Other
  *                 values:
  *                 GEMM_ERR_INVALID_ARG.
+ *   cluster_k     2, 4 or 8 (needs block_m 0 or 64, which then means 64):
+ *                 tiny tiles with K split across a thread-block cluster of
+ *                 that many CTAs, one cluster per 64 x 64 tile and one K
+ *                 slice per CTA (at most one per 64-wide K tile, so fewer
+ *                 CTAs when K is short); each CTA keeps its slice's fp32 sums
+ *                 in shared memory and the cluster adds them, in slice order,
+ *                 through distributed shared memory before the one rounding
+ *                 to fp16.  No workspace and no second kernel.  Each CTA then
+ *                 streams 1/cluster_k of the tile's operands, which is what
+ *                 bounds small problems.  Not on the pages.  1: no K split.
+ *                 0 (default): with the tiny tiles and max_clusters 0, the
+ *                 largest of 8, 4, 2 that leaves each CTA a K tile and lets
+ *                 all the clusters run at once, else 1.  max_clusters does not
+ *                 cap this grid.  Other values: GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;
@@ -120,6 +134,7 @@ typedef struct gemm_f16_options {
     int32_t consumers;
     int32_t block_n;
     int32_t block_m;
+    int32_t cluster_k;
 } gemm_f16_options;
 
 /*
@@ -220,9 +235,12 @@ typedef struct gemm_f16_launch_info {
     int32_t split_k;          /* K slices S (1 = no split-K; > 1 adds the reduction kernel) */
     int32_t block_m;          /* rows of D per CTA and consumer: 128 or 64 */
     int32_t stages;           /* depth of the shared-memory operand ring */
-    int64_t clusters;         /* persistent clusters in the grid (CTAs = clusters * cta_group) */
-    int64_t work_items;       /* tiles, half tiles or K slices dealt to the clusters */
+    int64_t clusters;         /* clusters in the grid (CTAs = clusters * cta_group * cluster_k); persistent
+                                 unless cluster_k > 1, which runs one cluster per tile */
+    int64_t work_items;       /* tiles, half tiles or K slices dealt to the clusters (to the CTAs with
+                                 cluster_k > 1) */
     int64_t workspace_bytes;  /* split-K partials, 0 without split-K */
+    int32_t cluster_k;        /* CTAs sharing one tile's K (1 = none; see gemm_f16_options) */
 } gemm_f16_launch_info;
 
 /*
@@ -248,7 +266,8 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
  * first failure happened: bits 56-63 role (1 producer, 2 MMA issuer, 3
  * epilogue), 0-31 the tile's sequence number in that CTA, and 32-55 the CTA
  * index for a timeout, or 48-55 the check (1 work item, 2 ring stage, 3 TMEM
- * columns, 4 epilogue chunk, 5 staging buffer) and 32-47 the CTA index for a
+ * columns, 4 epilogue chunk, 5 staging buffer, 6 the rows a CTA adds up in a
+ * K split across a cluster) and 32-47 the CTA index for a
  * failed range check.  Returns GEMM_ERR_CUDA if the
  * synchronisation itself reports an error.
  */
@@ -281,7 +300,12 @@ typedef struct gemm_f16_work_item {
  * 148 CTAs leave 6.9 tiles per CTA, i.e. a partly idle last wave).  With
  * split_k = 1 (what gemm_f16_nt_ws() does given enough workspace) and few
  * tiles, K is instead cut into slices: item t*S + s is slice s of tile t.
- * Narrow and tiny tiles are never split, along N or K.
+ * Narrow and tiny tiles are never split along N, nor along K this way.
+ * split_k 2, 4 or 8 (tiny tiles only) is the K split across a cluster
+ * (cluster_k of gemm_f16_options): S = split_k, reduced to at most the
+ * number of 64-wide K tiles, with the same item numbering; that kernel runs
+ * one item per CTA, so pass num_clusters = T * S and iter 0 (CTA i of the
+ * grid runs item i; the S CTAs of tile t form one cluster).
  * Cluster `cluster_id` takes work items cluster_id, cluster_id + P, ...
  * Returns 1 and fills *out with the iter-th item of that cluster, 0 if the
  * cluster has no iter-th item, or GEMM_ERR_INVALID_ARG for bad arguments.

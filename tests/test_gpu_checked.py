@@ -3,7 +3,8 @@
 Instead of an external memory checker, the kernel carries its own range
 checks, compiled in only for the checked library (-DGEMM_F16_DEVICE_CHECKS=1):
 every work item the scheduler hands out, every ring stage, the TMEM columns of
-each accumulator, the epilogue's chunk count and staging buffer.  A failed
+each accumulator, the epilogue's chunk count and staging buffer, and the rows a
+CTA adds up when K is split across a cluster.  A failed
 check would end the kernel with GEMM_ERR_DEVICE_BOUNDS in the status word
 (never a trap).  Every kernel variant runs here through that build, over tile
 grids, ragged edges, split tails, split-K and few persistent clusters: no
@@ -23,9 +24,11 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # (M, N, K, cta_group, consumers, block_n, max_clusters, workspace[, block_m])
+    # (M, N, K, cta_group, consumers, block_n, max_clusters, workspace[, block_m[, cluster_k]])
     (128, 128, 64, 0, 0, 0, 0, False),       # default: tiny tiles
-    (256, 256, 512, 0, 0, 0, 0, False),
+    (256, 256, 512, 0, 0, 0, 0, False),      # default: tiny tiles, K split across clusters
+    (200, 136, 520, 1, 1, 64, 0, False, 64, 8),   # K split over 8 CTAs, ragged M, N and K
+    (520, 264, 1000, 1, 1, 64, 0, False, 64, 2),  # K split over 2 CTAs, K beyond the ring
     (700, 600, 1000, 1, 1, 64, 5, False, 64),  # tiny tiles, many per CTA, K beyond the ring
     (1000, 520, 1000, 2, 1, 256, 3, False),  # pairs, many tiles per cluster, ragged
     (1000, 520, 1000, 1, 1, 256, 5, False),  # single CTAs
@@ -52,12 +55,12 @@ def _call(lib, dA, dB, M, N, K, o, ws):
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(str(v) for v in c[:3]) + f"-cg{c[3]}-nc{c[4]}-bn{c[5]}"
-                         + (f"-bm{c[8]}" if len(c) > 8 else ""))
+                         + (f"-bm{c[8]}" if len(c) > 8 else "") + (f"-ck{c[9]}" if len(c) > 9 else ""))
 def test_checked_build_runs_clean_and_matches(gpu_lib, case):
     M, N, K, cg, nc, bn, clusters, use_ws = case[:8]
     checked, prod = gpu_lib.load_checked(), gpu_lib.load()
     o = gpu_lib.Options(cta_group=cg, consumers=nc, block_n=bn, max_clusters=clusters,
-                        block_m=case[8] if len(case) > 8 else 0)
+                        block_m=case[8] if len(case) > 8 else 0, cluster_k=case[9] if len(case) > 9 else 0)
     A, B = si.custom(M, N, K, seed=M + 2 * N + 3 * K).operands()
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     ws = None

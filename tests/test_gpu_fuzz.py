@@ -2,15 +2,16 @@
 
 Each case draws M (any), N and K (multiples of 8, the supported set), a kernel
 variant (default, CTA pair, single CTA, two consumers; further series the
-narrow 128 x 64 and the tiny 64 x 64 tiles), a cap on the number of
+narrow 128 x 64 and the tiny 64 x 64 tiles, and the tiny tiles with K split
+across clusters of 2, 4 or 8 CTAs), a cap on the number of
 persistent clusters (so that tail splits and multi-tile CTAs occur at small
 sizes) and an entry point (no workspace, caller workspace, the library's fixed
 scratch).  Every element must meet |gpu - oracle| <= 2^-9 |oracle| + 1e-3.
 
 GEMM_FUZZ_CASES and GEMM_FUZZ_SEED (environment) change the number of cases of
 the first series and the seed, and GEMM_FUZZ_SERIES_CASES the number of cases of
-each of the narrow and tiny series, for longer sweeps; the defaults are 36, 2026
-and 12.
+each of the narrow, tiny and K-split series, for longer sweeps; the defaults are
+36, 2026 and 12.
 """
 import ctypes
 import os
@@ -42,7 +43,7 @@ def _cases(n=36, seed=2026, per_series=12):
     out.append((n + 1, 500, 512, 2048, (1, 1), 0, "static"))
     # narrow and tiny tiles, forced, with the K-loop both inside and beyond
     # the 8- and 12-stage rings
-    for series, variant in ((1, (1, 1, 64, 128)), (2, (1, 1, 64, 64))):
+    for series, variant in ((1, (1, 1, 64, 128)), (2, (1, 1, 64, 64)), (3, None)):
         rng = np.random.default_rng(seed + series)
         first = n + 2 + per_series * (series - 1)
         for i in range(first, first + per_series):
@@ -51,7 +52,8 @@ def _cases(n=36, seed=2026, per_series=12):
             K = int(rng.integers(1, 130)) * 8
             clusters = int(rng.choice([0, 0, 1, 3, 7]))
             entry = ["nt", "ws", "static"][int(rng.integers(0, 3))]
-            out.append((i, M, N, K, variant, clusters, entry))
+            v = variant if variant is not None else (1, 1, 64, 64, int(rng.choice([2, 4, 8])))
+            out.append((i, M, N, K, v, clusters, entry))
     return out
 
 
@@ -66,7 +68,8 @@ def test_random_case(gpu_lib, i, M, N, K, variant, clusters, entry):
     dB = torch.from_numpy(B).cuda()
     D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
     o = gpu_lib.Options(cta_group=variant[0], consumers=variant[1], max_clusters=clusters,
-                        block_n=variant[2] if len(variant) > 2 else 0, block_m=variant[3] if len(variant) > 3 else 0)
+                        block_n=variant[2] if len(variant) > 2 else 0, block_m=variant[3] if len(variant) > 3 else 0,
+                        cluster_k=variant[4] if len(variant) > 4 else 0)
     stream = torch.cuda.current_stream().cuda_stream
     if entry == "nt":
         rc = gpu_lib.gemm_f16_nt_ptr(dA.data_ptr(), dB.data_ptr(), D.data_ptr(), M, N, K, stream, o)

@@ -48,17 +48,21 @@ def assert_close(gpu_f16, ref_bits, what=""):
                              f"gpu={got[i]!r} oracle={ref[i]!r}")
 
 
-# (cta_group, consumers, block_n[, block_m]): the CTA pair with one MMA
-# consumer (the default), a single CTA, the pair with two consumers sharing
-# each B stage, the narrow 128 x 64 single-CTA tiles of small problems, and the
-# tiny 64 x 64 tiles (MMAs of M = 64) of the smallest.
-VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64, 128), (1, 1, 64, 64)]
-VIDS = ["pair", "single", "pair-2consumers", "narrow", "tiny"]
+# (cta_group, consumers, block_n[, block_m[, cluster_k]]): the CTA pair with
+# one MMA consumer (the default), a single CTA, the pair with two consumers
+# sharing each B stage, the narrow 128 x 64 single-CTA tiles of small problems,
+# the tiny 64 x 64 tiles (MMAs of M = 64) of the smallest, without a K split
+# and with K split across clusters of 2, 4 and 8 CTAs (fewer where K has fewer
+# 64-wide tiles).
+VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64, 128), (1, 1, 64, 64, 1), (1, 1, 64, 64, 2),
+            (1, 1, 64, 64, 4), (1, 1, 64, 64, 8)]
+VIDS = ["pair", "single", "pair-2consumers", "narrow", "tiny", "tiny-k2", "tiny-k4", "tiny-k8"]
 
 
 def opts(g, variant=(0, 0), max_clusters=0):
     return g.Options(cta_group=variant[0], max_clusters=max_clusters, consumers=variant[1],
-                     block_n=variant[2] if len(variant) > 2 else 0, block_m=variant[3] if len(variant) > 3 else 0)
+                     block_n=variant[2] if len(variant) > 2 else 0, block_m=variant[3] if len(variant) > 3 else 0,
+                     cluster_k=variant[4] if len(variant) > 4 else 0)
 
 
 # ----------------------------------------------------------- full compares --
@@ -69,6 +73,15 @@ def test_small_workloads_full(gpu_lib, name, v):
     w = si.WORKLOADS[name]
     A, B = w.operands()
     assert_close(run(gpu_lib, A, B, opts(gpu_lib, v)), oracle.gemm_f16_nt(A, B), f"{name} {v}")
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 4096), (128, 128, 4096), (128, 1024, 1024), (200, 136, 3000)])
+def test_default_cluster_k_split_full(gpu_lib, M, N, K):
+    # small outputs with a long K take tiny tiles with K split across a cluster by default
+    ks = gpu_lib.describe(M, N, K)["cluster_k"]
+    assert ks > 1, "this shape is meant to split K across a cluster"
+    A, B = si.custom(M, N, K, seed=M + N + K + 5).operands()
+    assert_close(run(gpu_lib, A, B), oracle.gemm_f16_nt(A, B), f"{M}x{N}x{K} cluster_k={ks}")
 
 
 @pytest.mark.parametrize("v", VARIANTS, ids=VIDS)
@@ -213,7 +226,7 @@ def test_binding_workspace_on_a_side_stream(gpu_lib):
     # The binding's cached split-K workspace belongs to the stream the call runs on; a larger
     # problem on the same stream replaces it while the first GEMM may still be queued.
     side = torch.cuda.Stream()
-    shapes = [(256, 256, 4096), (512, 512, 4096)]  # 2 MiB, then 8 MiB of partials
+    shapes = [(768, 640, 4096), (768, 768, 4096)]  # 15 MiB, then 18 MiB of partials
     outs = []
     for i, (M, N, K) in enumerate(shapes):
         assert gpu_lib.workspace_size(M, N, K) > 0
