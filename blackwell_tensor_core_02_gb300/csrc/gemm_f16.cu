@@ -102,9 +102,17 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
             if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2, 256>(&d.max_clusters[2]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64>(&d.max_clusters[3]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64>(&d.max_clusters[4]);
-            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64, 2>(&d.max_clusters[5]);
-            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64, 4>(&d.max_clusters[6]);
-            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64, 8>(&d.max_clusters[7]);
+            // The K splits across clusters are optional: a device that cannot
+            // co-schedule clusters of that size (0 co-resident) never takes them.
+            if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 64, 2>(&d.max_clusters[5]) != GEMM_OK) {
+                d.max_clusters[5] = 0;
+            }
+            if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 64, 4>(&d.max_clusters[6]) != GEMM_OK) {
+                d.max_clusters[6] = 0;
+            }
+            if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 64, 8>(&d.max_clusters[7]) != GEMM_OK) {
+                d.max_clusters[7] = 0;
+            }
         }
         if (d.status == GEMM_OK && g_encode == nullptr) {
             void *fn = nullptr;
@@ -229,7 +237,8 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
 // most half the co-resident CTAs); with at least 24 K tiles per CTA a whole
 // wave of clusters still pays.  Automatic: the largest KS of 8, 4, 2 that
 // meets this; a grid capped by max_clusters keeps the persistent tiles.
-// Forced: at most the number of K tiles.
+// Forced: at most the number of K tiles, and halved until the device can
+// co-schedule clusters of that size.
 int32_t tiny_cluster_k(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o) {
     const int64_t k_tiles = (K + 63) / 64;
     const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
@@ -245,7 +254,8 @@ int32_t tiny_cluster_k(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, c
         }
         return 1;
     }
-    while (ks > 1 && ks > k_tiles) ks /= 2;  // every CTA needs a K tile
+    // every CTA needs a K tile, and the device must co-schedule clusters of that size
+    while (ks > 1 && (ks > k_tiles || dev.max_clusters[ks == 2 ? 5 : (ks == 4 ? 6 : 7)] <= 0)) ks /= 2;
     return ks;
 }
 

@@ -113,7 +113,8 @@ typedef enum gemm_status {
  *                 tiny tiles with K split across a thread-block cluster of
  *                 that many CTAs, one cluster per 64 x 64 tile and one K
  *                 slice per CTA (at most one per 64-wide K tile, so fewer
- *                 CTAs when K is short); each CTA keeps its slice's fp32 sums
+ *                 CTAs when K is short, and halved until the device can run
+ *                 clusters of that size); each CTA keeps its slice's fp32 sums
  *                 in shared memory and the cluster adds them, in slice order,
  *                 through distributed shared memory before the one rounding
  *                 to fp16.  No workspace and no second kernel.  Each CTA then

@@ -20,13 +20,22 @@ pytestmark = pytest.mark.gpu
 TIMEOUT = -7
 
 
-@pytest.mark.parametrize("cg,consumers", [(2, 1), (1, 1), (2, 2)])
-def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg, consumers):
+# (cta_group, consumers, block_n, block_m, cluster_k): the CTA pair, a single CTA, two
+# consumers, narrow and tiny tiles, and tiny tiles with K split across clusters of 4 and 8
+# CTAs (there every CTA still reaches the cluster barrier after its roles gave up)
+VARIANTS = [(2, 1, 0, 0, 0), (1, 1, 0, 0, 0), (2, 2, 0, 0, 0), (1, 1, 64, 128, 0), (1, 1, 64, 64, 1),
+            (1, 1, 64, 64, 4), (1, 1, 64, 64, 8)]
+
+
+@pytest.mark.parametrize("cg,consumers,bn,bm,ks", VARIANTS,
+                         ids=["pair", "single", "pair-2consumers", "narrow", "tiny", "tiny-k4", "tiny-k8"])
+def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg, consumers, bn, bm, ks):
     w = si.WORKLOADS["ktile_grid_256x256x512"]
     A, B = w.operands()
     dA, dB = torch.from_numpy(A).cuda(), torch.from_numpy(B).cuda()
     D = torch.zeros((w.M, w.N), dtype=torch.float16, device="cuda")
-    bad = gpu_lib.Options(cta_group=cg, consumers=consumers, debug_flags=1, timeout_ns=100_000_000)  # 0.1 s a wait
+    shape = dict(cta_group=cg, consumers=consumers, block_n=bn, block_m=bm, cluster_k=ks)
+    bad = gpu_lib.Options(**shape, debug_flags=1, timeout_ns=100_000_000)  # 0.1 s a wait
     gpu_lib.gemm_f16_nt(dA, dB, D, options=bad)
     status, info = gpu_lib.last_device_status()
     assert status == TIMEOUT, gpu_lib.status_string(status)
@@ -34,7 +43,7 @@ def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg, consumers):
     # limit runs out first is recorded (producer 1, MMA issuer 2, epilogue 3)
     assert info >> 56 in (1, 2, 3)
     # a later, correct launch on the same context works and leaves the status clear
-    D2 = gpu_lib.gemm_f16_nt(dA, dB, options=gpu_lib.Options(cta_group=cg, consumers=consumers))
+    D2 = gpu_lib.gemm_f16_nt(dA, dB, options=gpu_lib.Options(**shape))
     assert gpu_lib.last_device_status()[0] == 0
     got = D2.cpu().numpy().astype(np.float64)
     ref = oracle.gemm_f16_nt(A, B).view(np.float16).astype(np.float64)
