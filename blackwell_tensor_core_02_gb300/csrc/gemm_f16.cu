@@ -225,14 +225,14 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
 // of the tile's operands: small problems with a long K are bound by how fast
 // one SM's loads arrive, not by the tensor pipe.  The slices' fp32 sums meet
 // in shared memory through the copy engine and are added in the same kernel
-// (no workspace, no second launch), which costs about a microsecond more
-// than the tiles alone.  Measured on GB300 (graph-timed, us, KS = 1 / 2 / 4 /
-// 8): 256x256x128 2.14 / 3.06, 256x256x512 2.86 / 3.35 / 3.14 / 6.80 (16
-// clusters of 8 do not all fit at once: two waves), 256x256x1024 4.10 /
-// 3.91 / 3.46, 256x256x4096 10.08 / 7.16 / 5.16 / 8.82, 128x128x4096 10.10 /
-// 7.01 / 5.00 / 3.84, 128x1024x1024 4.24 / 3.97 / 4.26, 384x384x2048 6.19 /
-// 5.20 / 5.17, 512x512x512 2.90 / 4.25, 512x512x4096 10.21 / 8.45 / 12.68.
-// So the split pays from 16 K tiles of 64 on, with at least 4 per CTA, while
+// (no workspace, no second launch), which costs about half a microsecond
+// more than the tiles alone.  Measured on GB300 (graph-timed, us, KS = 1 / 2
+// / 4 / 8): 256x256x128 2.15 / 2.70, 256x256x512 2.86 / 3.00 / 2.79 / 6.11
+// (16 clusters of 8 do not all fit at once: two waves), 256x256x1024 4.12 /
+// 3.55 / 3.07, 256x256x4096 10.10 / 6.81 / 4.81 / 8.15, 128x128x4096 10.13 /
+// 6.64 / 4.65 / 3.49, 128x1024x1024 4.25 / 3.61 / 3.91, 384x384x2048 6.21 /
+// 4.84 / 4.78, 512x512x512 2.90 / 3.87, 512x512x4096 10.25 / 8.10 / 11.97.
+// So the split pays from 8 K tiles of 64 on, with at least 2 per CTA, while
 // the grid leaves half of the SMs to the next kernel's set-up (tiles * KS at
 // most half the co-resident CTAs); with at least 24 K tiles per CTA a whole
 // wave of clusters still pays.  Automatic: the largest KS of 8, 4, 2 that
@@ -244,12 +244,12 @@ int32_t tiny_cluster_k(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, c
     const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
     int32_t ks = o.cluster_k;
     if (ks == 0) {
-        if (o.max_clusters > 0 || k_tiles < 16) return 1;
+        if (o.max_clusters > 0 || k_tiles < 8) return 1;
         const int32_t options[3] = {8, 4, 2};
         const int slot[3] = {7, 6, 5};
         for (int i = 0; i < 3; ++i) {
             const int64_t per_cta = k_tiles / options[i];
-            if (per_cta < 4 || tiles > dev.max_clusters[slot[i]]) continue;  // all clusters in one wave
+            if (per_cta < 2 || tiles > dev.max_clusters[slot[i]]) continue;  // all clusters in one wave
             if (2 * tiles * options[i] <= dev.max_clusters[4] || per_cta >= 24) return options[i];
         }
         return 1;

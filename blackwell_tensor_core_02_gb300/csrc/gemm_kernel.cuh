@@ -737,13 +737,17 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
         ptx::tcgen05_fence_before();
         if (warp < C::EPI_WARP0) ptx::cluster_arrive();
         if (warp >= C::EPI_WARP0) {
-            // all KS slices of this CTA's rows are in: KS_RECV_BYTES of copies
-            const bool ok = wait_bounded<true>(bar_recv, 0, abort_flag, p.timeout_ns, kRoleEpilogue, 0xFFFFFFFEu);
-            ptx::cluster_arrive();
+            // where this CTA's rows go, worked out while the copies are in flight
             ptx::griddep_wait();  // returns at once when this warp has waited already
             const WorkItem w = work_of(cluster, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
                                        p.k_tiles, p.slices, C::BLOCK_N);
             const CtaOrigin o = cta_origin(w, CG, 0, NC, C::BLOCK_N, C::BLOCK_M);
+            // all KS slices of this CTA's rows are in: KS_RECV_BYTES of copies.
+            // The arrival needs no release: it only has to follow the wait,
+            // and what the barrier guards (no copy still touching a CTA's
+            // shared memory at exit) is the completion this thread just saw.
+            const bool ok = wait_bounded<true>(bar_recv, 0, abort_flag, p.timeout_ns, kRoleEpilogue, 0xFFFFFFFEu);
+            ptx::cluster_arrive_relaxed();
             // per 8-column chunk of a row: add the KS slices in slice order
             // (fp32), round once to fp16, store 16 bytes; eight consecutive
             // threads cover one 128-byte row of D

@@ -52,6 +52,12 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void cluster_arrive() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
+// An arrival that orders no memory operations (a release at cluster scope can
+// cost hundreds of cycles): for a thread whose arrival only has to come after
+// something it has already observed, such as an mbarrier wait that returned.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // Address of the same shared-memory offset in CTA `rank` of this cluster.

@@ -120,10 +120,13 @@ typedef enum gemm_status {
  *                 to fp16.  No workspace and no second kernel.  Each CTA then
  *                 streams 1/cluster_k of the tile's operands, which is what
  *                 bounds small problems.  Not on the pages.  1: no K split.
- *                 0 (default): with the tiny tiles and max_clusters 0, the
- *                 largest of 8, 4, 2 that leaves each CTA a K tile and lets
- *                 all the clusters run at once, else 1.  max_clusters does not
- *                 cap this grid.  Other values: GEMM_ERR_INVALID_ARG.
+ *                 0 (default): with the tiny tiles, max_clusters 0 and at
+ *                 least 8 K tiles of 64, the largest of 8, 4, 2 that leaves
+ *                 each CTA at least 2 K tiles, lets all the clusters run at
+ *                 once and keeps the grid within half the co-resident CTAs
+ *                 (within all of them from 24 K tiles per CTA), else 1.
+ *                 max_clusters does not cap this grid.  Other values:
+ *                 GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;

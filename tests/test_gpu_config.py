@@ -22,13 +22,13 @@ def test_smallest_problems_take_tiny_tiles(gpu_lib):
     c1 = gpu_lib.describe(128, 128, 64)
     assert (c1["cta_group"], c1["block_n"], c1["block_m"], c1["split_k"], c1["clusters"], c1["work_items"],
             c1["stages"]) == (1, 64, 64, 1, 4, 4, 12)
-    c2 = gpu_lib.describe(256, 256, 512)
-    assert (c2["cta_group"], c2["block_n"], c2["block_m"], c2["split_k"], c2["clusters"],
-            c2["work_items"]) == (1, 64, 64, 1, 16, 16)
+    c2 = gpu_lib.describe(256, 256, 512)  # sixteen tiles, K split across clusters of 4
+    assert (c2["cta_group"], c2["block_n"], c2["block_m"], c2["split_k"], c2["cluster_k"], c2["clusters"],
+            c2["work_items"]) == (1, 64, 64, 1, 4, 16, 64)
     # 64 x 64 tiles up to two thirds of the co-resident CTAs, any K, without a workspace
     P = _resident_tiny_ctas(gpu_lib)
     assert P >= 140  # GB300: 152 SMs, one tiny-tile CTA each
-    for M, N, K in ((256, 256, 512), (512, 512, 512), (64 * (2 * P // 3), 64, 1024), (576, 576, 1024),
+    for M, N, K in ((256, 256, 448), (512, 512, 512), (64 * (2 * P // 3), 64, 1024), (576, 576, 1024),
                     (200, 1000, 72)):
         c = gpu_lib.describe(M, N, K)
         tiles = -(-M // 64) * -(-N // 64)
@@ -38,12 +38,13 @@ def test_smallest_problems_take_tiny_tiles(gpu_lib):
 
 
 def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
-    # from 16 K tiles of 64 on, tiny tiles split K across a cluster: the largest of 8, 4, 2 CTAs
-    # that leaves each at least 4 K tiles, with tiles * cluster_k at most half the co-resident
+    # from 8 K tiles of 64 on, tiny tiles split K across a cluster: the largest of 8, 4, 2 CTAs
+    # that leaves each at least 2 K tiles, with tiles * cluster_k at most half the co-resident
     # CTAs (a whole wave with at least 24 K tiles per CTA)
     for (M, N, K), ks in (((256, 256, 4096), 4), ((128, 128, 4096), 8), ((256, 256, 1024), 4),
                           ((128, 1024, 1024), 2), ((384, 384, 2048), 2), ((512, 512, 4096), 2),
-                          ((256, 256, 512), 1), ((576, 576, 1024), 1)):
+                          ((256, 256, 512), 4), ((128, 128, 512), 4), ((256, 256, 448), 1),
+                          ((512, 512, 512), 1), ((576, 576, 1024), 1)):
         c = gpu_lib.describe(M, N, K)
         tiles = -(-M // 64) * -(-N // 64)
         assert (c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (64, 64, ks, 1), (M, N, K)
