@@ -26,9 +26,9 @@ struct DeviceInfo {
     bool ready = false;
     int status = GEMM_OK;
     int sm_count = 0;
-    int max_clusters[8] = {};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2 consumers,
-                               // [3] narrow single-CTA tiles, [4] tiny tiles, [5] [6] [7] tiny tiles with
-                               // K split across clusters of 2, 4 and 8 CTAs
+    int max_clusters[11] = {};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2 consumers,
+                                // [3] narrow single-CTA tiles, [4] tiny tiles, [5] [6] [7] tiny tiles with
+                                // K split across clusters of 2, 4 and 8 CTAs, [8] [9] [10] narrow tiles so
 };
 
 std::mutex g_mutex;
@@ -113,6 +113,15 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
             if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 64, 8>(&d.max_clusters[7]) != GEMM_OK) {
                 d.max_clusters[7] = 0;
             }
+            if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 128, 2>(&d.max_clusters[8]) != GEMM_OK) {
+                d.max_clusters[8] = 0;
+            }
+            if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 128, 4>(&d.max_clusters[9]) != GEMM_OK) {
+                d.max_clusters[9] = 0;
+            }
+            if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 128, 8>(&d.max_clusters[10]) != GEMM_OK) {
+                d.max_clusters[10] = 0;
+            }
         }
         if (d.status == GEMM_OK && g_encode == nullptr) {
             void *fn = nullptr;
@@ -173,7 +182,8 @@ struct Opts {
     int32_t consumers = 1;
     int32_t block_n = 0;    // tile width 256 or 64; 0: chosen from the shape (resolve_config)
     int32_t block_m = 0;    // rows per CTA 128 or 64 (64 only with block_n 64); 0: chosen likewise
-    int32_t cluster_k = 0;  // tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 chosen likewise
+    int32_t cluster_k = 0;  // narrow / tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 chosen
+                            // likewise
     int32_t max_clusters = 0;
     int32_t raster_group = 0;
     int64_t timeout_ns = kDefaultTimeoutNs;
@@ -209,8 +219,10 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o->consumers == 2 && o->cta_group == 1) return GEMM_ERR_INVALID_ARG;
     if (o->cluster_k > 1) {
-        if (o->block_m == 128) return GEMM_ERR_INVALID_ARG;
-        o->block_m = 64;  // the K split runs on tiny tiles
+        // the K split runs on 64-wide tiles: tiny ones unless 128 rows are asked for
+        if (o->block_n == 256) return GEMM_ERR_INVALID_ARG;
+        o->block_n = 64;
+        if (o->block_m == 0) o->block_m = 64;
     }
     if (o->block_m == 64) {
         if (o->block_n == 256) return GEMM_ERR_INVALID_ARG;
@@ -220,9 +232,10 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     return GEMM_OK;
 }
 
-// The K split of tiny tiles across a cluster (cluster_k).  Each cluster owns
-// one 64 x 64 tile and each of its KS CTAs one K slice, so a CTA streams 1/KS
-// of the tile's operands: small problems with a long K are bound by how fast
+// The K split of narrow (128 x 64) and tiny (64 x 64) tiles across a cluster
+// (cluster_k).  Each cluster owns one tile and each of its KS CTAs one K
+// slice, so a CTA streams 1/KS of the tile's operands: small problems with a
+// long K are bound by how fast
 // one SM's loads arrive, not by the tensor pipe.  The slices' fp32 sums meet
 // in shared memory through the copy engine and are added in the same kernel
 // (no workspace, no second launch), which costs about half a microsecond
@@ -239,34 +252,82 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
 // meets this; a grid capped by max_clusters keeps the persistent tiles.
 // Forced: at most the number of K tiles, and halved until the device can
 // co-schedule clusters of that size.
-int32_t tiny_cluster_k(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o) {
+int32_t cluster_k_slot(int32_t ks, int32_t block_m) {
+    return (ks == 2 ? 5 : (ks == 4 ? 6 : 7)) + (block_m == 64 ? 0 : 3);
+}
+
+int32_t cluster_k_for(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o, int32_t block_m) {
     const int64_t k_tiles = (K + 63) / 64;
-    const int64_t tiles = ((M + 63) / 64) * ((N + 63) / 64);
+    const int64_t tiles = ((M + block_m - 1) / block_m) * ((N + 63) / 64);
+    const int64_t ctas = dev.max_clusters[block_m == 64 ? 4 : 3];  // co-resident single CTAs of these tiles
     int32_t ks = o.cluster_k;
     if (ks == 0) {
         if (o.max_clusters > 0 || k_tiles < 8) return 1;
         const int32_t options[3] = {8, 4, 2};
-        const int slot[3] = {7, 6, 5};
         for (int i = 0; i < 3; ++i) {
             const int64_t per_cta = k_tiles / options[i];
-            if (per_cta < 2 || tiles > dev.max_clusters[slot[i]]) continue;  // all clusters in one wave
-            if (2 * tiles * options[i] <= dev.max_clusters[4] || per_cta >= 24) return options[i];
+            if (per_cta < 2 || tiles > dev.max_clusters[cluster_k_slot(options[i], block_m)]) continue;
+            if (2 * tiles * options[i] <= ctas || per_cta >= 24) return options[i];
         }
         return 1;
     }
     // every CTA needs a K tile, and the device must co-schedule clusters of that size
-    while (ks > 1 && (ks > k_tiles || dev.max_clusters[ks == 2 ? 5 : (ks == 4 ? 6 : 7)] <= 0)) ks /= 2;
+    while (ks > 1 && (ks > k_tiles || dev.max_clusters[cluster_k_slot(ks, block_m)] <= 0)) ks /= 2;
     return ks;
 }
 
-// Whether a problem left to the defaults would take the tiny tiles with a K
-// split (which then wins over split-K through a workspace).
-bool tiny_cluster_k_applies(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o) {
-    if (o.block_m == 128 || o.cluster_k == 1) return false;
+// Rows per tile and K split for a problem on 64-wide tiles (block_n 64).
+// Tiny tiles when they fill at most two thirds of a wave, else narrow ones,
+// each with the split cluster_k_for() gives them.  With a long K the narrow
+// tiles win in two cases (measured on GB300, graph-timed, us): where the tiny
+// tiles get no split but the narrow ones do with at least 24 K tiles per CTA
+// (640x640x4096 10.68 -> 9.33, 768x512x4096 10.68 -> 9.24), and where the
+// tiny tiles split in 2 and the narrow ones can split in 4 with at least 16
+// K tiles per CTA: the same grid with a quarter fewer operand bytes per CTA
+// (512x512x4096 8.09 -> 7.12).  With a shorter K the extra exchange loses
+// (128x1024x1024 3.61 -> 3.96, 512x512x1024 4.21 -> 4.66).  block_m and
+// cluster_k given by the caller are kept.
+void small_tiles(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, Opts *o) {
+    const int32_t forced_k = o->cluster_k;
+    if (o->block_m != 0) {
+        o->cluster_k = cluster_k_for(M, N, K, dev, *o, o->block_m);
+        return;
+    }
     int64_t ctas = dev.max_clusters[4];
-    if (o.max_clusters > 0 && o.max_clusters < ctas) ctas = o.max_clusters;
-    if (o.block_m == 0 && 3 * ((M + 63) / 64) * ((N + 63) / 64) > 2 * ctas) return false;
-    return tiny_cluster_k(M, N, K, dev, o) > 1;
+    if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
+    const bool tiny_fits = 3 * ((M + 63) / 64) * ((N + 63) / 64) <= 2 * ctas;
+    const int32_t ks_narrow = cluster_k_for(M, N, K, dev, *o, 128);
+    if (!tiny_fits) {
+        o->block_m = 128;
+        o->cluster_k = ks_narrow;
+        return;
+    }
+    const int32_t ks_tiny = cluster_k_for(M, N, K, dev, *o, 64);
+    const int64_t k_tiles = (K + 63) / 64;
+    o->block_m = 64;
+    o->cluster_k = ks_tiny;
+    if (forced_k != 0) return;  // cluster_k given (1: no split): keep the tiny tiles
+    if (ks_tiny == 1 && ks_narrow > 1 && k_tiles / ks_narrow >= 24) {
+        o->block_m = 128;
+        o->cluster_k = ks_narrow;
+    } else if (ks_tiny == 2 && o->max_clusters == 0 && k_tiles / 4 >= 16) {
+        const int64_t tiles_narrow = ((M + 127) / 128) * ((N + 63) / 64);
+        if (tiles_narrow <= dev.max_clusters[cluster_k_slot(4, 128)] && 4 * tiles_narrow <= dev.max_clusters[3]) {
+            o->block_m = 128;
+            o->cluster_k = 4;
+        }
+    }
+}
+
+// Whether a problem whose 128 x 64 tiles fit one wave would take its narrow
+// or tiny tiles with a K split (which then wins over split-K through a
+// workspace: 768x768x4096 10.07 vs 12.84, 512x512x4096 7.12 vs 9.30,
+// 256x256x4096 4.81 vs 8.69 us).
+bool cluster_k_applies(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, const Opts &o) {
+    if (o.cluster_k == 1) return false;
+    Opts t = o;
+    small_tiles(M, N, K, dev, &t);
+    return t.cluster_k > 1;
 }
 
 // The default CTA group and tile width.
@@ -303,7 +364,7 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
             int64_t ctas = dev.max_clusters[3];
             if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
             narrow = ((M + 127) / 128) * ((N + 63) / 64) <= ctas;
-            if (narrow && allow_splitk && !tiny_cluster_k_applies(M, N, K, dev, *o)) {
+            if (narrow && allow_splitk && !cluster_k_applies(M, N, K, dev, *o)) {
                 int64_t pairs = dev.max_clusters[1];
                 if (o->max_clusters > 0 && o->max_clusters < pairs) pairs = o->max_clusters;
                 const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
@@ -318,12 +379,7 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
     }
     if (o->block_n == 64) {
         o->cta_group = 1;
-        if (o->block_m == 0) {
-            int64_t ctas = dev.max_clusters[4];
-            if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
-            o->block_m = 3 * ((M + 63) / 64) * ((N + 63) / 64) <= 2 * ctas ? 64 : 128;
-        }
-        o->cluster_k = o->block_m == 64 ? tiny_cluster_k(M, N, K, dev, *o) : 1;
+        small_tiles(M, N, K, dev, o);
         return;
     }
     o->cluster_k = 1;
@@ -515,7 +571,14 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
             default: return launch<1, 1, 64, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
         }
     }
-    if (o.block_n == 64) return launch<1, 1, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+    if (o.block_n == 64) {
+        switch (o.cluster_k) {
+            case 2: return launch<1, 1, 64, 128, 2>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+            case 4: return launch<1, 1, 64, 128, 4>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+            case 8: return launch<1, 1, 64, 128, 8>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+            default: return launch<1, 1, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
+        }
+    }
     if (o.cta_group == 2 && o.consumers == 2) return launch<2, 2, 256>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.cta_group == 2) return launch<2, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
     return launch<1, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
@@ -608,6 +671,15 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
     } else if (o.block_n == 64 && o.block_m == 64) {
         st = make_plan<1, 1, 64, 64>(M, N, K, *info, o, false, &plan);
         stages = Cfg<1, 1, 64, 64>::STAGES;
+    } else if (o.block_n == 64 && o.cluster_k == 2) {
+        st = make_plan<1, 1, 64, 128, 2>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 128, 2>::STAGES;
+    } else if (o.block_n == 64 && o.cluster_k == 4) {
+        st = make_plan<1, 1, 64, 128, 4>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 128, 4>::STAGES;
+    } else if (o.block_n == 64 && o.cluster_k == 8) {
+        st = make_plan<1, 1, 64, 128, 8>(M, N, K, *info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 128, 8>::STAGES;
     } else if (o.block_n == 64) {
         st = make_plan<1, 1, 64>(M, N, K, *info, o, false, &plan);
         stages = Cfg<1, 1, 64>::STAGES;
@@ -694,7 +766,7 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
         (block_n == 64 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
         (block_m == 64 && block_n != 64) || raster_group < 0 ||
         (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8) ||
-        (split_k > 1 && block_m != 64) || K < 0 ||
+        (split_k > 1 && block_n != 64) || K < 0 ||
         K > kDimLimit || M <= 0 || N <= 0 || M > kDimLimit || N > kDimLimit || num_clusters <= 0 ||
         num_clusters > kDimLimit || cluster_id < 0 || cluster_id >= num_clusters || iter < 0 || !out) {
         return GEMM_ERR_INVALID_ARG;
@@ -708,7 +780,7 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
     const bool narrow = block_n == 64;
     int32_t slices = 1;
     if (split_k > 1) {
-        // tiny tiles with K split across clusters of split_k CTAs (cluster_k)
+        // narrow or tiny tiles with K split across clusters of split_k CTAs (cluster_k)
         slices = split_k;
         while (slices > 1 && slices > k_tiles) slices /= 2;
     } else if (split_k && consumers == 1 && !narrow) {

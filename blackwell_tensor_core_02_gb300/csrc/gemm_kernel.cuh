@@ -101,8 +101,8 @@ enum : uint32_t {
 // BN is the tile width: 256, or 64 for the narrow single-CTA tiles of small
 // problems (more CTAs, and a ring deep enough to hold a K of 512 at once).
 // BM is the rows of D per CTA and consumer: 128, or 64 for the tiny tiles
-// (64 x 64) of the smallest problems.  KS > 1 (tiny tiles only) splits K
-// across a cluster of KS CTAs that add their partial sums through
+// (64 x 64) of the smallest problems.  KS > 1 (narrow and tiny tiles) splits
+// K across a cluster of KS CTAs that add their partial sums through
 // distributed shared memory.
 template <int CG, int NC, int BN = 256, int BM = 128, int KS = 1>
 struct Cfg {
@@ -110,14 +110,14 @@ struct Cfg {
     static_assert(NC == 1 || (NC == 2 && CG == 2), "two consumers need a CTA pair");
     static_assert(BN == 256 || (BN == 64 && CG == 1 && NC == 1), "narrow tiles are single-CTA, one consumer");
     static_assert(BM == 128 || (BM == 64 && BN == 64), "64-row tiles are narrow");
-    static_assert(KS == 1 || ((KS == 2 || KS == 4 || KS == 8) && BM == 64), "a K split over 2, 4 or 8 tiny CTAs");
+    static_assert(KS == 1 || ((KS == 2 || KS == 4 || KS == 8) && BN == 64), "a K split over 2, 4 or 8 narrow or tiny CTAs");
     static constexpr bool NARROW = BN != 256;
     static constexpr bool TINY = BM == 64;
     static constexpr bool KSPLIT = KS > 1;
     static constexpr int CLUSTER = CG * KS;             // CTAs per cluster
     // co-resident cluster count slot of this configuration in the host's
     // per-device table
-    static constexpr int KIND = KSPLIT ? (KS == 2 ? 5 : (KS == 4 ? 6 : 7))
+    static constexpr int KIND = KSPLIT ? (KS == 2 ? 5 : (KS == 4 ? 6 : 7)) + (TINY ? 0 : 3)
                                        : (TINY ? 4 : (NARROW ? 3 : (CG == 1 ? 0 : NC)));
     static constexpr int BLOCK_M = BM;                  // rows of D per CTA and consumer
     static constexpr int BLOCK_N = BN;                  // columns of D per tile (MMA N)
@@ -129,7 +129,8 @@ struct Cfg {
     static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
     static constexpr int A_STAGE = A_BLOCK * NC;
     static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
-    static constexpr int STAGES = TINY ? 12 : (NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)));
+    // (narrow tiles with a K split give two stages to the exchange buffers)
+    static constexpr int STAGES = TINY ? 12 : (NARROW ? (KSPLIT ? 6 : 8) : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)));
     static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
     static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
@@ -156,7 +157,11 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_D = OFF_B + STAGES * B_STAGE;
     // K split: the CTA's own fp32 sums, all BLOCK_M rows, staged for the copies to their owners
-    static constexpr int OFF_SRC = OFF_D + EPI_WARPS * EPI_BUFS * EPI_BUF;
+    // With a K split the epilogue region at OFF_D receives the cluster's fp32
+    // partial sums of this CTA's rows (KS slices x BLOCK_M / KS rows x BLOCK_N),
+    // in place of the staging buffers, and OFF_SRC holds the CTA's own sums.
+    static constexpr int EPI_REGION = KSPLIT ? BLOCK_M * BLOCK_N * 4 : EPI_WARPS * EPI_BUFS * EPI_BUF;
+    static constexpr int OFF_SRC = OFF_D + EPI_REGION;
     static constexpr int OFF_BAR = OFF_SRC + (KSPLIT ? BLOCK_M * BLOCK_N * 4 : 0);
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (KSPLIT ? 1 : 0);  // + drain (+ recv)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;         // tmem base, abort flag
@@ -168,8 +173,7 @@ struct Cfg {
     // sums of this CTA's rows: KS slices x (BLOCK_M / KS) rows x BLOCK_N fp32
     static constexpr int KS_ROWS = BLOCK_M / KS;        // rows of the tile this CTA adds up and stores
     static constexpr uint32_t KS_RECV_BYTES = BLOCK_M * BLOCK_N * 4;  // all slices of those rows
-    static_assert(!KSPLIT || (EPI_COALESCED && BLOCK_M * BLOCK_N * 4 <= EPI_WARPS * EPI_BUFS * EPI_BUF &&
-                              KS_ROWS % 8 == 0),
+    static_assert(!KSPLIT || (EPI_COALESCED && KS_ROWS % 8 == 0),
                   "the cluster's partial sums of a CTA's rows fit its staging buffers");
 };
 
@@ -631,7 +635,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     // 16-byte unit u at u ^ (R % 8): no bank conflicts); then
                     // one lane copies the warp's rows, by the copy engine, to
                     // slots krank * KS_ROWS + R % KS_ROWS of each owner's
-                    // staging buffers (the same swizzle, as KS_ROWS is a
+                    // receive region (the same swizzle, as KS_ROWS is a
                     // multiple of 8), counted in bytes on its receive barrier.
                     const uint32_t src = base + C::OFF_SRC;
                     if (lane < C::WARP_ROWS) {

@@ -109,9 +109,11 @@ typedef enum gemm_status {
  *                 most two thirds of the co-resident CTAs, else 128.  Other
  *                 values:
  *                 GEMM_ERR_INVALID_ARG.
- *   cluster_k     2, 4 or 8 (needs block_m 0 or 64, which then means 64):
- *                 tiny tiles with K split across a thread-block cluster of
- *                 that many CTAs, one cluster per 64 x 64 tile and one K
+ *   cluster_k     2, 4 or 8 (needs block_n 0 or 64, which then means 64, and
+ *                 one single-CTA consumer; block_m 0 then means 64): tiny
+ *                 (block_m 64) or narrow (block_m 128) tiles with K split
+ *                 across a thread-block cluster of that many CTAs, one
+ *                 cluster per tile and one K
  *                 slice per CTA (at most one per 64-wide K tile, so fewer
  *                 CTAs when K is short, and halved until the device can run
  *                 clusters of that size); each CTA keeps its slice's fp32 sums
@@ -120,8 +122,8 @@ typedef enum gemm_status {
  *                 to fp16.  No workspace and no second kernel.  Each CTA then
  *                 streams 1/cluster_k of the tile's operands, which is what
  *                 bounds small problems.  Not on the pages.  1: no K split.
- *                 0 (default): with the tiny tiles, max_clusters 0 and at
- *                 least 8 K tiles of 64, the largest of 8, 4, 2 that leaves
+ *                 0 (default): with the narrow or tiny tiles, max_clusters 0
+ *                 and at least 8 K tiles of 64, the largest of 8, 4, 2 that leaves
  *                 each CTA at least 2 K tiles, lets all the clusters run at
  *                 once and keeps the grid within half the co-resident CTAs
  *                 (within all of them from 24 K tiles per CTA), else 1.
@@ -175,7 +177,11 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
  * at least 32 K tiles of 64; the pages' persistent scheduler, TIRx notes V6,
  * would otherwise leave most SMs idle for the whole K-loop).  With the default
  * options a problem whose narrow 128 x 64 tiles fit one wave (see block_n)
- * takes those instead, unless the split would cut K into at least 8 slices.
+ * takes those instead, unless the split would cut K into at least 8 slices;
+ * and a problem whose narrow or tiny tiles split K across a cluster
+ * (cluster_k) takes that, which needs no workspace and is faster, so with
+ * the defaults this workspace serves mostly grids capped by max_clusters and
+ * calls that ask for 256-wide tiles.
  * K is then cut into S slices (4..16); each slice's fp32 partial sums go to the workspace
  * as [S][M][N] fp32 and a second kernel on `stream` adds them in fp32 and
  * rounds once to fp16.  `workspace` is a device pointer, 16-byte aligned,
@@ -305,7 +311,7 @@ typedef struct gemm_f16_work_item {
  * split_k = 1 (what gemm_f16_nt_ws() does given enough workspace) and few
  * tiles, K is instead cut into slices: item t*S + s is slice s of tile t.
  * Narrow and tiny tiles are never split along N, nor along K this way.
- * split_k 2, 4 or 8 (tiny tiles only) is the K split across a cluster
+ * split_k 2, 4 or 8 (narrow or tiny tiles) is the K split across a cluster
  * (cluster_k of gemm_f16_options): S = split_k, reduced to at most the
  * number of 64-wide K tiles, with the same item numbering; that kernel runs
  * one item per CTA, so pass num_clusters = T * S and iter 0 (CTA i of the

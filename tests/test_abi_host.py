@@ -127,7 +127,7 @@ def test_argument_errors_are_returned_before_any_launch():
                 g.Options(block_m=32), g.Options(block_m=256), g.Options(block_m=64, block_n=256),
                 g.Options(block_m=64, cta_group=2), g.Options(block_m=64, consumers=2),
                 g.Options(cluster_k=3), g.Options(cluster_k=16), g.Options(cluster_k=-1),
-                g.Options(cluster_k=2, block_m=128), g.Options(cluster_k=4, block_n=256),
+                g.Options(cluster_k=4, block_n=256),
                 g.Options(cluster_k=8, cta_group=2), g.Options(cluster_k=2, consumers=2)):
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
@@ -343,11 +343,12 @@ def test_tiny_schedule_covers_every_output_once(M, N, K, clusters):
     (256, 256, 512, 4), (256, 256, 512, 8), (128, 128, 128, 2), (200, 72, 4096, 8), (64, 64, 64, 8),
     (64, 64, 192, 8), (1000, 520, 520, 4), (1, 8, 8, 2),
 ])
-def test_cluster_k_schedule_covers_every_k_tile_once(M, N, K, ks):
-    """Tiny tiles with K split across clusters (split_k 2, 4, 8 = cluster_k): CTA i of a grid of
-    T * S CTAs runs item i, the S consecutive CTAs of tile t take its K slices 0..S-1 in order, and
-    S is at most the number of K tiles (halved until it is)."""
-    num_m, num_n = -(-M // 64), -(-N // 64)
+@pytest.mark.parametrize("bm", [64, 128])
+def test_cluster_k_schedule_covers_every_k_tile_once(M, N, K, ks, bm):
+    """Tiny or narrow tiles with K split across clusters (split_k 2, 4, 8 = cluster_k): CTA i of a
+    grid of T * S CTAs runs item i, the S consecutive CTAs of tile t take its K slices 0..S-1 in
+    order, and S is at most the number of K tiles (halved until it is)."""
+    num_m, num_n = -(-M // bm), -(-N // 64)
     k_tiles = -(-K // 64)
     S = ks
     while S > 1 and S > k_tiles:
@@ -356,9 +357,9 @@ def test_cluster_k_schedule_covers_every_k_tile_once(M, N, K, ks):
     grid = tiles * S
     seen = {}
     for i in range(grid):
-        w = g.schedule(M, N, 1, 0, grid, i, 0, K=K, block_n=64, block_m=64, split_k=ks)
+        w = g.schedule(M, N, 1, 0, grid, i, 0, K=K, block_n=64, block_m=bm, split_k=ks)
         assert w is not None
-        assert g.schedule(M, N, 1, 0, grid, i, 1, K=K, block_n=64, block_m=64, split_k=ks) is None
+        assert g.schedule(M, N, 1, 0, grid, i, 1, K=K, block_n=64, block_m=bm, split_k=ks) is None
         m_idx, n_idx, n_off, n_len, sl, kb, ke = w
         assert (n_off, n_len, sl) == (0, 64, i % S)
         assert (kb, ke) == (sl * k_tiles // S, (sl + 1) * k_tiles // S) and kb < ke
@@ -369,7 +370,7 @@ def test_cluster_k_schedule_covers_every_k_tile_once(M, N, K, ks):
         assert idx == list(range(idx[0], idx[0] + S)) and idx[0] % S == 0  # one cluster per tile
         assert parts[0][1] == 0 and parts[-1][2] == k_tiles
         assert all(parts[j][2] == parts[j + 1][1] for j in range(S - 1))  # contiguous, in slice order
-    for bad in (dict(split_k=3), dict(split_k=16), dict(split_k=2, block_m=128)):
+    for bad in (dict(split_k=3), dict(split_k=16), dict(split_k=2, block_n=256, block_m=128)):
         with pytest.raises(g.GemmError):
             g.schedule(M, N, 1, 0, grid, 0, 0, K=K, **{"block_n": 64, "block_m": 64, **bad})
 

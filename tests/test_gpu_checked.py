@@ -29,6 +29,7 @@ CASES = [
     (256, 256, 512, 0, 0, 0, 0, False),      # default: tiny tiles, K split across clusters
     (200, 136, 520, 1, 1, 64, 0, False, 64, 8),   # K split over 8 CTAs, ragged M, N and K
     (520, 264, 1000, 1, 1, 64, 0, False, 64, 2),  # K split over 2 CTAs, K beyond the ring
+    (300, 200, 1000, 1, 1, 64, 0, False, 128, 4),  # narrow tiles, K split over 4 CTAs, ragged
     (700, 600, 1000, 1, 1, 64, 5, False, 64),  # tiny tiles, many per CTA, K beyond the ring
     (1000, 520, 1000, 2, 1, 256, 3, False),  # pairs, many tiles per cluster, ragged
     (1000, 520, 1000, 1, 1, 256, 5, False),  # single CTAs

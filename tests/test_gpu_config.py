@@ -38,21 +38,25 @@ def test_smallest_problems_take_tiny_tiles(gpu_lib):
 
 
 def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
-    # from 8 K tiles of 64 on, tiny tiles split K across a cluster: the largest of 8, 4, 2 CTAs
+    # from 8 K tiles of 64 on, 64-wide tiles split K across a cluster: the largest of 8, 4, 2 CTAs
     # that leaves each at least 2 K tiles, with tiles * cluster_k at most half the co-resident
-    # CTAs (a whole wave with at least 24 K tiles per CTA)
-    for (M, N, K), ks in (((256, 256, 4096), 4), ((128, 128, 4096), 8), ((256, 256, 1024), 4),
-                          ((128, 1024, 1024), 2), ((384, 384, 2048), 2), ((512, 512, 4096), 2),
-                          ((256, 256, 512), 4), ((128, 128, 512), 4), ((256, 256, 448), 1),
-                          ((512, 512, 512), 1), ((576, 576, 1024), 1)):
+    # CTAs (a whole wave with at least 24 K tiles per CTA); narrow tiles instead of tiny ones
+    # where the tiny ones get no split but the narrow ones do with at least 24 K tiles per CTA,
+    # or where the tiny ones split in 2 and the narrow ones can split in 4 with at least 16
+    for (M, N, K), bm, ks in (((256, 256, 4096), 64, 4), ((128, 128, 4096), 64, 8), ((256, 256, 1024), 64, 4),
+                              ((128, 1024, 1024), 64, 2), ((384, 384, 2048), 64, 2), ((512, 512, 4096), 128, 4),
+                              ((256, 256, 512), 64, 4), ((128, 128, 512), 64, 4), ((256, 256, 448), 64, 1),
+                              ((512, 512, 512), 64, 1), ((512, 512, 1024), 64, 1), ((576, 576, 1024), 64, 1),
+                              ((640, 640, 4096), 128, 2), ((768, 512, 4096), 128, 2), ((512, 1024, 4096), 128, 2),
+                              ((768, 768, 4096), 128, 2), ((768, 768, 2048), 128, 1)):
         c = gpu_lib.describe(M, N, K)
-        tiles = -(-M // 64) * -(-N // 64)
-        assert (c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (64, 64, ks, 1), (M, N, K)
+        tiles = -(-M // bm) * -(-N // 64)
+        assert (c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (64, bm, ks, 1), (M, N, K)
         assert (c["clusters"], c["work_items"], c["workspace_bytes"]) == (tiles, tiles * ks, 0), (M, N, K)
         # it needs no workspace, and wins over split-K through one
         w = gpu_lib.describe(M, N, K, with_workspace=True)
         if ks > 1:
-            assert (w["block_m"], w["cluster_k"], w["workspace_bytes"]) == (64, ks, 0), (M, N, K)
+            assert (w["block_m"], w["cluster_k"], w["workspace_bytes"]) == (bm, ks, 0), (M, N, K)
             assert gpu_lib.workspace_size(M, N, K) == 0
     # forced: at most one CTA per K tile; off; and not with a capped persistent grid
     assert gpu_lib.describe(256, 256, 512, gpu_lib.Options(cluster_k=8))["cluster_k"] == 8
@@ -62,6 +66,9 @@ def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
     assert gpu_lib.describe(256, 256, 4096, gpu_lib.Options(max_clusters=5))["cluster_k"] == 1
     forced = gpu_lib.describe(1000, 520, 1000, gpu_lib.Options(cluster_k=4))  # more clusters than fit at once
     assert (forced["block_m"], forced["cluster_k"], forced["clusters"]) == (64, 4, 16 * 9)
+    narrow = gpu_lib.describe(1000, 520, 1000, gpu_lib.Options(cluster_k=4, block_m=128))
+    assert (narrow["block_n"], narrow["block_m"], narrow["cluster_k"], narrow["clusters"], narrow["stages"]) == \
+        (64, 128, 4, 8 * 9, 6)
 
 
 def test_small_problems_take_narrow_tiles(gpu_lib):
@@ -87,10 +94,15 @@ def test_more_than_one_wave_keeps_256_wide_tiles(gpu_lib):
 
 
 def test_split_k_wins_only_with_at_least_8_slices(gpu_lib):
-    # 9 pair tiles, 64 K tiles; 120 tiny tiles are too many for the tiny tiles
-    deep = gpu_lib.describe(768, 640, 4096, with_workspace=True)
+    # Where a K split across clusters applies it wins (checked above); with the grid capped
+    # (max_clusters, which also turns the cluster split off) the choice is between narrow
+    # tiles and split-K through a workspace: 9 pair tiles with 64 K tiles split 8 ways.
+    pairs = gpu_lib.describe(4096, 4096, 4096)["clusters"]
+    capped = gpu_lib.Options(max_clusters=pairs)
+    deep = gpu_lib.describe(768, 640, 4096, capped, with_workspace=True)
     assert (deep["cta_group"], deep["block_n"], deep["split_k"], deep["cluster_k"]) == (2, 256, 8, 1)
-    assert deep["workspace_bytes"] == 8 * 768 * 640 * 4 == gpu_lib.workspace_size(768, 640, 4096)
+    assert deep["workspace_bytes"] == 8 * 768 * 640 * 4 == gpu_lib.workspace_size(768, 640, 4096, capped)
+    assert gpu_lib.workspace_size(768, 640, 4096) == 0  # by default the narrow tiles split K in clusters
     shallow = gpu_lib.describe(1024, 1024, 4096, with_workspace=True)  # 4 slices: narrow tiles instead
     assert shallow["block_n"] == 64 and shallow["split_k"] == 1 and gpu_lib.workspace_size(1024, 1024, 4096) == 0
     tiny = gpu_lib.describe(256, 256, 1024, with_workspace=True)  # split-K would give 2 slices: tiny tiles

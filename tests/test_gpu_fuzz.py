@@ -2,8 +2,8 @@
 
 Each case draws M (any), N and K (multiples of 8, the supported set), a kernel
 variant (default, CTA pair, single CTA, two consumers; further series the
-narrow 128 x 64 and the tiny 64 x 64 tiles, and the tiny tiles with K split
-across clusters of 2, 4 or 8 CTAs), a cap on the number of
+narrow 128 x 64 and the tiny 64 x 64 tiles, and narrow or tiny tiles with K
+split across clusters of 2, 4 or 8 CTAs), a cap on the number of
 persistent clusters (so that tail splits and multi-tile CTAs occur at small
 sizes) and an entry point (no workspace, caller workspace, the library's fixed
 scratch).  Every element must meet |gpu - oracle| <= 2^-9 |oracle| + 1e-3.
@@ -52,7 +52,7 @@ def _cases(n=36, seed=2026, per_series=12):
             K = int(rng.integers(1, 130)) * 8
             clusters = int(rng.choice([0, 0, 1, 3, 7]))
             entry = ["nt", "ws", "static"][int(rng.integers(0, 3))]
-            v = variant if variant is not None else (1, 1, 64, 64, int(rng.choice([2, 4, 8])))
+            v = variant if variant is not None else (1, 1, 64, int(rng.choice([64, 128])), int(rng.choice([2, 4, 8])))
             out.append((i, M, N, K, v, clusters, entry))
     return out
 

@@ -50,13 +50,14 @@ def assert_close(gpu_f16, ref_bits, what=""):
 
 # (cta_group, consumers, block_n[, block_m[, cluster_k]]): the CTA pair with
 # one MMA consumer (the default), a single CTA, the pair with two consumers
-# sharing each B stage, the narrow 128 x 64 single-CTA tiles of small problems,
-# the tiny 64 x 64 tiles (MMAs of M = 64) of the smallest, without a K split
-# and with K split across clusters of 2, 4 and 8 CTAs (fewer where K has fewer
-# 64-wide tiles).
-VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64, 128), (1, 1, 64, 64, 1), (1, 1, 64, 64, 2),
-            (1, 1, 64, 64, 4), (1, 1, 64, 64, 8)]
-VIDS = ["pair", "single", "pair-2consumers", "narrow", "tiny", "tiny-k2", "tiny-k4", "tiny-k8"]
+# sharing each B stage, the narrow 128 x 64 single-CTA tiles of small problems
+# and the tiny 64 x 64 tiles (MMAs of M = 64) of the smallest, each without a K
+# split and with K split across clusters of 2, 4 and 8 CTAs (fewer where K has
+# fewer 64-wide tiles).
+VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64, 128, 1), (1, 1, 64, 128, 2), (1, 1, 64, 128, 4),
+            (1, 1, 64, 128, 8), (1, 1, 64, 64, 1), (1, 1, 64, 64, 2), (1, 1, 64, 64, 4), (1, 1, 64, 64, 8)]
+VIDS = ["pair", "single", "pair-2consumers", "narrow", "narrow-k2", "narrow-k4", "narrow-k8", "tiny", "tiny-k2",
+        "tiny-k4", "tiny-k8"]
 
 
 def opts(g, variant=(0, 0), max_clusters=0):
@@ -225,16 +226,18 @@ def test_split_k_full(gpu_lib, M, N, K, cg):
 def test_binding_workspace_on_a_side_stream(gpu_lib):
     # The binding's cached split-K workspace belongs to the stream the call runs on; a larger
     # problem on the same stream replaces it while the first GEMM may still be queued.
+    # (CTA pairs forced: by default these shapes split K across clusters, without a workspace)
     side = torch.cuda.Stream()
+    pairs = gpu_lib.Options(cta_group=2)
     shapes = [(768, 640, 4096), (768, 768, 4096)]  # 15 MiB, then 18 MiB of partials
     outs = []
     for i, (M, N, K) in enumerate(shapes):
-        assert gpu_lib.workspace_size(M, N, K) > 0
+        assert gpu_lib.workspace_size(M, N, K, pairs) > 0
         A, B = si.custom(M, N, K, seed=700 + i).operands()
         dA, dB = to_dev(A), to_dev(B)
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            D = gpu_lib.gemm_f16_nt(dA, dB, stream=side)
+            D = gpu_lib.gemm_f16_nt(dA, dB, stream=side, options=pairs)
         outs.append((A, B, D))
     side.synchronize()
     assert gpu_lib.last_device_status(side.cuda_stream)[0] == 0

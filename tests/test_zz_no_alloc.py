@@ -34,20 +34,26 @@ def _dev(x):
     return torch.from_numpy(np.ascontiguousarray(x)).cuda()
 
 
-def _static_call(lib, A, B, D, M, N, K):
+def _pairs(gpu_lib):
+    # CTA pairs: their split-K uses scratch (by default these long-K shapes would instead split
+    # K across thread-block clusters, which needs none)
+    return ctypes.byref(gpu_lib.Options(cta_group=2))
+
+
+def _static_call(lib, A, B, D, M, N, K, opts=None):
     stream = torch.cuda.current_stream().cuda_stream
     return lib.gemm_f16_nt_static_ws(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
-                                     ctypes.c_void_p(D.data_ptr()), M, N, K, ctypes.c_void_p(stream), None)
+                                     ctypes.c_void_p(D.data_ptr()), M, N, K, ctypes.c_void_p(stream), opts)
 
 
-def _workspace_call(lib, A, B, D, M, N, K):
-    need = lib.gemm_f16_nt_workspace_size(M, N, K, None)
+def _workspace_call(lib, A, B, D, M, N, K, opts=None):
+    need = lib.gemm_f16_nt_workspace_size(M, N, K, opts)
     assert need >= 0
     ws = torch.empty(max(need, 16), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream().cuda_stream
     rc = lib.gemm_f16_nt_ws(ctypes.c_void_p(A.data_ptr()), ctypes.c_void_p(B.data_ptr()),
                             ctypes.c_void_p(D.data_ptr()), M, N, K, ctypes.c_void_p(ws.data_ptr()), need,
-                            ctypes.c_void_p(stream), None)
+                            ctypes.c_void_p(stream), opts)
     torch.cuda.synchronize()
     return rc
 
@@ -63,20 +69,20 @@ def test_static_scratch_matches_the_workspace_entry_point(gpu_lib):
     shapes = [(768, 640, 4096), (512, 1024, 4096)]  # both split K (15 MiB and 16 MiB of scratch)
     probs = []
     for i, (M, N, K) in enumerate(shapes):
-        assert 0 < lib.gemm_f16_nt_workspace_size(M, N, K, None) <= STATIC_BYTES
+        assert 0 < lib.gemm_f16_nt_workspace_size(M, N, K, _pairs(gpu_lib)) <= STATIC_BYTES
         A, B = si.custom(M, N, K, seed=90 + i).operands()
         probs.append((M, N, K, _dev(A), _dev(B)))
     # two calls in a row through the fixed scratch, the second on top of the first's leftovers
     outs = []
     for M, N, K, A, B in probs:
         D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
-        assert _static_call(lib, A, B, D, M, N, K) == 0
+        assert _static_call(lib, A, B, D, M, N, K, _pairs(gpu_lib)) == 0
         outs.append(D)
     torch.cuda.synchronize()
     assert gpu_lib.last_device_status()[0] == 0
     for (M, N, K, A, B), D in zip(probs, outs):
         ref = torch.empty((M, N), dtype=torch.float16, device="cuda")
-        assert _workspace_call(lib, A, B, ref, M, N, K) == 0
+        assert _workspace_call(lib, A, B, ref, M, N, K, _pairs(gpu_lib)) == 0
         assert _close(D, ref), f"{M}x{N}x{K}"
 
 
@@ -96,12 +102,12 @@ def test_static_scratch_without_split_k(gpu_lib):
 def test_static_scratch_refuses_what_does_not_fit(gpu_lib):
     lib = gpu_lib.load()
     M, N, K = 768, 768, 4096  # 9 pair tiles, 8 K slices: 8 x 768 x 768 x 4 B = 18 MiB of scratch
-    need = lib.gemm_f16_nt_workspace_size(M, N, K, None)
+    need = lib.gemm_f16_nt_workspace_size(M, N, K, _pairs(gpu_lib))
     if need <= STATIC_BYTES:
         pytest.skip(f"on this device the shape needs only {need} bytes")
     A, B = si.custom(M, N, K, seed=96).operands()
     D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
-    assert _static_call(lib, _dev(A), _dev(B), D, M, N, K) == SCRATCH_LIMIT
+    assert _static_call(lib, _dev(A), _dev(B), D, M, N, K, _pairs(gpu_lib)) == SCRATCH_LIMIT
     torch.cuda.synchronize()
     assert torch.isnan(D).all()  # nothing ran
     assert "16 MiB" in gpu_lib.status_string(SCRATCH_LIMIT)
