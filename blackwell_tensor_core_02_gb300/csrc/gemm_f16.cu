@@ -235,12 +235,11 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
 // The K split of narrow (128 x 64) and tiny (64 x 64) tiles across a cluster
 // (cluster_k).  Each cluster owns one tile and each of its KS CTAs one K
 // slice, so a CTA streams 1/KS of the tile's operands: small problems with a
-// long K are bound by how fast
-// one SM's loads arrive, not by the tensor pipe.  The slices' fp32 sums meet
-// in shared memory through the copy engine and are added in the same kernel
-// (no workspace, no second launch), which costs about half a microsecond
-// more than the tiles alone.  Measured on GB300 (graph-timed, us, KS = 1 / 2
-// / 4 / 8): 256x256x128 2.15 / 2.70, 256x256x512 2.86 / 3.00 / 2.79 / 6.11
+// long K are bound by how fast one SM's loads arrive, not by the tensor pipe.
+// The slices' fp32 sums meet in shared memory through the copy engine and are
+// added in the same kernel (no workspace, no second launch), which costs
+// about half a microsecond more than the tiles alone.  Measured on GB300 with
+// tiny tiles (graph-timed, us, KS = 1 / 2 / 4 / 8): 256x256x128 2.15 / 2.70, 256x256x512 2.86 / 3.00 / 2.79 / 6.11
 // (16 clusters of 8 do not all fit at once: two waves), 256x256x1024 4.12 /
 // 3.55 / 3.07, 256x256x4096 10.10 / 6.81 / 4.81 / 8.15, 128x128x4096 10.13 /
 // 6.64 / 4.65 / 3.49, 128x1024x1024 4.25 / 3.61 / 3.91, 384x384x2048 6.21 /
