@@ -340,10 +340,16 @@ def test_dependent_chain_with_overlap_matches_plain_launches(gpu_lib):
 
 def test_concurrent_host_threads(gpu_lib):
     # Four host threads, each on its own stream, call the library at once
-    # (device set-up is guarded; tensor maps are built per call).
+    # (device set-up is guarded; tensor maps are built per call).  Two of them
+    # run K split across thread-block clusters (tiny tiles over 4 CTAs, narrow
+    # tiles over 2), whose clusters then share the GPU with the others' grids.
     import threading
 
-    probs = [si.custom(256 + 64 * t, 520, 200 + 8 * t, seed=60 + t).operands() for t in range(4)]
+    shapes = [(256, 520, 200), (320, 520, 208), (384, 264, 1024), (448, 264, 1088)]
+    options = [None, None, gpu_lib.Options(cluster_k=4), gpu_lib.Options(block_m=128, cluster_k=2)]
+    assert gpu_lib.describe(*shapes[2], options[2])["cluster_k"] == 4
+    assert gpu_lib.describe(*shapes[3], options[3])["cluster_k"] == 2
+    probs = [si.custom(M, N, K, seed=60 + t).operands() for t, (M, N, K) in enumerate(shapes)]
     outs = [None] * 4
     errors = []
 
@@ -354,7 +360,7 @@ def test_concurrent_host_threads(gpu_lib):
             with torch.cuda.stream(s):
                 dA, dB = to_dev(A), to_dev(B)
                 for _ in range(10):
-                    D = gpu_lib.gemm_f16_nt(dA, dB, stream=s)
+                    D = gpu_lib.gemm_f16_nt(dA, dB, stream=s, options=options[t])
             s.synchronize()
             outs[t] = D.cpu().numpy()
         except Exception as e:  # reported below
