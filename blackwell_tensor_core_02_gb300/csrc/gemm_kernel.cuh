@@ -48,13 +48,19 @@
 // Narrow tiles (BN = 64, CG = 1, NC = 1): for problems whose 128 x 64 tiles fit
 // one wave of CTAs.  Same roles; an 8-stage ring of 24 KiB stages holds a K of
 // 512 at once, TMEM is 128 columns (two 64-column accumulators), and the
-// epilogue writes D from registers.  Not on the pages, which fix the tile.
+// epilogue stages each warp's rows in shared memory and writes D with
+// coalesced warp stores.  Not on the pages, which fix the tile.
 //
 // Tiny tiles (BM = 64, BN = 64): for problems whose 64 x 64 tiles fill at most
 // two thirds of a wave, the same again with MMAs of M = 64 and a 12-stage ring of
 // 16 KiB stages.  An M = 64 accumulator takes lanes 0-15 of each 32-lane
 // quarter of TMEM (row r in lane 32 * (r / 16) + r % 16), so each epilogue
 // warp reads its quarter as usual and stores 16 rows from its lanes 0-15.
+//
+// K split across a cluster (KS = 2, 4, 8; narrow and tiny tiles): KS CTAs own
+// one tile, CTA s runs K slice s, and the copy engine moves each CTA's fp32
+// sums to the CTA that owns those rows, which adds the KS slices in order,
+// rounds once and stores D (see the end of the kernel).
 //
 // Split-K (NC = 1): with very few tiles, item t*S + s runs K slice s of tile
 // t and its epilogue writes the fp32 partial sum of that slice to a workspace

@@ -94,8 +94,8 @@ typedef enum gemm_status {
  *   block_n       tile width in columns of D.  256: the tiles above.  64
  *                 (needs cta_group 0 or 1 and one consumer): single CTAs
  *                 with 128 x 64 tiles and an 8-stage ring (all of a K up to
- *                 512 in flight after one load latency), D stored straight
- *                 from registers; for small, latency-bound problems.  Not on
+ *                 512 in flight after one load latency), D stored by
+ *                 coalesced warp stores; for small, latency-bound problems.  Not on
  *                 the pages: they fix the tile at 128 or 256 x 256.  0
  *                 (default): 64 when cta_group is 0, the K-loop is at most 8
  *                 tiles of 64 and the 128 x 64 tiles fit one wave of
