@@ -299,6 +299,10 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
     const uint32_t bar_drain = bar_tempty + 8 * C::ACC_BUFS;
     const uint32_t bar_recv = bar_drain + 8;  // K split: the cluster's partial rows have arrived
     const uint32_t krank = C::KSPLIT ? ptx::cluster_ctarank() : 0u;  // K slice of this CTA
+    // A CTA pair splits its teardown cluster barrier: the epilogue warps arrive
+    // as soon as their last TMEM read is done, so the barrier's latency passes
+    // under the last tile's stores; every thread arrives exactly once.
+    bool cluster_arrived = false;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
 
@@ -542,6 +546,17 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                         ptx::mbar_arrive_cluster(ptx::mapa(bar_tempty + 8 * acc.stage, 0));
                     } else {
                         ptx::mbar_arrive(bar_tempty + 8 * acc.stage);
+                    }
+                }
+                if constexpr (C::CLUSTER > 1 && !C::KSPLIT) {
+                    if (item + num_clusters >= p.num_items) {
+                        // This CTA's last work item: the warp touches no TMEM
+                        // and no other CTA's shared memory from here on (its
+                        // release orders the arrival above on the leader's
+                        // barrier), only its own staging and D.
+                        __syncwarp();  // the arrival is warp-aligned
+                        ptx::cluster_arrive();
+                        cluster_arrived = true;
                     }
                 }
             };
@@ -807,10 +822,11 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
     }
 
     // ---- teardown: the cluster's CTAs done with TMEM and with each other's
-    // SMEM
+    // SMEM (the epilogue warps of a pair arrived after their last TMEM read)
     ptx::tcgen05_fence_before();
     if constexpr (C::CLUSTER > 1) {
-        ptx::cluster_sync();
+        if (!cluster_arrived) ptx::cluster_arrive();
+        ptx::cluster_wait();
     } else {
         __syncthreads();
     }
