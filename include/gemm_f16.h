@@ -113,22 +113,26 @@ typedef enum gemm_status {
  *                 one single-CTA consumer; block_m 0 then means 64): tiny
  *                 (block_m 64) or narrow (block_m 128) tiles with K split
  *                 across a thread-block cluster of that many CTAs, one
- *                 cluster per tile and one K
- *                 slice per CTA (at most one per 64-wide K tile, so fewer
- *                 CTAs when K is short, and halved until the device can run
- *                 clusters of that size); each CTA keeps its slice's fp32 sums
- *                 in shared memory and the cluster adds them, in slice order,
- *                 through distributed shared memory before the one rounding
- *                 to fp16.  No workspace and no second kernel.  Each CTA then
- *                 streams 1/cluster_k of the tile's operands, which is what
- *                 bounds small problems.  Not on the pages.  1: no K split.
- *                 0 (default): with the narrow or tiny tiles, max_clusters 0
- *                 and at least 8 K tiles of 64, the largest of 8, 4, 2 that leaves
- *                 each CTA at least 2 K tiles, lets all the clusters run at
- *                 once and keeps the grid within half the co-resident CTAs
- *                 (within all of them from 24 K tiles per CTA), else 1.
- *                 max_clusters does not cap this grid.  Other values:
- *                 GEMM_ERR_INVALID_ARG.
+ *                 cluster per tile and one K slice per CTA (at most one per
+ *                 64-wide K tile, so fewer CTAs when K is short, and halved
+ *                 until the device can run clusters of that size).  Each CTA
+ *                 keeps its slice's fp32 sums in shared memory and the
+ *                 cluster adds them, in slice order, through distributed
+ *                 shared memory before the one rounding to fp16: no
+ *                 workspace and no second kernel.  Each CTA then streams
+ *                 1/cluster_k of the tile's operands, which is what bounds
+ *                 small problems.  Not on the pages.  1: no K split.
+ *                 0 (default): with max_clusters 0 and at least 8 K tiles
+ *                 of 64, the largest of 8, 4, 2 that leaves each CTA at
+ *                 least 2 K tiles, lets all the clusters run at once and
+ *                 keeps the grid within half the co-resident CTAs (within
+ *                 all of them from 24 K tiles per CTA), else 1.  With
+ *                 block_m 0 as well, a long K can turn tiny tiles into
+ *                 narrow ones: where the tiny tiles get no split but the
+ *                 narrow ones do with at least 24 K tiles per CTA, and where
+ *                 the tiny ones split in 2 but the narrow ones can split in
+ *                 4 with at least 16.  max_clusters does not cap this grid.
+ *                 Other values: GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {
     int32_t cta_group;
