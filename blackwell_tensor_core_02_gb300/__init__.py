@@ -89,6 +89,11 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_f16_nt_describe.restype = ctypes.c_int
     lib.gemm_f16_pipeline_trace.argtypes = [i32, i32, i32, i32p, i32p]
     lib.gemm_f16_pipeline_trace.restype = ctypes.c_int
+    lib.gemm_f16_co_resident.argtypes = [i32p, i32]
+    lib.gemm_f16_co_resident.restype = ctypes.c_int
+    lib.gemm_f16_nt_describe_for.argtypes = [i64, i64, i64, ctypes.POINTER(Options), i32, i32p, i32,
+                                             ctypes.POINTER(LaunchInfo)]
+    lib.gemm_f16_nt_describe_for.restype = ctypes.c_int
     return lib
 
 
@@ -355,6 +360,31 @@ def describe(M: int, N: int, K: int, options: Options | None = None, with_worksp
                                      1 if with_workspace else 0, ctypes.byref(info))
     if rc != 0:
         raise GemmError(rc, "gemm_f16_nt_describe")
+    return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
+
+
+CONFIG_KINDS = 11  # GEMM_F16_CONFIG_KINDS
+
+
+def co_resident() -> list[int]:
+    """Co-resident clusters of each kernel configuration on the current device (see the C header)."""
+    buf = (ctypes.c_int32 * CONFIG_KINDS)()
+    rc = load().gemm_f16_co_resident(buf, CONFIG_KINDS)
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_co_resident")
+    return list(buf)
+
+
+def describe_for(M: int, N: int, K: int, co_resident_counts, options: Options | None = None,
+                 with_workspace: bool = False) -> dict:
+    """The configuration a call would launch on a device with these co-resident counts (pure host)."""
+    counts = (ctypes.c_int32 * len(co_resident_counts))(*co_resident_counts)
+    info = LaunchInfo()
+    rc = load().gemm_f16_nt_describe_for(M, N, K, ctypes.byref(options) if options is not None else None,
+                                         1 if with_workspace else 0, counts, len(co_resident_counts),
+                                         ctypes.byref(info))
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_nt_describe_for")
     return {f: getattr(info, f) for f, _ in LaunchInfo._fields_}
 
 

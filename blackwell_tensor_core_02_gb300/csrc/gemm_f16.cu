@@ -26,7 +26,8 @@ struct DeviceInfo {
     bool ready = false;
     int status = GEMM_OK;
     int sm_count = 0;
-    int max_clusters[11] = {};  // co-resident clusters: [0] cta_group 1, [1] pair, [2] pair + 2 consumers,
+    int max_clusters[GEMM_F16_CONFIG_KINDS] = {};  // co-resident clusters (the order of gemm_f16_co_resident):
+                                // [0] cta_group 1, [1] pair, [2] pair + 2 consumers,
                                 // [3] narrow single-CTA tiles, [4] tiny tiles, [5] [6] [7] tiny tiles with
                                 // K split across clusters of 2, 4 and 8 CTAs, [8] [9] [10] narrow tiles so
 };
@@ -583,6 +584,62 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     return launch<1, 1, 256>(A, B, D, M, N, K, s, *info, o, workspace, workspace_bytes);
 }
 
+// What a call would launch on a device with these co-resident cluster counts
+// (the body of gemm_f16_nt_describe and gemm_f16_nt_describe_for).
+int describe_with(const DeviceInfo &info, Opts o, int64_t M, int64_t N, int64_t K, bool ws,
+                  gemm_f16_launch_info *out) {
+    int st = GEMM_OK;
+    resolve_config(M, N, K, info, ws, &o);
+    Plan plan;
+    int stages = 0;
+    if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 2) {
+        st = make_plan<1, 1, 64, 64, 2>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64, 2>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 4) {
+        st = make_plan<1, 1, 64, 64, 4>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64, 4>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 8) {
+        st = make_plan<1, 1, 64, 64, 8>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64, 8>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64) {
+        st = make_plan<1, 1, 64, 64>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 64>::STAGES;
+    } else if (o.block_n == 64 && o.cluster_k == 2) {
+        st = make_plan<1, 1, 64, 128, 2>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 128, 2>::STAGES;
+    } else if (o.block_n == 64 && o.cluster_k == 4) {
+        st = make_plan<1, 1, 64, 128, 4>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 128, 4>::STAGES;
+    } else if (o.block_n == 64 && o.cluster_k == 8) {
+        st = make_plan<1, 1, 64, 128, 8>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64, 128, 8>::STAGES;
+    } else if (o.block_n == 64) {
+        st = make_plan<1, 1, 64>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 64>::STAGES;
+    } else if (o.cta_group == 2 && o.consumers == 2) {
+        st = make_plan<2, 2, 256>(M, N, K, info, o, false, &plan);
+        stages = Cfg<2, 2, 256>::STAGES;
+    } else if (o.cta_group == 2) {
+        st = make_plan<2, 1, 256>(M, N, K, info, o, ws, &plan);
+        stages = Cfg<2, 1, 256>::STAGES;
+    } else {
+        st = make_plan<1, 1, 256>(M, N, K, info, o, ws, &plan);
+        stages = Cfg<1, 1, 256>::STAGES;
+    }
+    if (st != GEMM_OK) return st;
+    out->cta_group = o.cta_group;
+    out->consumers = o.consumers;
+    out->block_n = o.block_n;
+    out->block_m = o.block_m;
+    out->stages = stages;
+    out->cluster_k = o.cluster_k > 1 ? o.cluster_k : 1;
+    out->split_k = o.cluster_k > 1 ? 1 : plan.p.slices;
+    out->clusters = plan.clusters;
+    out->work_items = plan.p.num_items;
+    out->workspace_bytes = plan.workspace_bytes;
+    return GEMM_OK;
+}
+
 int zero_fill(void *D, int64_t M, int64_t N, cudaStream_t stream) {
     const int64_t elems = M * N;
     const int64_t n16 = elems / 8;
@@ -654,56 +711,39 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
     DeviceInfo *info = nullptr;
     st = device_setup(&dev, &info);
     if (st != GEMM_OK) return st;
-    const bool ws = with_workspace != 0;
-    resolve_config(M, N, K, *info, ws, &o);
-    Plan plan;
-    int stages = 0;
-    if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 2) {
-        st = make_plan<1, 1, 64, 64, 2>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64, 2>::STAGES;
-    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 4) {
-        st = make_plan<1, 1, 64, 64, 4>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64, 4>::STAGES;
-    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 8) {
-        st = make_plan<1, 1, 64, 64, 8>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64, 8>::STAGES;
-    } else if (o.block_n == 64 && o.block_m == 64) {
-        st = make_plan<1, 1, 64, 64>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64>::STAGES;
-    } else if (o.block_n == 64 && o.cluster_k == 2) {
-        st = make_plan<1, 1, 64, 128, 2>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 128, 2>::STAGES;
-    } else if (o.block_n == 64 && o.cluster_k == 4) {
-        st = make_plan<1, 1, 64, 128, 4>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 128, 4>::STAGES;
-    } else if (o.block_n == 64 && o.cluster_k == 8) {
-        st = make_plan<1, 1, 64, 128, 8>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 128, 8>::STAGES;
-    } else if (o.block_n == 64) {
-        st = make_plan<1, 1, 64>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<1, 1, 64>::STAGES;
-    } else if (o.cta_group == 2 && o.consumers == 2) {
-        st = make_plan<2, 2, 256>(M, N, K, *info, o, false, &plan);
-        stages = Cfg<2, 2, 256>::STAGES;
-    } else if (o.cta_group == 2) {
-        st = make_plan<2, 1, 256>(M, N, K, *info, o, ws, &plan);
-        stages = Cfg<2, 1, 256>::STAGES;
-    } else {
-        st = make_plan<1, 1, 256>(M, N, K, *info, o, ws, &plan);
-        stages = Cfg<1, 1, 256>::STAGES;
-    }
+    return describe_with(*info, o, M, N, K, with_workspace != 0, out);
+}
+
+int gemm_f16_co_resident(int32_t *out, int32_t count) {
+    if (!out || count != GEMM_F16_CONFIG_KINDS) return GEMM_ERR_INVALID_ARG;
+    int dev = -1;
+    DeviceInfo *info = nullptr;
+    const int st = device_setup(&dev, &info);
     if (st != GEMM_OK) return st;
-    out->cta_group = o.cta_group;
-    out->consumers = o.consumers;
-    out->block_n = o.block_n;
-    out->block_m = o.block_m;
-    out->stages = stages;
-    out->cluster_k = o.cluster_k > 1 ? o.cluster_k : 1;
-    out->split_k = o.cluster_k > 1 ? 1 : plan.p.slices;
-    out->clusters = plan.clusters;
-    out->work_items = plan.p.num_items;
-    out->workspace_bytes = plan.workspace_bytes;
+    for (int i = 0; i < GEMM_F16_CONFIG_KINDS; ++i) out[i] = info->max_clusters[i];
     return GEMM_OK;
+}
+
+int gemm_f16_nt_describe_for(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts, int32_t with_workspace,
+                             const int32_t *co_resident, int32_t count, gemm_f16_launch_info *out) {
+    Opts o;
+    int st = parse_options(opts, &o);
+    if (st != GEMM_OK) return st;
+    if (M < 0 || N < 0 || K < 0 || !out || (with_workspace != 0 && with_workspace != 1) || !co_resident ||
+        count != GEMM_F16_CONFIG_KINDS) {
+        return GEMM_ERR_INVALID_ARG;
+    }
+    DeviceInfo info;
+    info.ready = true;
+    for (int i = 0; i < GEMM_F16_CONFIG_KINDS; ++i) {
+        // the five base configurations must run; the K splits may be missing (0)
+        if (co_resident[i] < (i < 5 ? 1 : 0)) return GEMM_ERR_INVALID_ARG;
+        info.max_clusters[i] = co_resident[i];
+    }
+    if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
+    *out = gemm_f16_launch_info{};
+    if (M == 0 || N == 0 || K == 0) return GEMM_OK;
+    return describe_with(info, o, M, N, K, with_workspace != 0, out);
 }
 
 int gemm_f16_last_device_status(void *stream, uint64_t *info) {

@@ -271,6 +271,35 @@ int gemm_f16_nt_describe(int64_t M, int64_t N, int64_t K, const gemm_f16_options
                          gemm_f16_launch_info *out);
 
 /*
+ * Kernel configurations whose co-resident cluster counts steer the choices of
+ * gemm_f16_options (see gemm_f16_co_resident()).
+ */
+#define GEMM_F16_CONFIG_KINDS 11
+
+/*
+ * How many clusters of each kernel configuration fit on the current device at
+ * once (cudaOccupancyMaxActiveClusters, measured at the per-device set-up the
+ * first GEMM call makes), in this order: [0] single CTAs with 128 x 256 tiles,
+ * [1] CTA pairs, [2] CTA pairs with two consumers, [3] narrow 128 x 64 tiles,
+ * [4] tiny 64 x 64 tiles, [5] [6] [7] tiny tiles with K split across clusters
+ * of 2, 4 and 8 CTAs, [8] [9] [10] narrow tiles likewise (0: the device cannot
+ * run that split).  `count` must be GEMM_F16_CONFIG_KINDS.  Returns GEMM_OK, the
+ * errors of the device set-up, or GEMM_ERR_INVALID_ARG.  Not on the pages.
+ */
+int gemm_f16_co_resident(int32_t *out, int32_t count);
+
+/*
+ * As gemm_f16_nt_describe(), for a device with the given co-resident counts
+ * (the order of gemm_f16_co_resident(); the first five at least 1, the rest
+ * at least 0) instead of the current one: pure host logic, no CUDA call.  On
+ * the current device, with its own counts, it gives what
+ * gemm_f16_nt_describe() gives.  Errors as gemm_f16_nt_describe(), and
+ * GEMM_ERR_INVALID_ARG for a null or short `co_resident`.  Not on the pages.
+ */
+int gemm_f16_nt_describe_for(int64_t M, int64_t N, int64_t K, const gemm_f16_options *opts, int32_t with_workspace,
+                             const int32_t *co_resident, int32_t count, gemm_f16_launch_info *out);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's status
  * word: GEMM_OK, or GEMM_ERR_DEVICE_TIMEOUT if a wait inside a kernel ran out
  * (the kernel then skipped its remaining work and exited; D is incomplete),

@@ -515,3 +515,102 @@ def test_forgotten_phase_toggle_corrupts_silently():
     # the library's traces, same seeds: always in order
     for seed in range(40):
         assert _simulate_ring(depth, 1, steps, seed) == list(range(steps))
+
+
+# ------------------------------------------- configuration choice, host only --
+# gemm_f16_nt_describe_for runs the library's configuration choice for a device
+# given by its co-resident cluster counts, without a GPU.  GB300: 152 SMs, one
+# CTA of any configuration per SM, so 152 single CTAs, 76 pairs, 36 clusters of
+# 4 and 15 of 8 (the GPU test checks these counts on the device itself).
+GB300 = [152, 76, 76, 152, 152, 76, 36, 15, 76, 36, 15]
+HALF = [76, 38, 38, 76, 76, 38, 18, 7, 38, 18, 7]      # a device with half the SMs
+NO_SPLIT = GB300[:5] + [0] * 6                         # one that cannot co-schedule clusters
+
+
+def test_describe_for_the_five_workloads_on_gb300():
+    expect = {
+        (128, 128, 64): dict(cta_group=1, block_n=64, block_m=64, cluster_k=1, clusters=4, work_items=4),
+        (256, 256, 512): dict(cta_group=1, block_n=64, block_m=64, cluster_k=4, clusters=16, work_items=64),
+        (4096, 4096, 4096): dict(cta_group=2, block_n=256, block_m=128, cluster_k=1, clusters=76, work_items=284),
+        (8192, 8192, 8192): dict(cta_group=2, block_n=256, block_m=128, cluster_k=1, clusters=76, work_items=1060),
+        (8192, 28672, 4096): dict(cta_group=2, block_n=256, block_m=128, cluster_k=1, clusters=76,
+                                  work_items=3596),
+    }
+    for (M, N, K), want in expect.items():
+        got = g.describe_for(M, N, K, GB300)
+        assert {k: got[k] for k in want} == want, (M, N, K)
+        assert got["split_k"] == 1 and got["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("M,N,K,bm,ks", [
+    (256, 256, 4096, 64, 4), (128, 128, 4096, 64, 8), (256, 256, 1024, 64, 4), (128, 1024, 1024, 64, 2),
+    (384, 384, 2048, 64, 2), (512, 512, 4096, 128, 4), (256, 256, 512, 64, 4), (128, 128, 512, 64, 4),
+    (256, 256, 448, 64, 1), (512, 512, 512, 64, 1), (512, 512, 1024, 64, 1), (576, 576, 1024, 64, 1),
+    (640, 640, 4096, 128, 2), (768, 512, 4096, 128, 2), (512, 1024, 4096, 128, 2), (768, 768, 4096, 128, 2),
+    (768, 768, 2048, 128, 1),
+])
+def test_describe_for_the_cluster_k_split_rule(M, N, K, bm, ks):
+    c = g.describe_for(M, N, K, GB300)
+    tiles = -(-M // bm) * -(-N // 64)
+    assert (c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (64, bm, ks, 1)
+    assert (c["clusters"], c["work_items"], c["workspace_bytes"]) == (tiles, tiles * ks, 0)
+    # with a workspace the split still wins; without the device's clusters it is off
+    assert g.describe_for(M, N, K, GB300, with_workspace=True)["workspace_bytes"] == 0
+    assert g.describe_for(M, N, K, NO_SPLIT)["cluster_k"] == 1
+
+
+def test_describe_for_the_workspace_split_k_choice():
+    capped = g.Options(max_clusters=76)  # a capped grid turns the cluster split off
+    deep = g.describe_for(768, 640, 4096, GB300, capped, with_workspace=True)
+    assert (deep["cta_group"], deep["block_n"], deep["split_k"], deep["workspace_bytes"]) == (2, 256, 8, 8 * 768 * 640 * 4)
+    assert g.describe_for(768, 640, 4096, GB300, with_workspace=True)["workspace_bytes"] == 0
+    # 4 slices only: narrow tiles instead
+    assert g.describe_for(1024, 1024, 4096, GB300, with_workspace=True)["block_n"] == 64
+
+
+def test_describe_for_rejects_bad_devices_and_arguments():
+    lib = g.load()
+    info = g.LaunchInfo()
+    counts = (ctypes.c_int32 * 11)(*GB300)
+    assert lib.gemm_f16_nt_describe_for(128, 128, 64, None, 0, counts, 10, ctypes.byref(info)) == INVALID
+    assert lib.gemm_f16_nt_describe_for(128, 128, 64, None, 0, None, 11, ctypes.byref(info)) == INVALID
+    assert lib.gemm_f16_nt_describe_for(128, 128, 64, None, 0, counts, 11, None) == INVALID
+    assert lib.gemm_f16_nt_describe_for(128, 128, 64, None, 2, counts, 11, ctypes.byref(info)) == INVALID
+    assert lib.gemm_f16_nt_describe_for(128, 12, 64, None, 0, counts, 11, ctypes.byref(info)) == UNSUPPORTED
+    for bad in ([0] + GB300[1:], GB300[:4] + [0] + GB300[5:], GB300[:7] + [-1] + GB300[8:]):
+        with pytest.raises(g.GemmError):
+            g.describe_for(128, 128, 64, bad)
+    assert g.describe_for(0, 128, 64, GB300)["clusters"] == 0
+    with pytest.raises(g.GemmError):
+        g.describe_for(128, 128, 64, GB300, g.Options(cluster_k=3))
+
+
+@pytest.mark.parametrize("device", [GB300, HALF, NO_SPLIT], ids=["gb300", "half", "no-split"])
+def test_describe_for_random_shapes_keep_the_launch_rules(device):
+    """Whatever the shape, the chosen configuration respects the launch rules: a K split only
+    on 64-wide tiles, one cluster per tile, every cluster co-resident at once, at least one K
+    tile per CTA, and no split on a device that cannot run its clusters."""
+    rng = np.random.default_rng(5)
+    slots = {(64, 2): 5, (64, 4): 6, (64, 8): 7, (128, 2): 8, (128, 4): 9, (128, 8): 10}
+    for _ in range(400):
+        M = int(rng.integers(1, 6000))
+        N = int(rng.integers(1, 800)) * 8
+        K = int(rng.choice([int(rng.integers(1, 64)) * 8, int(rng.integers(64, 1200)) * 8]))
+        ws = bool(rng.integers(0, 2))
+        c = g.describe_for(M, N, K, device, with_workspace=ws)
+        k_tiles = -(-K // 64)
+        assert c["cluster_k"] in (1, 2, 4, 8) and c["split_k"] >= 1
+        if c["block_n"] == 64:
+            assert c["cta_group"] == 1 and c["block_m"] in (64, 128) and c["workspace_bytes"] == 0
+            tiles = -(-M // c["block_m"]) * -(-N // 64)
+        if c["cluster_k"] > 1:
+            assert c["block_n"] == 64 and c["split_k"] == 1
+            assert c["clusters"] == tiles and c["work_items"] == tiles * c["cluster_k"]
+            assert c["clusters"] <= device[slots[(c["block_m"], c["cluster_k"])]]
+            assert c["cluster_k"] <= k_tiles and k_tiles >= 8
+        elif c["block_n"] == 64:
+            assert c["work_items"] == tiles
+        if c["split_k"] > 1:
+            assert ws and c["block_n"] == 256 and c["workspace_bytes"] == c["split_k"] * M * N * 4
+        if device is NO_SPLIT:
+            assert c["cluster_k"] == 1

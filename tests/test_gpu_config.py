@@ -124,3 +124,23 @@ def test_explicit_options_are_obeyed(gpu_lib):
     assert (tiny["cta_group"], tiny["block_n"], tiny["block_m"], tiny["work_items"]) == (1, 64, 64, 64 * 64)
     capped = gpu_lib.describe(4096, 4096, 4096, gpu_lib.Options(max_clusters=5))
     assert capped["clusters"] == 5
+
+
+def test_host_query_agrees_with_the_device(gpu_lib):
+    # The device's own co-resident counts are the fixture the host-only tests use, and the
+    # host-only query with them gives what the device query gives, for any shape and options.
+    import numpy as np
+
+    counts = gpu_lib.co_resident()
+    assert counts == [152, 76, 76, 152, 152, 76, 36, 15, 76, 36, 15]
+    rng = np.random.default_rng(9)
+    opts = [None, gpu_lib.Options(cta_group=1), gpu_lib.Options(block_m=64), gpu_lib.Options(block_m=128, block_n=64),
+            gpu_lib.Options(cluster_k=4), gpu_lib.Options(max_clusters=7), gpu_lib.Options(consumers=2)]
+    for _ in range(300):
+        M = int(rng.integers(1, 9000))
+        N = int(rng.integers(1, 1200)) * 8
+        K = int(rng.integers(1, 1100)) * 8
+        o = opts[int(rng.integers(0, len(opts)))]
+        ws = bool(rng.integers(0, 2))
+        assert gpu_lib.describe(M, N, K, o, with_workspace=ws) == gpu_lib.describe_for(M, N, K, counts, o,
+                                                                                        with_workspace=ws), (M, N, K)
