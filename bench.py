@@ -170,6 +170,22 @@ class ClockSampler:
                 "note": note}
 
 
+DISQUALIFYING_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown")
+
+
+def needs_remeasure(clocks) -> bool:
+    """Whether a timed region's clock record disqualifies the run: a hardware or thermal
+    slowdown, or SM clocks far below their maximum with no reason given (a clock lock left
+    by someone else).  The power cap (sw_power_cap) is normal for a dense GEMM and is kept."""
+    if not clocks or clocks.get("sm_mhz") is None:
+        return False
+    reasons = set(clocks.get("reasons") or [])
+    if reasons & set(DISQUALIFYING_REASONS):
+        return True
+    top = clocks.get("sm_max_mhz")
+    return not reasons and bool(top) and clocks["sm_mhz"] < 0.7 * top
+
+
 # ------------------------------------------------------------- CPU oracle --
 
 def parity_stats(got, ref) -> dict:
@@ -443,28 +459,40 @@ def run_ours(args) -> None:
         if not parity["pass"]:
             raise RuntimeError("bench correctness guard failed against the oracle")
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    for i in range(args.warmup):
-        step(i)
-    barrier()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    t_wall0 = time.time()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    ev1.synchronize()
-    t_wall1 = time.time()
-    barrier()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    status, info = g.last_device_status(stream)
-    if status != 0:
-        raise RuntimeError(f"device status {g.status_string(status)} info={info:#x}")
-    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
-    if sampler:
-        sampler.stop()
+    def timed_region():
+        """W warm-up steps, then K timed steps between barriers; (max elapsed ms over ranks,
+        rank 0's clock record of the timed region)."""
+        sampler = ClockSampler(local) if rank == 0 else None
+        for i in range(args.warmup):
+            step(i)
+        barrier()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        ev1.synchronize()
+        t_wall1 = time.time()
+        barrier()
+        ms = ev0.elapsed_time(ev1)
+        status, info = g.last_device_status(stream)
+        if status != 0:
+            raise RuntimeError(f"device status {g.status_string(status)} info={info:#x}")
+        ms = max_over_ranks(ms, dist, dev)
+        record = sampler.summary(t_wall0, t_wall1) if sampler else None
+        if sampler:
+            sampler.stop()
+        return ms, record
+
+    elapsed_ms, clocks = timed_region()
+    # a run the clock record disqualifies is measured once more (every rank, in step)
+    if max_over_ranks(1.0 if needs_remeasure(clocks) else 0.0, dist, dev) > 0:
+        first = clocks
+        elapsed_ms, clocks = timed_region()
+        if clocks is not None:
+            clocks["remeasured_after"] = {k: first.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons")} if first else None
 
     ms_per_step = elapsed_ms / args.steps
     value = whole_job_tflops(flop, args.steps, world, elapsed_ms)

@@ -57,3 +57,15 @@ def test_warmup_below_three_is_rejected():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
                        text=True, timeout=120)
     assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_clock_records_that_disqualify_a_run():
+    # kept: the power cap of a dense GEMM, and clocks near the maximum
+    assert not bench.needs_remeasure({"sm_mhz": 1520.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"]})
+    assert not bench.needs_remeasure({"sm_mhz": 2000.0, "sm_max_mhz": 2070.0, "reasons": []})
+    assert not bench.needs_remeasure(None)
+    assert not bench.needs_remeasure({"sm_mhz": None, "sm_max_mhz": None, "reasons": []})
+    # measured again: a hardware or thermal slowdown, or clocks far down with no reason (a lock)
+    for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
+        assert bench.needs_remeasure({"sm_mhz": 1400.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap", r]})
+    assert bench.needs_remeasure({"sm_mhz": 1000.0, "sm_max_mhz": 2070.0, "reasons": []})
