@@ -29,7 +29,8 @@ struct DeviceInfo {
     int max_clusters[GEMM_F16_CONFIG_KINDS] = {};  // co-resident clusters (the order of gemm_f16_co_resident):
                                 // [0] cta_group 1, [1] pair, [2] pair + 2 consumers,
                                 // [3] narrow single-CTA tiles, [4] tiny tiles, [5] [6] [7] tiny tiles with
-                                // K split across clusters of 2, 4 and 8 CTAs, [8] [9] [10] narrow tiles so
+                                // K split across clusters of 2, 4 and 8 CTAs, [8] [9] [10] narrow tiles
+                                // likewise
 };
 
 std::mutex g_mutex;

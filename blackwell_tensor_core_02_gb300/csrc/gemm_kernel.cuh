@@ -135,8 +135,7 @@ struct Cfg {
     static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
     static constexpr int A_STAGE = A_BLOCK * NC;
     static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
-    // (narrow tiles with a K split give two stages to the exchange buffers)
-    static constexpr int STAGES = TINY ? 12 : (NARROW ? (KSPLIT ? 6 : 8) : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)));
+    static constexpr int STAGES = TINY ? 12 : (NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)));
     static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
     static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
@@ -162,13 +161,16 @@ struct Cfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_D = OFF_B + STAGES * B_STAGE;
-    // K split: the CTA's own fp32 sums, all BLOCK_M rows, staged for the copies to their owners
     // With a K split the epilogue region at OFF_D receives the cluster's fp32
     // partial sums of this CTA's rows (KS slices x BLOCK_M / KS rows x BLOCK_N),
-    // in place of the staging buffers, and OFF_SRC holds the CTA's own sums.
+    // in place of the staging buffers.  The CTA's own sums (all BLOCK_M rows,
+    // staged for the copies to their owners) go to OFF_SRC, the start of the
+    // operand ring: a CTA of a K split has one work item, so when its
+    // accumulator is complete every load has landed and every MMA has read
+    // its operands, and the ring is idle for good.
     static constexpr int EPI_REGION = KSPLIT ? BLOCK_M * BLOCK_N * 4 : EPI_WARPS * EPI_BUFS * EPI_BUF;
-    static constexpr int OFF_SRC = OFF_D + EPI_REGION;
-    static constexpr int OFF_BAR = OFF_SRC + (KSPLIT ? BLOCK_M * BLOCK_N * 4 : 0);
+    static constexpr int OFF_SRC = OFF_A;
+    static constexpr int OFF_BAR = OFF_D + EPI_REGION;
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1 + (KSPLIT ? 1 : 0);  // + drain (+ recv)
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;         // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
@@ -178,9 +180,12 @@ struct Cfg {
     // with a K split, the staging buffers receive the cluster's fp32 partial
     // sums of this CTA's rows: KS slices x (BLOCK_M / KS) rows x BLOCK_N fp32
     static constexpr int KS_ROWS = BLOCK_M / KS;        // rows of the tile this CTA adds up and stores
-    static constexpr uint32_t KS_RECV_BYTES = BLOCK_M * BLOCK_N * 4;  // all slices of those rows
+    static constexpr uint32_t KS_ROW_BYTES = BLOCK_N * 4;             // one row of fp32 sums
+    static constexpr uint32_t KS_RECV_BYTES = BLOCK_M * KS_ROW_BYTES;  // all slices of those rows
     static_assert(!KSPLIT || (EPI_COALESCED && KS_ROWS % 8 == 0),
                   "the cluster's partial sums of a CTA's rows fit its staging buffers");
+    static_assert(!KSPLIT || BLOCK_M * KS_ROW_BYTES <= STAGES * (A_STAGE + B_STAGE),
+                  "a K split's own sums fit the idle operand ring");
 };
 
 struct Params {
@@ -652,8 +657,9 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     // K split across the cluster: CTA s adds up and stores
                     // rows [s * KS_ROWS, (s + 1) * KS_ROWS) of the tile.
                     // Lane r writes its row R's fp32 sums over this CTA's K
-                    // slice to row R of the CTA's source buffer (256 bytes,
-                    // 16-byte unit u at u ^ (R % 8): no bank conflicts); then
+                    // slice, chunk c at 16-byte units 16c .. 16c + 15, to row
+                    // R of the CTA's source buffer (KS_ROW_BYTES, unit u at
+                    // u ^ (R % 8): no bank conflicts).  After the last chunk
                     // one lane copies the warp's rows, by the copy engine, to
                     // slots krank * KS_ROWS + R % KS_ROWS of each owner's
                     // receive region (the same swizzle, as KS_ROWS is a
@@ -661,29 +667,33 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     const uint32_t src = base + C::OFF_SRC;
                     if (lane < C::WARP_ROWS) {
                         const uint32_t R = static_cast<uint32_t>(quarter * C::WARP_ROWS + lane);
-                        const uint32_t row_addr = src + R * 256u;
+                        const uint32_t row_addr = src + R * C::KS_ROW_BYTES;
                         const uint32_t sw = R & 7u;
+                        const uint32_t u0 = 16u * static_cast<uint32_t>(c);
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
-                            ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ sw) * 16u), lo[4 * j],
-                                              lo[4 * j + 1], lo[4 * j + 2], lo[4 * j + 3]);
-                            ptx::st_shared_v4(row_addr + ((static_cast<uint32_t>(8 + j) ^ sw) * 16u), hi[4 * j],
-                                              hi[4 * j + 1], hi[4 * j + 2], hi[4 * j + 3]);
+                            ptx::st_shared_v4(row_addr + (((u0 + j) ^ sw) * 16u), lo[4 * j], lo[4 * j + 1],
+                                              lo[4 * j + 2], lo[4 * j + 3]);
+                            ptx::st_shared_v4(row_addr + (((u0 + 8 + j) ^ sw) * 16u), hi[4 * j], hi[4 * j + 1],
+                                              hi[4 * j + 2], hi[4 * j + 3]);
                         }
                     }
-                    ptx::fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        // rows [r0, r0 + WARP_ROWS) of the tile, cut at owner boundaries
-                        const uint32_t r0 = static_cast<uint32_t>(quarter * C::WARP_ROWS);
-                        for (uint32_t R = r0; R < r0 + C::WARP_ROWS;) {
-                            const uint32_t owner = R / C::KS_ROWS;
-                            uint32_t end = (owner + 1) * C::KS_ROWS;
-                            if (end > r0 + C::WARP_ROWS) end = r0 + C::WARP_ROWS;
-                            const uint32_t slot = krank * C::KS_ROWS + R % C::KS_ROWS;
-                            ptx::bulk_copy_to_cluster(ptx::mapa(sD + slot * 256u, owner), src + R * 256u,
-                                                      (end - R) * 256u, ptx::mapa(bar_recv, owner));
-                            R = end;
+                    if (c == chunks - 1) {
+                        ptx::fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            // rows [r0, r0 + WARP_ROWS) of the tile, cut at owner boundaries
+                            const uint32_t r0 = static_cast<uint32_t>(quarter * C::WARP_ROWS);
+                            for (uint32_t R = r0; R < r0 + C::WARP_ROWS;) {
+                                const uint32_t owner = R / C::KS_ROWS;
+                                uint32_t end = (owner + 1) * C::KS_ROWS;
+                                if (end > r0 + C::WARP_ROWS) end = r0 + C::WARP_ROWS;
+                                const uint32_t slot = krank * C::KS_ROWS + R % C::KS_ROWS;
+                                ptx::bulk_copy_to_cluster(ptx::mapa(sD + slot * C::KS_ROW_BYTES, owner),
+                                                          src + R * C::KS_ROW_BYTES, (end - R) * C::KS_ROW_BYTES,
+                                                          ptx::mapa(bar_recv, owner));
+                                R = end;
+                            }
                         }
                     }
                 } else if constexpr (C::EPI_COALESCED) {
@@ -774,12 +784,13 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
             const bool ok = wait_bounded<true>(bar_recv, 0, abort_flag, p.timeout_ns, kRoleEpilogue, 0xFFFFFFFEu);
             ptx::cluster_arrive_relaxed();
             // per 8-column chunk of a row: add the KS slices in slice order
-            // (fp32), round once to fp16, store 16 bytes; eight consecutive
-            // threads cover one 128-byte row of D
-            for (int u = static_cast<int>(threadIdx.x) - 32 * C::EPI_WARP0; ok && u < C::KS_ROWS * 8;
+            // (fp32), round once to fp16, store 16 bytes; BLOCK_N / 8
+            // consecutive threads cover one row of the tile in D
+            constexpr int kChunks = C::BLOCK_N / 8;
+            for (int u = static_cast<int>(threadIdx.x) - 32 * C::EPI_WARP0; ok && u < C::KS_ROWS * kChunks;
                  u += 32 * C::EPI_WARPS) {
-                const int r = u / 8;   // row among this CTA's rows
-                const int ch = u % 8;  // 8-column chunk
+                const int r = u / kChunks;   // row among this CTA's rows
+                const int ch = u % kChunks;  // 8-column chunk
                 if (!in_bounds(krank < static_cast<uint32_t>(KS) && r < C::KS_ROWS, abort_flag, kRoleEpilogue,
                                kCheckReduceRow, 0)) {
                     break;
@@ -788,7 +799,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                 float4 x, y;
 #pragma unroll
                 for (int j = 0; j < KS; ++j) {
-                    const uint32_t row_addr = sD + static_cast<uint32_t>(j * C::KS_ROWS + r) * 256u;
+                    const uint32_t row_addr = sD + static_cast<uint32_t>(j * C::KS_ROWS + r) * C::KS_ROW_BYTES;
                     const uint4 a = ptx::ld_shared_v4(row_addr + ((static_cast<uint32_t>(2 * ch) ^ sw) * 16u));
                     const uint4 b = ptx::ld_shared_v4(row_addr + ((static_cast<uint32_t>(2 * ch + 1) ^ sw) * 16u));
                     const float4 fa = make_float4(__uint_as_float(a.x), __uint_as_float(a.y), __uint_as_float(a.z),

@@ -68,7 +68,7 @@ def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
     assert (forced["block_m"], forced["cluster_k"], forced["clusters"]) == (64, 4, 16 * 9)
     narrow = gpu_lib.describe(1000, 520, 1000, gpu_lib.Options(cluster_k=4, block_m=128))
     assert (narrow["block_n"], narrow["block_m"], narrow["cluster_k"], narrow["clusters"], narrow["stages"]) == \
-        (64, 128, 4, 8 * 9, 6)
+        (64, 128, 4, 8 * 9, 8)
 
 
 def test_small_problems_take_narrow_tiles(gpu_lib):
