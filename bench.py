@@ -267,13 +267,13 @@ def run_reference(args) -> None:
     A, B = w.operands()
     threads = os.cpu_count() or 1
     oracle.build()
-    # size each step so that warm-up + timed steps take about a minute in total
+    # size each step so that warm-up + timed steps take about --ref-seconds (a minute) in total
     rng = np.random.default_rng(0)
     calib = 2048
     t0 = time.perf_counter()
     oracle.gemm_f16_nt_points(A, B, rng.integers(0, w.M, calib), rng.integers(0, w.N, calib), threads=threads)
     per_point = (time.perf_counter() - t0) / calib
-    budget = 60.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     points = int(min(1 << 20, max(threads, budget / per_point)))
     samples = [(rng.integers(0, w.M, points), rng.integers(0, w.N, points)) for _ in range(2)]
     for i in range(args.warmup):
@@ -595,11 +595,15 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the pass over all five shapes")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: host time for warm-up and timed steps together")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.steps < 1:
         ap.error("--steps must be at least 1")
+    if not args.ref_seconds > 0:
+        ap.error("--ref-seconds must be positive")
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -69,3 +69,28 @@ def test_clock_records_that_disqualify_a_run():
     for r in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"):
         assert bench.needs_remeasure({"sm_mhz": 1400.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap", r]})
     assert bench.needs_remeasure({"sm_mhz": 1000.0, "sm_max_mhz": 2070.0, "reasons": []})
+
+
+def test_reference_arm_prints_the_contract_line():
+    """--impl reference on the host cores: one JSON line with the main arm's metric, unit and
+    direction, the oracle as its cpu_baseline, and an e2e that moves no bytes to or from a GPU."""
+    env = dict(os.environ, RANK="0")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "3", "--ref-seconds", "1"], cwd=ROOT, env=env, capture_output=True, text=True,
+                         timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert (d["impl"], d["metric"], d["unit"], d["higher_is_better"]) == ("reference", bench.METRIC, bench.UNIT, True)
+    assert (d["n_gpus"], d["steps"], d["warmup"], d["data"], d["dtype"]) == (1, 2, 3, "synthetic", "f64")
+    assert d["config"]["workload"] == bench.WORKLOAD and d["value"] > 0 and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_budget_must_be_positive():
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--ref-seconds", "0"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=120)
+    assert out.returncode != 0 and "--ref-seconds" in out.stderr
