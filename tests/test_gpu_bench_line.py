@@ -1,0 +1,48 @@
+"""bench.py's main arm on the GPU: one JSON line that keeps the measurement contract.
+
+A short run (few steps, no cuBLAS, no CPU baseline, no workload pass) through the same code
+as the default one: the headline value is the 4096^3 GEMM's whole-job TFLOP/s, the roofline
+object divides it by the measured peak, the end-to-end figure moves A and B in and D out
+every step, and every timed step is one launch of this library's kernel.
+"""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_main_arm_prints_the_contract_line():
+    steps, warmup = 50, 3
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", str(steps), "--warmup",
+                          str(warmup), "--no-cublas", "--no-cpu-baseline", "--no-workloads", "--e2e-steps", "5"],
+                         cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert (d["metric"], d["unit"], d["higher_is_better"], d["scaling"]) == (bench.METRIC, bench.UNIT, True, "weak")
+    assert (d["n_gpus"], d["steps"], d["warmup"], d["dtype"], d["data"]) == (1, steps, warmup, "f16", "synthetic")
+    assert d["config"]["workload"] == bench.WORKLOAD and d["vs_baseline"] is None
+    M = N = K = 4096
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["value"] == pytest.approx(2.0 * M * N * K / (d["ms_per_step"] * 1e-3) / 1e12, rel=1e-6)
+    r = d["roofline"]
+    assert (r["bound"], r["unit"]) == ("tensor", "TFLOP/s") and r["peak"] > 0
+    assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-9)
+    assert r["traffic"] is None or r["traffic"] > 0
+    e = d["e2e"]
+    assert e["unit"] == d["unit"] and 0 < e["value"] < d["value"]
+    assert (e["h2d_bytes_per_step"], e["d2h_bytes_per_step"]) == (2 * (M * K + N * K), 2 * M * N)
+    assert d["gpu_launches"] == steps
+    assert d["parity_vs_oracle"]["pass"] is True  # the guard's sampled outputs against the oracle
+    c = d["clocks"]
+    assert set(c) >= {"sm_mhz", "sm_max_mhz", "reasons"}
