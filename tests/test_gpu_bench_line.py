@@ -1,9 +1,10 @@
 """bench.py's main arm on the GPU: one JSON line that keeps the measurement contract.
 
-A short run (few steps, no cuBLAS, no CPU baseline, no workload pass) through the same code
-as the default one: the headline value is the 4096^3 GEMM's whole-job TFLOP/s, the roofline
-object divides it by the measured peak, the end-to-end figure moves A and B in and D out
-every step, and every timed step is one launch of this library's kernel.
+A short run (few steps, no cuBLAS, no workload pass) through the same code as the default
+one: the headline value is the 4096^3 GEMM's whole-job TFLOP/s, the roofline object divides
+it by the measured peak, the end-to-end figure moves A and B in and D out every step, every
+timed step is one launch of this library's kernel, and the cpu_baseline leg times the oracle
+after checking sampled outputs against it.  Without that leg the oracle is not run at all.
 """
 import json
 import os
@@ -23,7 +24,7 @@ import bench  # noqa: E402
 def test_main_arm_prints_the_contract_line():
     steps, warmup = 50, 3
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", str(steps), "--warmup",
-                          str(warmup), "--no-cublas", "--no-cpu-baseline", "--no-workloads", "--e2e-steps", "5"],
+                          str(warmup), "--no-cublas", "--no-workloads", "--e2e-steps", "5"],
                          cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-3000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
@@ -44,5 +45,21 @@ def test_main_arm_prints_the_contract_line():
     assert (e["h2d_bytes_per_step"], e["d2h_bytes_per_step"]) == (2 * (M * K + N * K), 2 * M * N)
     assert d["gpu_launches"] == steps
     assert d["parity_vs_oracle"]["pass"] is True  # the guard's sampled outputs against the oracle
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["unit"] == d["unit"] and cb["value"] > 0 and cb["cores"] >= 1
     c = d["clocks"]
     assert set(c) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+
+
+def test_without_the_cpu_baseline_leg_the_oracle_is_not_run():
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    code = ("import sys, runpy; sys.argv = ['bench.py', '--steps', '5', '--warmup', '3', '--no-cublas', "
+            "'--no-cpu-baseline', '--e2e-steps', '2']; runpy.run_path('bench.py', run_name='__main__'); "
+            "print('ORACLE_LOADED' if any(m == 'oracle' or m.startswith('oracle.') for m in sys.modules) "
+            "else 'ORACLE_ABSENT')")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-3000:]
+    assert out.stdout.strip().splitlines()[-1] == "ORACLE_ABSENT"
+    d = json.loads([ln for ln in out.stdout.splitlines() if ln.startswith("{")][0])
+    assert d["parity_vs_oracle"] is None and "cpu_baseline" not in d
+    assert all(w["parity_vs_oracle"] is None and "oracle" not in w for w in d["workloads"])
