@@ -281,13 +281,14 @@ int32_t cluster_k_for(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, co
 // Tiny tiles when they fill at most two thirds of a wave, else narrow ones,
 // each with the split cluster_k_for() gives them.  With a long K the narrow
 // tiles win in two cases (measured on GB300, graph-timed, us): where the tiny
-// tiles get no split but the narrow ones do with at least 24 K tiles per CTA
-// (640x640x4096 10.68 -> 9.33, 768x512x4096 10.68 -> 9.24), and where the
-// tiny tiles split in 2 and the narrow ones can split in 4 with at least 16
-// K tiles per CTA: the same grid with a quarter fewer operand bytes per CTA
-// (512x512x4096 8.09 -> 7.12).  With a shorter K the extra exchange loses
-// (128x1024x1024 3.61 -> 3.96, 512x512x1024 4.21 -> 4.66).  block_m and
-// cluster_k given by the caller are kept.
+// tiles get no split but the narrow ones do with at least 16 K tiles per CTA
+// (640x640x4096 10.68 -> 9.33, 768x512x4096 10.68 -> 9.24, 512x512x2048
+// 6.25 -> 5.76), and where the tiny tiles split in 2 and the narrow ones can
+// split in 4 with at least 8 K tiles per CTA: the same grid with a quarter
+// fewer operand bytes per CTA (512x512x4096 8.09 -> 7.12, 384x384x2048
+// 4.82 -> 4.41).  With a shorter K the extra exchange loses (128x1024x1024
+// 3.61 -> 3.96, 512x512x1024 4.21 -> 4.66).  block_m and cluster_k given by
+// the caller are kept.
 void small_tiles(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, Opts *o) {
     const int32_t forced_k = o->cluster_k;
     if (o->block_m != 0) {
@@ -308,10 +309,10 @@ void small_tiles(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, Opts *o
     o->block_m = 64;
     o->cluster_k = ks_tiny;
     if (forced_k != 0) return;  // cluster_k given (1: no split): keep the tiny tiles
-    if (ks_tiny == 1 && ks_narrow > 1 && k_tiles / ks_narrow >= 24) {
+    if (ks_tiny == 1 && ks_narrow > 1 && k_tiles / ks_narrow >= 16) {
         o->block_m = 128;
         o->cluster_k = ks_narrow;
-    } else if (ks_tiny == 2 && o->max_clusters == 0 && k_tiles / 4 >= 16) {
+    } else if (ks_tiny == 2 && o->max_clusters == 0 && k_tiles / 4 >= 8) {
         const int64_t tiles_narrow = ((M + 127) / 128) * ((N + 63) / 64);
         if (tiles_narrow <= dev.max_clusters[cluster_k_slot(4, 128)] && 4 * tiles_narrow <= dev.max_clusters[3]) {
             o->block_m = 128;

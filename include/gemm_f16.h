@@ -129,9 +129,9 @@ typedef enum gemm_status {
  *                 all of them from 24 K tiles per CTA), else 1.  With
  *                 block_m 0 as well, a long K can turn tiny tiles into
  *                 narrow ones: where the tiny tiles get no split but the
- *                 narrow ones do with at least 24 K tiles per CTA, and where
+ *                 narrow ones do with at least 16 K tiles per CTA, and where
  *                 the tiny ones split in 2 but the narrow ones can split in
- *                 4 with at least 16.  max_clusters does not cap this grid.
+ *                 4 with at least 8.  max_clusters does not cap this grid.
  *                 Other values: GEMM_ERR_INVALID_ARG.
  */
 typedef struct gemm_f16_options {

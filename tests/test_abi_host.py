@@ -544,10 +544,10 @@ def test_describe_for_the_five_workloads_on_gb300():
 
 @pytest.mark.parametrize("M,N,K,bm,ks", [
     (256, 256, 4096, 64, 4), (128, 128, 4096, 64, 8), (256, 256, 1024, 64, 4), (128, 1024, 1024, 64, 2),
-    (384, 384, 2048, 64, 2), (512, 512, 4096, 128, 4), (256, 256, 512, 64, 4), (128, 128, 512, 64, 4),
+    (512, 512, 4096, 128, 4), (256, 256, 512, 64, 4), (128, 128, 512, 64, 4),
     (256, 256, 448, 64, 1), (512, 512, 512, 64, 1), (512, 512, 1024, 64, 1), (576, 576, 1024, 64, 1),
     (640, 640, 4096, 128, 2), (768, 512, 4096, 128, 2), (512, 1024, 4096, 128, 2), (768, 768, 4096, 128, 2),
-    (768, 768, 2048, 128, 1),
+    (768, 768, 2048, 128, 1), (384, 384, 2048, 128, 4), (512, 512, 2048, 128, 2),
 ])
 def test_describe_for_the_cluster_k_split_rule(M, N, K, bm, ks):
     c = g.describe_for(M, N, K, GB300)

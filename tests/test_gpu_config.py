@@ -41,14 +41,14 @@ def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
     # from 8 K tiles of 64 on, 64-wide tiles split K across a cluster: the largest of 8, 4, 2 CTAs
     # that leaves each at least 2 K tiles, with tiles * cluster_k at most half the co-resident
     # CTAs (a whole wave with at least 24 K tiles per CTA); narrow tiles instead of tiny ones
-    # where the tiny ones get no split but the narrow ones do with at least 24 K tiles per CTA,
-    # or where the tiny ones split in 2 and the narrow ones can split in 4 with at least 16
+    # where the tiny ones get no split but the narrow ones do with at least 16 K tiles per CTA,
+    # or where the tiny ones split in 2 and the narrow ones can split in 4 with at least 8
     for (M, N, K), bm, ks in (((256, 256, 4096), 64, 4), ((128, 128, 4096), 64, 8), ((256, 256, 1024), 64, 4),
-                              ((128, 1024, 1024), 64, 2), ((384, 384, 2048), 64, 2), ((512, 512, 4096), 128, 4),
+                              ((128, 1024, 1024), 64, 2), ((384, 384, 2048), 128, 4), ((512, 512, 4096), 128, 4),
                               ((256, 256, 512), 64, 4), ((128, 128, 512), 64, 4), ((256, 256, 448), 64, 1),
                               ((512, 512, 512), 64, 1), ((512, 512, 1024), 64, 1), ((576, 576, 1024), 64, 1),
                               ((640, 640, 4096), 128, 2), ((768, 512, 4096), 128, 2), ((512, 1024, 4096), 128, 2),
-                              ((768, 768, 4096), 128, 2), ((768, 768, 2048), 128, 1)):
+                              ((768, 768, 4096), 128, 2), ((768, 768, 2048), 128, 1), ((512, 512, 2048), 128, 2)):
         c = gpu_lib.describe(M, N, K)
         tiles = -(-M // bm) * -(-N // 64)
         assert (c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (64, bm, ks, 1), (M, N, K)
