@@ -43,7 +43,9 @@ METRIC = "GEMM TFLOP/s at M=N=K=4096 fp16→fp32 acc; % of GB300 dense fp16 tens
 UNIT = "TFLOP/s"
 WORKLOAD = si.HEADLINE
 ROTATE = 4
-NOMINAL_PEAK_TFLOPS = 2250.0          # GB300 dense fp16/bf16 tensor, nominal
+# NVIDIA's published GB300 dense fp16/bf16 tensor figure (5 PFLOP/s with 2:4 sparsity, halved):
+# the stated peak the target of >= 70 % refers to
+STATED_PEAK_TFLOPS = 2500.0
 FALLBACK_PEAK_TFLOPS = 1900.0         # one earlier cuBLAS bf16 measurement on a GB300
 KERNEL_NAME = "gemm_f16_nt_kernel<2, 1, 256, 128, 1>"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "ncu_gemm_f16_nt_kernel_square_4096.json")
@@ -120,6 +122,7 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, gpu_index: int, interval_ms: int = 100):
+        self.interval_s = interval_ms / 1000.0
         self.samples: list[tuple[float, list[str]]] = []
         self.proc = None
         try:
@@ -138,6 +141,18 @@ class ClockSampler:
             if len(parts) == len(self.FIELDS):
                 self.samples.append((time.time(), parts))
 
+    def wait_for_sample(self, after: float, timeout_s: float = 3.0) -> bool:
+        """Block until a sample stamped after `after` has arrived (or the timeout): nvidia-smi
+        takes a moment to start, and a short timed region may end before the next sample."""
+        if self.proc is None:
+            return False
+        t_end = time.time() + timeout_s
+        while time.time() < t_end:
+            if any(t > after for t, _ in self.samples):
+                return True
+            time.sleep(0.01)
+        return False
+
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -147,13 +162,24 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0: float, t1: float) -> dict:
+        """Clock record of the region [t0, t1] (wall-clock seconds).  A region shorter than the
+        sampling interval may hold no sample: then the sample nearest to the region (waiting
+        for the next one if none has arrived yet) stands for it, and the note says how far
+        from the region it was taken."""
         inside = [p for t, p in self.samples if t0 <= t <= t1]
         note = "samples inside the timed region"
         if not inside:
-            after = [p for t, p in self.samples if t >= t0][:1]
-            inside, note = after, "timed region shorter than the sampling interval: first sample after its start"
+            self.wait_for_sample(t1, timeout_s=3 * self.interval_s + 1.0)
+            if self.samples:
+                mid = 0.5 * (t0 + t1)
+                t, p = min(self.samples, key=lambda tp: abs(tp[0] - mid))
+                gap_ms = (t0 - t if t < t0 else t - t1) * 1e3
+                side = "before the region's start" if t < t0 else "after the region's end"
+                inside = [p]
+                note = (f"timed region ({(t1 - t0) * 1e3:.1f} ms) shorter than the {self.interval_s * 1e3:.0f} ms "
+                        f"sampling interval: the nearest sample, {gap_ms:.0f} ms {side}")
         if not inside:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no nvidia-smi sample arrived"}
 
         def num(x):
             try:
@@ -223,10 +249,34 @@ def oracle_rows_calibrated(A, B, threads: int, target_s: float):
     return rows, v, dt, per_row, fixed
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu's "Model name", else /proc/cpuinfo's), with its vendor."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10, env=dict(os.environ, LC_ALL="C"))
+        fields = dict(line.split(":", 1) for line in out.stdout.splitlines() if ":" in line)
+        fields = {k.strip(): v.strip() for k, v in fields.items()}
+        name = fields.get("Model name")
+        if name:
+            vendor = fields.get("Vendor ID")
+            return f"{vendor} {name}" if vendor and vendor not in name else name
+    except (OSError, subprocess.SubprocessError, ValueError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
 def cpu_baseline(A, B, target_s: float = 12.0) -> dict:
     threads = os.cpu_count() or 1
     rows, v, dt, _, _ = oracle_rows_calibrated(A, B, threads, target_s)
-    return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle",
+    return {"value": v, "unit": UNIT, "cores": threads, "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"rows 0..{rows - 1} of D for {WORKLOAD} ({rows}x{B.shape[0]} outputs, K={A.shape[1]}), "
                       f"{dt:.1f} s on {threads} host threads"}
 
@@ -290,7 +340,8 @@ def run_reference(args) -> None:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": WORKLOAD, "M": w.M, "N": w.N, "K": w.K, "seed": w.seed},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "cpu_model": cpu_model(),
+                         "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -400,6 +451,132 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
     return out
 
 
+# --------------------------------------------------- sustained, at the cap --
+
+def measure_sustained(g, dev, A, B, local: int, seconds: float, with_cublas: bool = True) -> dict:
+    """The headline GEMM back to back for `seconds` per window, ours and cuBLAS alternating
+    (ours, cuBLAS, ours, cuBLAS), each window a CUDA graph of launches replayed over and over
+    with the inputs rotating over ROTATE device copies, its SM clock sampled inside the window.
+    Long windows run at the power cap, where the clock follows the power; the fraction of the
+    measured sustained peak (a cuBLAS bf16 loop under the same cap) is the fair comparison."""
+    import torch
+
+    w = si.WORKLOADS[WORKLOAD]
+    flop = float(w.flop)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        a0, b0 = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+        As = [a0.clone() for _ in range(ROTATE)]
+        Bs = [b0.clone() for _ in range(ROTATE)]
+        Ds = [torch.empty((w.M, w.N), dtype=torch.float16, device=dev) for _ in range(ROTATE)]
+        del a0, b0
+    stream.synchronize()
+    torch.backends.cuda.matmul.allow_fp16_reduced_precision_reduction = False
+
+    def ours(i):
+        j = i % ROTATE
+        rc = g.gemm_f16_nt_ptr(As[j].data_ptr(), Bs[j].data_ptr(), Ds[j].data_ptr(), w.M, w.N, w.K, sh)
+        if rc != 0:
+            raise g.GemmError(rc, "gemm_f16_nt (sustained)")
+
+    def cublas(i):
+        j = i % ROTATE
+        torch.matmul(As[j], Bs[j].t(), out=Ds[j])
+
+    per_graph = 100
+    graphs = {}
+    for label, fn in (("ours", ours), ("cublas", cublas)):
+        if label == "cublas" and not with_cublas:
+            continue
+        with torch.cuda.stream(stream):
+            for i in range(5):
+                fn(i)
+        stream.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for i in range(per_graph):
+                fn(i)
+        graphs[label] = graph
+    windows = {label: [] for label in graphs}
+    for label in list(graphs) * 2:
+        graph = graphs[label]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            graph.replay()
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        e1.synchronize()
+        replays = max(1, int(seconds * 1e3 / max(e0.elapsed_time(e1), 1e-3)))
+        sampler = ClockSampler(local)
+        sampler.wait_for_sample(0.0)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.time()
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(replays):
+                graph.replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        t1 = time.time()
+        clocks = sampler.summary(t0, t1)
+        sampler.stop()
+        ms = ev0.elapsed_time(ev1) / (replays * per_graph)
+        tf = flop / (ms * 1e-3) / 1e12
+        win = {"tflops": tf, "us_per_gemm": ms * 1e3, "gemms": replays * per_graph,
+               "seconds": ev0.elapsed_time(ev1) * 1e-3, "sm_mhz": clocks.get("sm_mhz"),
+               "reasons": clocks.get("reasons"), "power_w_max": clocks.get("power_w_max"),
+               "samples": clocks.get("samples")}
+        if clocks.get("sm_mhz"):
+            win["tflops_per_ghz"] = tf / (clocks["sm_mhz"] / 1000.0)
+        windows[label].append(win)
+    status, info = g.last_device_status(stream)
+    if status != 0:
+        raise RuntimeError(f"device status {g.status_string(status)} info={info:#x}")
+    del graphs, As, Bs, Ds
+    torch.cuda.empty_cache()
+
+    def mean(label, key):
+        vals = [x[key] for x in windows[label] if x.get(key) is not None]
+        return statistics.fmean(vals) if vals else None
+
+    ours_tf = mean("ours", "tflops")
+    out = {"value": ours_tf, "unit": UNIT, "sm_mhz": mean("ours", "sm_mhz"),
+           "tflops_per_ghz": mean("ours", "tflops_per_ghz"), "windows": windows["ours"]}
+    if "cublas" in windows:
+        cb = mean("cublas", "tflops")
+        out["cublas"] = {"value": cb, "sm_mhz": mean("cublas", "sm_mhz"),
+                         "tflops_per_ghz": mean("cublas", "tflops_per_ghz"), "windows": windows["cublas"]}
+        out["vs_cublas"] = ours_tf / cb if cb else None
+    out["what"] = (f"{WORKLOAD} back to back, CUDA-graph replay, {seconds:g} s windows alternating ours / cuBLAS "
+                   f"twice; value = mean of our two windows; clocks sampled inside each window")
+    return out
+
+
+def kernel_label(cfg: dict) -> str:
+    """A short name for the configuration gemm_f16_nt_describe reports."""
+    if cfg["block_n"] == 64:
+        kind = f"{'tiny' if cfg['block_m'] == 64 else 'narrow'} {cfg['block_m']}x64"
+        if cfg["cluster_k"] > 1:
+            kind += f", K over {cfg['cluster_k']} CTAs"
+    else:
+        kind = ("pair" if cfg["cta_group"] == 2 else "single") + f" {128 * cfg['cta_group']}x256"
+    return f"{kind}, {cfg['clusters']} clusters"
+
+
+def workloads_summary(workloads: list[dict]) -> list[dict]:
+    """One short entry per workload (graph-timed median), for the end of the JSON line."""
+    out = []
+    for w in workloads:
+        p = w.get("parity_vs_oracle")
+        out.append({"workload": w["workload"], "kernel": kernel_label(w["kernel"]),
+                    "us": round(w["ms_median"] * 1e3, 2), "tflops": round(w["tflops"], 1),
+                    "cublas_us": round(w["cublas_ms_median"] * 1e3, 2) if w.get("cublas_ms_median") else None,
+                    "hbm_gbs": round(w["hbm_gbs_compulsory"], 1), "parity": p["pass"] if p else None})
+    return out
+
+
 # ---------------------------------------------------------------- GPU arm --
 
 def run_ours(args) -> None:
@@ -469,6 +646,8 @@ def run_ours(args) -> None:
         """W warm-up steps, then K timed steps between barriers; (max elapsed ms over ranks,
         rank 0's clock record of the timed region)."""
         sampler = ClockSampler(local) if rank == 0 else None
+        if sampler:
+            sampler.wait_for_sample(0.0)  # nvidia-smi is up and sampling before anything is timed
         for i in range(args.warmup):
             step(i)
         barrier()
@@ -568,7 +747,8 @@ def run_ours(args) -> None:
                          "frac": per_gpu_tflops / peak, "traffic": traffic, "kernel": KERNEL_NAME,
                          "peak_source": peak_src,
                          "frac_of_sustained": (per_gpu_tflops / peak_sustained) if peak_sustained else None,
-                         "frac_of_nominal_2250": per_gpu_tflops / NOMINAL_PEAK_TFLOPS,
+                         "stated_peak": STATED_PEAK_TFLOPS,
+                         "frac_of_stated_peak": per_gpu_tflops / STATED_PEAK_TFLOPS,
                          "traffic_source": traffic_src,
                          "algorithmic_flop_per_launch": flop,
                          "algorithmic_bytes_per_launch": w.min_bytes},
@@ -585,6 +765,15 @@ def run_ours(args) -> None:
             line["cpu_baseline"] = cpu_baseline(A, B)
         if world == 1 and not args.no_workloads:
             line["workloads"] = measure_all_workloads(g, dev, peak, A, B, oracle_timing=cpu_leg)
+        if world == 1 and args.sustained_seconds > 0:
+            sus = measure_sustained(g, dev, A, B, local, args.sustained_seconds, with_cublas=not args.no_cublas)
+            if peak_sustained:
+                sus["frac_of_measured_sustained"] = sus["value"] / peak_sustained
+            sus["frac_of_stated_peak"] = sus["value"] / STATED_PEAK_TFLOPS
+            line["sustained"] = sus
+        if "workloads" in line:
+            # last, so that a reader of the line's tail sees all five shapes
+            line["workloads_summary"] = workloads_summary(line["workloads"])
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -601,6 +790,8 @@ def main(argv=None) -> None:
     ap.add_argument("--no-cublas", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-workloads", action="store_true", help="skip the pass over all five shapes")
+    ap.add_argument("--sustained-seconds", type=float, default=2.0,
+                    help="length of each back-to-back window of the sustained (power-capped) measurement; 0: none")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
                     help="--impl reference: host time for warm-up and timed steps together")
     args = ap.parse_args(argv)

@@ -919,7 +919,10 @@ int gemm_f16_pipeline_trace(int32_t depth, int32_t initial_phase, int32_t steps,
 namespace gemm_f16 {
 namespace {
 
-constexpr int64_t kStaticScratchBytes = int64_t(16) << 20;
+// the size the public header promises (GEMM_F16_STATIC_SCRATCH_BYTES), which is also the
+// refusal limit of gemm_f16_nt_static_ws
+constexpr int64_t kStaticScratchBytes = GEMM_F16_STATIC_SCRATCH_BYTES;
+static_assert(kStaticScratchBytes % 256 == 0, "whole 256-byte units");
 
 static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
 

@@ -37,6 +37,8 @@ def main(argv=None) -> None:
     ap.add_argument("--block-m", type=int, default=0, help="rows per CTA: 64 (with 64-wide tiles), 128, or 0")
     ap.add_argument("--cluster-k", type=int, default=0,
                     help="tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 the shape's default")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="M-tiles per group of the tile order; 0 for the shape's default")
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--graph", action="store_true", help="time a CUDA graph of the launches")
@@ -52,7 +54,7 @@ def main(argv=None) -> None:
     Br = torch.from_numpy(B).to(dev).unsqueeze(0).repeat(rot, 1, 1)
     Dr = torch.empty((rot, M, N), dtype=torch.float16, device=dev)
     opts = g.Options(cta_group=args.cta_group, consumers=args.consumers, block_n=args.block_n,
-                     block_m=args.block_m, cluster_k=args.cluster_k)
+                     block_m=args.block_m, cluster_k=args.cluster_k, raster_group=args.raster_group)
     stream = torch.cuda.Stream()
     sh = stream.cuda_stream
     need = g.workspace_size(M, N, K, opts) if args.entry == "ws" else 0
@@ -105,6 +107,7 @@ def main(argv=None) -> None:
                           "block_n": args.block_n if label == "ours" else None,
                           "block_m": args.block_m if label == "ours" else None,
                           "cluster_k": args.cluster_k if label == "ours" else None,
+                          "raster_group": args.raster_group if label == "ours" else None,
                           "workspace_bytes": need, "us_per_gemm": round(us, 3),
                           "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 2), "graph": args.graph,
                           "status": status}), flush=True)

@@ -614,3 +614,41 @@ def test_describe_for_random_shapes_keep_the_launch_rules(device):
             assert ws and c["block_n"] == 256 and c["workspace_bytes"] == c["split_k"] * M * N * 4
         if device is NO_SPLIT:
             assert c["cluster_k"] == 1
+
+
+def test_status_codes_are_pinned():
+    """The status numbering is part of the ABI: the header's enum, the binding's table and the
+    library's status strings agree, and the values stay what they are.  The first eight follow
+    the boundary's original list; GEMM_ERR_CUDA (-8) was added for runtime errors that are not a
+    launch failure, so the device range-check code moved to -10, and the fixed-scratch refusal
+    took -9."""
+    with open(os.path.join(ROOT, "include", "gemm_f16.h")) as f:
+        text = f.read()
+    body = re.search(r"typedef enum gemm_status \{(.*?)\} gemm_status_t;", text, flags=re.S).group(1)
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    header = {name: int(val) for name, val in re.findall(r"(GEMM_\w+)\s*=\s*(-?\d+)", body)}
+    expected = {"GEMM_OK": 0, "GEMM_ERR_INVALID_ARG": -1, "GEMM_ERR_UNSUPPORTED_SHAPE": -2,
+                "GEMM_ERR_MISALIGNED": -3, "GEMM_ERR_NO_DEVICE": -4, "GEMM_ERR_ARCH": -5, "GEMM_ERR_LAUNCH": -6,
+                "GEMM_ERR_DEVICE_TIMEOUT": -7, "GEMM_ERR_CUDA": -8, "GEMM_ERR_SCRATCH_LIMIT": -9,
+                "GEMM_ERR_DEVICE_BOUNDS": -10}
+    assert header == expected
+    assert {name: code for code, name in g.STATUS.items()} == expected
+    for name, code in expected.items():
+        assert g.status_string(code).split(":")[0] == name
+    assert g.status_string(-11) == "unknown gemm_f16 status"
+
+
+def test_last_device_status_reports_where_through_an_out_parameter():
+    """gemm_f16_last_device_status(stream, info) takes an optional uint64_t* beside the stream
+    (the boundary's first sketch had the stream alone): NULL is allowed, and without a device
+    the call reports GEMM_ERR_NO_DEVICE before touching it."""
+    assert "int gemm_f16_last_device_status(void *stream, uint64_t *info);" in open(
+        os.path.join(ROOT, "include", "gemm_f16.h")).read()
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful on a machine without a GPU")
+    lib = g.load()
+    info = ctypes.c_uint64(0x1234)
+    assert lib.gemm_f16_last_device_status(None, None) == NO_DEVICE
+    assert lib.gemm_f16_last_device_status(None, ctypes.byref(info)) == NO_DEVICE
+    assert info.value == 0x1234  # untouched on an error before the synchronisation

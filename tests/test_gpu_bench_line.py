@@ -24,7 +24,8 @@ import bench  # noqa: E402
 def test_main_arm_prints_the_contract_line():
     steps, warmup = 50, 3
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", str(steps), "--warmup",
-                          str(warmup), "--no-cublas", "--no-workloads", "--e2e-steps", "5"],
+                          str(warmup), "--no-cublas", "--no-workloads", "--e2e-steps", "5",
+                          "--sustained-seconds", "0.5"],
                          cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert out.returncode == 0, out.stderr[-3000:]
     lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
@@ -45,10 +46,17 @@ def test_main_arm_prints_the_contract_line():
     assert (e["h2d_bytes_per_step"], e["d2h_bytes_per_step"]) == (2 * (M * K + N * K), 2 * M * N)
     assert d["gpu_launches"] == steps
     assert d["parity_vs_oracle"]["pass"] is True  # the guard's sampled outputs against the oracle
+    assert r["stated_peak"] == 2500.0 and r["frac_of_stated_peak"] == pytest.approx(r["achieved"] / 2500.0)
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["unit"] == d["unit"] and cb["value"] > 0 and cb["cores"] >= 1
+    assert cb["cpu_model"]
     c = d["clocks"]
-    assert set(c) >= {"sm_mhz", "sm_max_mhz", "reasons"}
+    assert set(c) >= {"sm_mhz", "sm_max_mhz", "reasons", "note"}
+    # a timed region shorter than the sampling interval still gets the nearest sample
+    assert c["sm_mhz"] is not None and c["sm_max_mhz"] is not None, c
+    s = d["sustained"]
+    assert s["value"] > 0 and s["unit"] == d["unit"] and len(s["windows"]) == 2
+    assert all(w["gemms"] > 0 and w["sm_mhz"] for w in s["windows"])
 
 
 def test_without_the_cpu_baseline_leg_the_oracle_is_not_run():

@@ -4,10 +4,9 @@ Bar (per element, floating point): |gpu − oracle| ≤ 2⁻⁹·|oracle| + 1e-3
 the oracle the fp64 sum rounded once to fp16.  Cases with one product per
 output (identity operands) must match bit for bit.
 
-Small and medium shapes are compared in full; the three large workloads
-(4096³, 8192³, 8192×28672×4096) are compared, in the launch configuration the
-benchmark times, on whole sampled rows and columns (tile borders included)
-plus random points, all computed one by one by the oracle.
+Every shape is compared in full, the three large workloads (4096³, 8192³,
+8192×28672×4096) included, in the launch configuration the benchmark times and
+with two MMA consumers.
 """
 import numpy as np
 import pytest
@@ -438,30 +437,25 @@ def test_cuda_graph_capture_and_replay(gpu_lib):
         assert_close(D2.cpu().numpy(), oracle.gemm_f16_nt(D1h, C), "graph second")
 
 
-# ------------------------------------------------ full-size, sampled compares --
+# ------------------------------------------------------ full-size compares --
 
-def _sample_indices(n, tile, count, rng):
-    """Tile-border indices (every 4th border, both sides), the two ends, and `count` random ones."""
-    idx = {0, n - 1}
-    for b in range(tile, n, tile * 4):
-        idx.update({b - 1, b})
-    idx.update(rng.choice(n, size=min(n, count), replace=False).tolist())
-    return np.array(sorted(idx))
+def _assert_close_by_rows(got, ref_bits, what, rows_per_chunk=512):
+    """assert_close over whole row bands, so that the float64 temporaries stay small."""
+    for r0 in range(0, got.shape[0], rows_per_chunk):
+        assert_close(got[r0:r0 + rows_per_chunk], ref_bits[r0:r0 + rows_per_chunk], f"{what} rows {r0}..")
 
 
-@pytest.mark.parametrize("consumers", [1, 2], ids=["default", "2consumers"])
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "mlp_proj_8192x28672x4096"])
-def test_full_size_workloads_sampled(gpu_lib, name, consumers):
+def test_full_size_workloads_full(gpu_lib, name):
+    # The whole of D against the whole of the oracle's D, for the default options (the launch
+    # configuration the benchmark times: CTA pairs, 256 x 256 tiles, persistent clusters) and
+    # for the two-consumer variant (512 x 256 tiles).  Every 128 x 128 block of D has its owner
+    # CTA ("TIRx GEMM detailed technical notes", V8 "Output Ownership"), so a full compare covers
+    # every owner, every tile border and the half tiles of the split last wave.
     w = si.WORKLOADS[name]
     A, B = w.operands()
-    # consumers 1: the default options, the launch configuration the benchmark times
-    D = run(gpu_lib, A, B, None if consumers == 1 else gpu_lib.Options(consumers=2))
-    rng = np.random.default_rng(w.seed + 100)
-    rows = _sample_indices(w.M, 128, 40, rng)
-    cols = _sample_indices(w.N, 256, 40, rng)
-    assert_close(D[rows, :], oracle.gemm_f16_nt(A[rows], B), f"{name} rows")
-    assert_close(D[:, cols], oracle.gemm_f16_nt(A, B[cols]), f"{name} cols")
-    pr = rng.integers(0, w.M, size=20000)
-    pc = rng.integers(0, w.N, size=20000)
-    assert_close(D[pr, pc], oracle.gemm_f16_nt_points(A, B, pr, pc), f"{name} points")
-    assert np.isfinite(D.astype(np.float32)).all()
+    ref = oracle.gemm_f16_nt(A, B)  # all host threads; about a minute for the largest shape
+    for consumers in (1, 2):
+        D = run(gpu_lib, A, B, None if consumers == 1 else gpu_lib.Options(consumers=2))
+        assert np.isfinite(D.astype(np.float32)).all()
+        _assert_close_by_rows(D, ref, f"{name} consumers={consumers}")
