@@ -68,6 +68,16 @@ int prepare_kernel(int *max_clusters) {
     cudaError_t e = cudaFuncSetAttribute(gemm_f16_nt_kernel<CG, NC, BN, BM, KS>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC);
     if (e != cudaSuccess) return GEMM_ERR_CUDA;
+    if constexpr (C::REG_SPLIT) {
+        // The register split (setmaxnreg) is sized for a pool of THREADS x REGS_AT_LAUNCH
+        // registers: with fewer per thread, an epilogue warpgroup's increase would wait for
+        // registers that never come.  A build that compiled this kernel otherwise is unusable.
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, gemm_f16_nt_kernel<CG, NC, BN, BM, KS>) != cudaSuccess ||
+            fa.numRegs != C::REGS_AT_LAUNCH) {
+            return GEMM_ERR_CUDA;
+        }
+    }
     cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = launch_config<CG, NC, BN, BM, KS>(dim3(C::CLUSTER, 1, 1), nullptr, attr);
     int n = 0;

@@ -42,8 +42,14 @@
 // columns [256c, 256c + 256); with all 512 columns taken there is no second
 // accumulator buffer, so the next tile waits for the epilogue to drain TMEM.
 // The CTA has three warpgroups: warps 0-1 as above (2-3 idle), warps 4-7
-// drain consumer 0 and warps 8-11 consumer 1.  Its epilogue writes D from
-// registers (the SMEM goes to four 48 KiB stages).
+// drain consumer 0 and warps 8-11 consumer 1.  Registers move between them
+// ("GEMM III", Step 7, setmaxnreg): 384 threads launch with 168 registers
+// each; the producer/MMA warpgroup drops to 40 and the two epilogue
+// warpgroups rise to 232, enough to hold a warp's whole 32 x 256 slice as
+// packed fp16.  So, as in the default kernel, the epilogue reads and rounds
+// its slice, hands TMEM back (the next tile's MMAs start) and only then
+// stages and stores it by TMA, through one 4 KiB buffer per warp beside the
+// four 48 KiB stages.
 //
 // Narrow tiles (BN = 64, CG = 1, NC = 1): for problems whose 128 x 64 tiles fit
 // one wave of CTAs.  Same roles; an 8-stage ring of 24 KiB stages holds a K of
@@ -143,8 +149,7 @@ struct Cfg {
     static_assert(TMEM_COLS == 512 || TMEM_COLS == 128, "a power of two of at least 32 columns");
     static constexpr int EPI_WARPS = 4 * NC;
     static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
-    static constexpr bool EPI_DIRECT = NC == 2;         // store D from registers (one row per lane)
-    static constexpr bool EPI_TMA = !NARROW && NC == 1; // stage in SMEM, store D (or split-K partials) by TMA
+    static constexpr bool EPI_TMA = !NARROW;            // stage in SMEM, store D (or split-K partials) by TMA
     // Narrow and tiny tiles stage each warp's rows in SMEM and read them back
     // so that a warp's store covers whole 128-byte rows of D (coalesced
     // st.global): a row per lane would send 16-byte pieces of 16 or 32
@@ -153,9 +158,25 @@ struct Cfg {
     static constexpr int EPI_N = 64;                    // columns per epilogue chunk
     static constexpr int WARP_ROWS = BLOCK_M / 4;       // rows of D per epilogue warp: the first WARP_ROWS
                                                         // lanes of its TMEM quarter
-    static constexpr int EPI_BUFS = EPI_TMA ? 2 : (EPI_COALESCED ? 1 : 0);
+    // staging buffers per epilogue warp: two (one chunk's TMA store reads one while the next
+    // chunk fills the other), or one with two consumers, whose operand ring leaves room for
+    // no more
+    static constexpr int EPI_BUFS = EPI_TMA ? (NC == 2 ? 1 : 2) : (EPI_COALESCED ? 1 : 0);
     static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+    // Register split of the two-consumer kernel (setmaxnreg).  A CTA's pool is what it
+    // launches with: THREADS x the registers per thread the compiler assigns, at most
+    // REGS_AT_LAUNCH under __launch_bounds__(THREADS, 1).  The host refuses to launch this
+    // kernel unless the compiled count is exactly REGS_AT_LAUNCH, so the split below always
+    // fits the pool and no setmaxnreg.inc can wait for registers that never come.
+    static constexpr bool REG_SPLIT = NC == 2;
+    static constexpr int REGS_AT_LAUNCH = (65536 / THREADS) / 8 * 8;  // 168 for 384 threads
+    static constexpr int REGS_PRODUCER = 40;            // warps 0-3 after the split
+    static constexpr int REGS_EPILOGUE = 232;           // each epilogue warp after the split
+    static_assert(!REG_SPLIT || (EPI_WARP0 == 4 && 32 * EPI_WARP0 * REGS_PRODUCER +
+                                                      32 * EPI_WARPS * REGS_EPILOGUE <=
+                                                  THREADS * REGS_AT_LAUNCH),
+                  "the register split must fit the CTA's pool at launch");
     // Shared-memory layout (offsets from a 1024-byte aligned base; identical
     // in both CTAs of a pair, which the pair MMA relies on).
     static constexpr int OFF_A = 0;
@@ -356,154 +377,163 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
     // global memory).  A, B and D are read and written only after it.
     if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
-    if (warp == 0) {
-        // ---------------------------------------------------- TMA producer
-        if (ptx::elect_one()) {
-            // The producer end starts one phase ahead of the consumer end
-            // ("GEMM III", "The subtlest bug: opposite initial phases").  The
-            // debug flag starts it at phase 0 instead, which blocks every role;
-            // only the tests of the timeout path set it.
-            PipelineState ring(C::STAGES, (p.debug_flags & kDebugProducerPhase0) ? 0u : 1u);
-            uint32_t seq = 0;
-            bool ok = true;
-            bool dependency_met = false;  // griddepcontrol.wait has returned
-            int item = cluster;
-            WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
-                                 p.slices, C::BLOCK_N);
-            if (item < p.num_items) {
-                // Before the wait, only ask L2 for the A and B boxes of the
-                // first ring fill: L2 is where every later load reads them,
-                // and a line the previous kernel still writes is updated
-                // there, so the prefetch changes no value; it moves the HBM
-                // latency of the first k-tiles under the previous kernel's
-                // tail.
-                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
-                const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
-                const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
-                for (int kt = w.kt_begin; kt < kt_end; ++kt) {
+    if (warp < C::EPI_WARP0) {
+        // Warpgroup 0 with two consumers: its producer, its MMA issuer and two idle
+        // warps give registers to the two epilogue warpgroups, all four warps at once.
+        // (The register limit of each role's code then follows from the instruction
+        // that starts its branch.)
+        if constexpr (C::REG_SPLIT) ptx::setmaxnreg_dec<C::REGS_PRODUCER>();
+        if (warp == 0) {
+            // ---------------------------------------------------- TMA producer
+            if (ptx::elect_one()) {
+                // The producer end starts one phase ahead of the consumer end
+                // ("GEMM III", "The subtlest bug: opposite initial phases").  The
+                // debug flag starts it at phase 0 instead, which blocks every role;
+                // only the tests of the timeout path set it.
+                PipelineState ring(C::STAGES, (p.debug_flags & kDebugProducerPhase0) ? 0u : 1u);
+                uint32_t seq = 0;
+                bool ok = true;
+                bool dependency_met = false;  // griddepcontrol.wait has returned
+                int item = cluster;
+                WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
+                                     p.slices, C::BLOCK_N);
+                if (item < p.num_items) {
+                    // Before the wait, only ask L2 for the A and B boxes of the
+                    // first ring fill: L2 is where every later load reads them,
+                    // and a line the previous kernel still writes is updated
+                    // there, so the prefetch changes no value; it moves the HBM
+                    // latency of the first k-tiles under the previous kernel's
+                    // tail.
+                    const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
+                    const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
+                    const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
+                    for (int kt = w.kt_begin; kt < kt_end; ++kt) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        ptx::tma_prefetch_l2_2d(&tmA, kt * C::BLOCK_K, o.a_row + c * C::MMA_M);
+                        for (int c = 0; c < NC; ++c) {
+                            ptx::tma_prefetch_l2_2d(&tmA, kt * C::BLOCK_K, o.a_row + c * C::MMA_M);
+                        }
+                        ptx::tma_prefetch_l2_2d(mapB, kt * C::BLOCK_K, o.b_row);
                     }
-                    ptx::tma_prefetch_l2_2d(mapB, kt * C::BLOCK_K, o.b_row);
                 }
-            }
-            for (; ok && item < p.num_items; item += num_clusters, ++seq) {
-                if (seq > 0) {
-                    w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
-                                p.slices, C::BLOCK_N);
-                }
-                if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag,
-                               kRoleProducer, kCheckItem, seq)) {
-                    ok = false;
-                    break;
-                }
-                const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
-                const bool half = w.n_len < C::BLOCK_N;
-                const CUtensorMap *mapB = half ? &tmBh : &tmB;
-                for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
-                    if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleProducer, kCheckStage,
-                                   seq) ||
-                        !wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
-                                      kRoleProducer, seq)) {
+                for (; ok && item < p.num_items; item += num_clusters, ++seq) {
+                    if (seq > 0) {
+                        w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from, p.k_tiles,
+                                    p.slices, C::BLOCK_N);
+                    }
+                    if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag,
+                                   kRoleProducer, kCheckItem, seq)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t full = bar_full + 8 * ring.stage;
-                    if (leader) ptx::mbar_arrive_expect_tx(full, half ? C::TX_HALF : C::TX_BYTES);
-                    if (!dependency_met) {
-                        // the first load of A or B: the previous kernel of
-                        // the stream must be complete and its writes visible
-                        ptx::griddep_wait();
-                        dependency_met = true;
-                    }
-                    const int32_t k0 = kt * C::BLOCK_K;
-                    if constexpr (CG == 2) {
-                        const uint32_t full_leader = ptx::mapa(full, 0);
-#pragma unroll
-                        for (int c = 0; c < NC; ++c) {  // consumer c's A rows lie c * MMA_M below
-                            ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK, &tmA, full_leader,
-                                                  k0, o.a_row + c * C::MMA_M);
+                    const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
+                    const bool half = w.n_len < C::BLOCK_N;
+                    const CUtensorMap *mapB = half ? &tmBh : &tmB;
+                    for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
+                        if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleProducer, kCheckStage,
+                                       seq) ||
+                            !wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
+                                          kRoleProducer, seq)) {
+                            ok = false;
+                            break;
                         }
-                        ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, mapB, full_leader, k0, o.b_row);
-                    } else {
-                        ptx::tma_load_2d(sA + ring.stage * C::A_STAGE, &tmA, full, k0, o.a_row);
-                        ptx::tma_load_2d(sB + ring.stage * C::B_STAGE, mapB, full, k0, o.b_row);
+                        const uint32_t full = bar_full + 8 * ring.stage;
+                        if (leader) ptx::mbar_arrive_expect_tx(full, half ? C::TX_HALF : C::TX_BYTES);
+                        if (!dependency_met) {
+                            // the first load of A or B: the previous kernel of
+                            // the stream must be complete and its writes visible
+                            ptx::griddep_wait();
+                            dependency_met = true;
+                        }
+                        const int32_t k0 = kt * C::BLOCK_K;
+                        if constexpr (CG == 2) {
+                            const uint32_t full_leader = ptx::mapa(full, 0);
+#pragma unroll
+                            for (int c = 0; c < NC; ++c) {  // consumer c's A rows lie c * MMA_M below
+                                ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK, &tmA, full_leader,
+                                                      k0, o.a_row + c * C::MMA_M);
+                            }
+                            ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, mapB, full_leader, k0, o.b_row);
+                        } else {
+                            ptx::tma_load_2d(sA + ring.stage * C::A_STAGE, &tmA, full, k0, o.a_row);
+                            ptx::tma_load_2d(sB + ring.stage * C::B_STAGE, mapB, full, k0, o.b_row);
+                        }
+                        ring.advance();
                     }
-                    ring.advance();
+                }
+                if (!ok) {
+                    // Give loads already in flight time to land before teardown.
+                    const uint64_t t0 = ptx::globaltimer_ns();
+                    while (ptx::globaltimer_ns() - t0 < 20000) ptx::nanosleep(1000);
                 }
             }
-            if (!ok) {
-                // Give loads already in flight time to land before teardown.
-                const uint64_t t0 = ptx::globaltimer_ns();
-                while (ptx::globaltimer_ns() - t0 < 20000) ptx::nanosleep(1000);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (leader && ptx::elect_one()) {
-            constexpr uint32_t idesc_full = idesc_f16_f32(C::MMA_M, C::BLOCK_N);
-            constexpr uint32_t idesc_half = idesc_f16_f32(C::MMA_M, C::BLOCK_N / 2);
-            constexpr uint16_t pair_mask = CG == 2 ? 0x3 : 0x1;
-            PipelineState ring(C::STAGES, 0u);
-            PipelineState acc(C::ACC_BUFS, 1u);
-            uint32_t seq = 0;
-            bool ok = true;
-            for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
-                const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
-                                           p.k_tiles, p.slices, C::BLOCK_N);
-                const uint32_t idesc = w.n_len < C::BLOCK_N ? idesc_half : idesc_full;
-                if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag, kRoleMma,
-                               kCheckItem, seq) ||
-                    !in_bounds(acc.stage >= 0 && (acc.stage + 1) * NC * C::BLOCK_N <= C::TMEM_COLS, abort_flag,
-                               kRoleMma, kCheckTmem, seq) ||
-                    !wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
-                                  seq)) {
-                    ok = false;
-                    break;
-                }
-                ptx::tcgen05_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * NC * C::BLOCK_N);
-                for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
-                    if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleMma, kCheckStage, seq) ||
-                        !wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
+            __syncwarp();
+        } else if (warp == 1) {
+            // ------------------------------------------------------ MMA issuer
+            if (leader && ptx::elect_one()) {
+                constexpr uint32_t idesc_full = idesc_f16_f32(C::MMA_M, C::BLOCK_N);
+                constexpr uint32_t idesc_half = idesc_f16_f32(C::MMA_M, C::BLOCK_N / 2);
+                constexpr uint16_t pair_mask = CG == 2 ? 0x3 : 0x1;
+                PipelineState ring(C::STAGES, 0u);
+                PipelineState acc(C::ACC_BUFS, 1u);
+                uint32_t seq = 0;
+                bool ok = true;
+                for (int item = cluster; ok && item < p.num_items; item += num_clusters, ++seq) {
+                    const WorkItem w = work_of(item, p.num_m_tiles, p.num_n_tiles, p.raster_group, p.split_from,
+                                               p.k_tiles, p.slices, C::BLOCK_N);
+                    const uint32_t idesc = w.n_len < C::BLOCK_N ? idesc_half : idesc_full;
+                    if (!in_bounds(item_ok(w, p.num_m_tiles, p.num_n_tiles, p.k_tiles, C::BLOCK_N), abort_flag, kRoleMma,
+                                   kCheckItem, seq) ||
+                        !in_bounds(acc.stage >= 0 && (acc.stage + 1) * NC * C::BLOCK_N <= C::TMEM_COLS, abort_flag,
+                                   kRoleMma, kCheckTmem, seq) ||
+                        !wait_bounded(bar_tempty + 8 * acc.stage, acc.phase, abort_flag, p.timeout_ns, kRoleMma,
                                       seq)) {
                         ok = false;
                         break;
                     }
                     ptx::tcgen05_fence_after();
-                    const uint64_t b_desc = ptx::smem_desc_k_sw128(sB + ring.stage * C::B_STAGE);
-#pragma unroll
-                    for (int c = 0; c < NC; ++c) {  // both consumers read the same B stage
-                        const uint64_t a_desc =
-                            ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK);
-#pragma unroll
-                        for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
-                            // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
-                            const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
-                            ptx::mma_f16<CG>(d_tmem + c * C::BLOCK_N, a_desc + koff, b_desc + koff, idesc,
-                                             (kt != w.kt_begin || k != 0) ? 1u : 0u);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * NC * C::BLOCK_N);
+                    for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
+                        if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleMma, kCheckStage, seq) ||
+                            !wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
+                                          seq)) {
+                            ok = false;
+                            break;
                         }
+                        ptx::tcgen05_fence_after();
+                        const uint64_t b_desc = ptx::smem_desc_k_sw128(sB + ring.stage * C::B_STAGE);
+#pragma unroll
+                        for (int c = 0; c < NC; ++c) {  // both consumers read the same B stage
+                            const uint64_t a_desc =
+                                ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK);
+#pragma unroll
+                            for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
+                                // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
+                                const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
+                                ptx::mma_f16<CG>(d_tmem + c * C::BLOCK_N, a_desc + koff, b_desc + koff, idesc,
+                                                 (kt != w.kt_begin || k != 0) ? 1u : 0u);
+                            }
+                        }
+                        ptx::mma_commit<CG>(bar_empty + 8 * ring.stage, pair_mask);  // stage free, both CTAs
+                        ring.advance();
                     }
-                    ptx::mma_commit<CG>(bar_empty + 8 * ring.stage, pair_mask);  // stage free, both CTAs
-                    ring.advance();
+                    if (!ok) break;
+                    ptx::mma_commit<CG>(bar_tfull + 8 * acc.stage, pair_mask);  // accumulator ready, both CTAs
+                    acc.advance();
                 }
-                if (!ok) break;
-                ptx::mma_commit<CG>(bar_tfull + 8 * acc.stage, pair_mask);  // accumulator ready, both CTAs
-                acc.advance();
+                // Wait for every MMA issued so far before TMEM can be released,
+                // also after an abort (then only the time limit ends the wait).
+                ptx::mma_commit<CG>(bar_drain, 0x1);
+                wait_bounded(bar_drain, 0, abort_flag, p.timeout_ns, kRoleMma, 0xFFFFFFFFu, false);
             }
-            // Wait for every MMA issued so far before TMEM can be released,
-            // also after an abort (then only the time limit ends the wait).
-            ptx::mma_commit<CG>(bar_drain, 0x1);
-            wait_bounded(bar_drain, 0, abort_flag, p.timeout_ns, kRoleMma, 0xFFFFFFFFu, false);
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp >= C::EPI_WARP0) {
+    } else {
+        if constexpr (C::REG_SPLIT) ptx::setmaxnreg_inc<C::REGS_EPILOGUE>();
         // -------------------------------------------------------- epilogue
         const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 hold the rows of this warp
         const int consumer = (warp - C::EPI_WARP0) / 4;
-        const uint32_t stage_base = sD + static_cast<uint32_t>(quarter * C::EPI_BUFS * C::EPI_BUF);
+        // this warp's own staging buffers
+        const uint32_t stage_base = sD + static_cast<uint32_t>((warp - C::EPI_WARP0) * C::EPI_BUFS * C::EPI_BUF);
         PipelineState acc(C::ACC_BUFS, 0u);
         uint32_t buf = 0;
         uint32_t seq = 0;
@@ -588,8 +618,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < C::BLOCK_N / C::EPI_N; ++c) {
                         if (c < chunks) {
-                            // The store issued from this buffer two chunks ago
-                            // must have finished reading it.
+                            // The store issued from this buffer EPI_BUFS chunks
+                            // ago must have finished reading it.
                             if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
                             __syncwarp();
                             // Row `lane` of the 32 x 64 staging tile, in the
@@ -612,7 +642,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                                 }
                                 ptx::bulk_commit_group();
                             }
-                            buf ^= 1u;
+                            buf = (buf + 1u) % C::EPI_BUFS;
                         }
                     }
                     acc.advance();
@@ -651,7 +681,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                             }
                             ptx::bulk_commit_group();
                         }
-                        buf ^= 1u;
+                        buf = (buf + 1u) % C::EPI_BUFS;
                     }
                 } else if constexpr (C::KSPLIT) {
                     // K split across the cluster: CTA s adds up and stores
@@ -731,25 +761,6 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                         }
                     }
                     __syncwarp();  // the buffer is rewritten by the next chunk or work item
-                } else {
-                    // Two-consumer variant: row `lane` of this warp, 64
-                    // columns = eight 16-byte stores straight from registers
-                    // (N % 8 == 0, so a 16-byte unit is all in range or all
-                    // out).
-                    uint32_t h[32];
-                    to_f16x2(lo, h);
-                    to_f16x2(hi, h + 16);
-                    const int32_t row = row0 + lane;
-                    const int32_t col = col0 + c * C::EPI_N;
-                    if (lane < C::WARP_ROWS && row < p.M) {
-                        uint16_t *dst = p.D + static_cast<int64_t>(row) * p.N + col;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            if (col + 8 * j < p.N) {
-                                ptx::st_global_v4(dst + 8 * j, h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-                            }
-                        }
-                    }
                 }
             }
             acc.advance();

@@ -69,6 +69,21 @@ __device__ __forceinline__ uint32_t mapa(uint32_t smem_addr, uint32_t rank) {
 
 __device__ __forceinline__ void nanosleep(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
+// Register rebalancing between warpgroups ("GEMM III", Step 7, setmaxnreg): every warp of a
+// warpgroup executes the same instruction.  dec hands the warps' registers above N back to
+// the CTA's pool; inc waits until the pool holds enough to raise each warp to N.  N is a
+// multiple of 8 in [24, 256].
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // Programmatic dependent launch: wait until the grids this one depends on have
 // completed and their memory is visible (a no-op without such a dependency),
 // and let the next grid of the stream start its own set-up early.
