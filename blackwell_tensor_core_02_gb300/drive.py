@@ -1,6 +1,7 @@
-"""Time the GEMM on one shape from the command line (also a fixed workload to profile).
+"""Time the GEMM on one or more shapes from the command line (also a fixed workload to profile).
 
     python -m blackwell_tensor_core_02_gb300.drive --shape 1024,1024,4096 --entry ws --graph --cublas
+    python -m blackwell_tensor_core_02_gb300.drive --shape 1536,1536,1536 2048,2048,2048 --graph --cublas
 
 Operands come from the seeded generator (uniform[-1, 1], seed 1) and rotate
 over enough device copies that one pass exceeds the 129 MB L2.  ``--entry``
@@ -29,7 +30,7 @@ def main(argv=None) -> None:
     import seeded_inputs as si
 
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
-    ap.add_argument("--shape", required=True, help="M,N,K")
+    ap.add_argument("--shape", required=True, nargs="+", help="M,N,K (several: one after the other)")
     ap.add_argument("--entry", choices=["nt", "ws", "static"], default="nt")
     ap.add_argument("--cta-group", type=int, default=0)
     ap.add_argument("--consumers", type=int, default=0)
@@ -44,73 +45,74 @@ def main(argv=None) -> None:
     ap.add_argument("--graph", action="store_true", help="time a CUDA graph of the launches")
     ap.add_argument("--cublas", action="store_true", help="also time torch.matmul on the same rotation")
     args = ap.parse_args(argv)
-    M, N, K = (int(x) for x in args.shape.split(","))
     lib = g.load()
-    dev = torch.device("cuda")
-    A, B = si.custom(M, N, K, seed=1).operands()
-    footprint = 2 * (M * K + N * K + M * N)
-    rot = max(1, min(256, (256 << 20) // max(footprint, 1)))
-    Ar = torch.from_numpy(A).to(dev).unsqueeze(0).repeat(rot, 1, 1)
-    Br = torch.from_numpy(B).to(dev).unsqueeze(0).repeat(rot, 1, 1)
-    Dr = torch.empty((rot, M, N), dtype=torch.float16, device=dev)
-    opts = g.Options(cta_group=args.cta_group, consumers=args.consumers, block_n=args.block_n,
-                     block_m=args.block_m, cluster_k=args.cluster_k, raster_group=args.raster_group)
-    stream = torch.cuda.Stream()
-    sh = stream.cuda_stream
-    need = g.workspace_size(M, N, K, opts) if args.entry == "ws" else 0
-    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    for shape in args.shape:
+        M, N, K = (int(x) for x in shape.split(","))
+        dev = torch.device("cuda")
+        A, B = si.custom(M, N, K, seed=1).operands()
+        footprint = 2 * (M * K + N * K + M * N)
+        rot = max(1, min(256, (256 << 20) // max(footprint, 1)))
+        Ar = torch.from_numpy(A).to(dev).unsqueeze(0).repeat(rot, 1, 1)
+        Br = torch.from_numpy(B).to(dev).unsqueeze(0).repeat(rot, 1, 1)
+        Dr = torch.empty((rot, M, N), dtype=torch.float16, device=dev)
+        opts = g.Options(cta_group=args.cta_group, consumers=args.consumers, block_n=args.block_n,
+                         block_m=args.block_m, cluster_k=args.cluster_k, raster_group=args.raster_group)
+        stream = torch.cuda.Stream()
+        sh = stream.cuda_stream
+        need = g.workspace_size(M, N, K, opts) if args.entry == "ws" else 0
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
 
-    def ours(i):
-        j = i % rot
-        a, b, d = Ar[j].data_ptr(), Br[j].data_ptr(), Dr[j].data_ptr()
-        if args.entry == "ws":
-            rc = g.gemm_f16_nt_ptr(a, b, d, M, N, K, sh, opts, ws.data_ptr(), need)
-        elif args.entry == "static":
-            rc = lib.gemm_f16_nt_static_ws(a, b, d, M, N, K, sh, ctypes.byref(opts))
-        else:
-            rc = g.gemm_f16_nt_ptr(a, b, d, M, N, K, sh, opts)
-        if rc != 0:
-            raise g.GemmError(rc, "drive")
+        def ours(i):
+            j = i % rot
+            a, b, d = Ar[j].data_ptr(), Br[j].data_ptr(), Dr[j].data_ptr()
+            if args.entry == "ws":
+                rc = g.gemm_f16_nt_ptr(a, b, d, M, N, K, sh, opts, ws.data_ptr(), need)
+            elif args.entry == "static":
+                rc = lib.gemm_f16_nt_static_ws(a, b, d, M, N, K, sh, ctypes.byref(opts))
+            else:
+                rc = g.gemm_f16_nt_ptr(a, b, d, M, N, K, sh, opts)
+            if rc != 0:
+                raise g.GemmError(rc, "drive")
 
-    def cublas(i):
-        j = i % rot
-        torch.matmul(Ar[j], Br[j].t(), out=Dr[j])
+        def cublas(i):
+            j = i % rot
+            torch.matmul(Ar[j], Br[j].t(), out=Dr[j])
 
-    runs = [("ours", ours)] + ([("cublas", cublas)] if args.cublas else [])
-    for label, fn in runs:
-        with torch.cuda.stream(stream):
-            for i in range(args.warmup):
-                fn(i)
-        stream.synchronize()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        if args.graph:
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
-                for i in range(args.steps):
-                    fn(i)
+        runs = [("ours", ours)] + ([("cublas", cublas)] if args.cublas else [])
+        for label, fn in runs:
             with torch.cuda.stream(stream):
-                graph.replay()
-                e0.record(stream)
-                graph.replay()
-                e1.record(stream)
-        else:
-            with torch.cuda.stream(stream):
-                e0.record(stream)
-                for i in range(args.steps):
+                for i in range(args.warmup):
                     fn(i)
-                e1.record(stream)
-        e1.synchronize()
-        us = e0.elapsed_time(e1) / args.steps * 1e3
-        status = g.last_device_status(stream)[0]
-        print(json.dumps({"impl": label, "shape": [M, N, K], "entry": args.entry if label == "ours" else None,
-                          "block_n": args.block_n if label == "ours" else None,
-                          "block_m": args.block_m if label == "ours" else None,
-                          "cluster_k": args.cluster_k if label == "ours" else None,
-                          "raster_group": args.raster_group if label == "ours" else None,
-                          "workspace_bytes": need, "us_per_gemm": round(us, 3),
-                          "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 2), "graph": args.graph,
-                          "status": status}), flush=True)
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            if args.graph:
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+                    for i in range(args.steps):
+                        fn(i)
+                with torch.cuda.stream(stream):
+                    graph.replay()
+                    e0.record(stream)
+                    graph.replay()
+                    e1.record(stream)
+            else:
+                with torch.cuda.stream(stream):
+                    e0.record(stream)
+                    for i in range(args.steps):
+                        fn(i)
+                    e1.record(stream)
+            e1.synchronize()
+            us = e0.elapsed_time(e1) / args.steps * 1e3
+            status = g.last_device_status(stream)[0]
+            print(json.dumps({"impl": label, "shape": [M, N, K], "entry": args.entry if label == "ours" else None,
+                              "block_n": args.block_n if label == "ours" else None,
+                              "block_m": args.block_m if label == "ours" else None,
+                              "cluster_k": args.cluster_k if label == "ours" else None,
+                              "raster_group": args.raster_group if label == "ours" else None,
+                              "workspace_bytes": need, "us_per_gemm": round(us, 3),
+                              "tflops": round(2.0 * M * N * K / (us * 1e-6) / 1e12, 2), "graph": args.graph,
+                              "status": status}), flush=True)
 
 
 if __name__ == "__main__":
