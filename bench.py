@@ -470,8 +470,8 @@ def measure_all_workloads(g, dev, peak: float, A3=None, B3=None, budget_s: float
         per_graph = int(min(400, max(10, budget_s / replays / max(w.flop / 1.5e15, 3e-6))))
         cfg = g.describe(w.M, w.N, w.K)
         res = {"workload": name, "M": w.M, "N": w.N, "K": w.K, "steps": per_graph * replays,
-               "kernel": {k: cfg[k] for k in ("cta_group", "block_n", "block_m", "split_k", "cluster_k", "clusters",
-                                              "work_items")},
+               "kernel": {k: cfg[k] for k in ("cta_group", "consumers", "block_n", "block_m", "split_k", "cluster_k",
+                                              "clusters", "work_items")},
                "parity_vs_oracle": parity,
                "rotated_copies": rot,
                "timing": f"CUDA graph of {per_graph} launches, replayed {replays} times; "
@@ -623,7 +623,9 @@ def kernel_label(cfg: dict) -> str:
         if cfg["cluster_k"] > 1:
             kind += f", K over {cfg['cluster_k']} CTAs"
     else:
-        kind = ("pair" if cfg["cta_group"] == 2 else "single") + f" {128 * cfg['cta_group']}x256"
+        kind = ("pair" if cfg["cta_group"] == 2 else "single") + f" {128 * cfg['cta_group'] * cfg['consumers']}x256"
+        if cfg["consumers"] == 2:
+            kind += ", 2 consumers"
     return f"{kind}, {cfg['clusters']} clusters"
 
 

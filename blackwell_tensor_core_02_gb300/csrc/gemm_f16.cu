@@ -191,7 +191,7 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 
 struct Opts {
     int32_t cta_group = 0;  // 0: chosen from the shape (resolve_config)
-    int32_t consumers = 1;
+    int32_t consumers = 0;  // MMA consumers 1 or 2; 0: chosen from the shape (resolve_config)
     int32_t block_n = 0;    // tile width 256 or 64; 0: chosen from the shape (resolve_config)
     int32_t block_m = 0;    // rows per CTA 128 or 64 (64 only with block_n 64); 0: chosen likewise
     int32_t cluster_k = 0;  // narrow / tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 chosen
@@ -206,7 +206,7 @@ struct Opts {
 int parse_options(const gemm_f16_options *opts, Opts *o) {
     if (opts) {
         if (opts->consumers < 0 || opts->consumers > 2) return GEMM_ERR_INVALID_ARG;
-        if (opts->consumers == 2) o->consumers = 2;
+        o->consumers = opts->consumers;
         if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
         if (opts->overlap_launch == -1) o->overlap = false;
         if (opts->cta_group != 0) o->cta_group = opts->cta_group;
@@ -372,7 +372,7 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
     const int64_t k_tiles = (K + 63) / 64;
     if (o->block_n == 0) {
         bool narrow = false;
-        if (o->cta_group == 0 && o->consumers == 1) {
+        if (o->cta_group == 0 && o->consumers != 2) {
             int64_t ctas = dev.max_clusters[3];
             if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
             narrow = ((M + 127) / 128) * ((N + 63) / 64) <= ctas;
@@ -391,11 +391,28 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
     }
     if (o->block_n == 64) {
         o->cta_group = 1;
+        o->consumers = 1;
         small_tiles(M, N, K, dev, o);
         return;
     }
     o->cluster_k = 1;
     o->block_m = 128;
+    if (o->consumers == 0) {
+        // Two MMA consumers (512 x 256 tiles, B staged once for both) move a quarter fewer
+        // operand bytes from L2 per FLOP and draw less power per clock, so under the power cap
+        // they run faster; but with one accumulator per consumer the MMA waits for the
+        // epilogue's TMEM reads at every tile, which only a long K-loop amortises.  Measured on
+        // GB300 (graph-timed, ~1.2 s windows at the power cap, TFLOP/s, two consumers vs one):
+        // K >= 6144 gains: 4096x4096x8192 1562 vs 1524, 6144^3 1613 vs 1587, 8192^3 1642 vs 1597,
+        // 12288^3 1626 vs 1582, 8192x8192x16384 1638 vs 1568, 16384x8192x8192 1648 vs 1626;
+        // K <= 4096 loses: 4096^3 1535 vs 1564, 8192x8192x4096 1628 vs 1643,
+        // 8192x28672x4096 1662 vs 1677, 8192x8192x2048 1575 vs 1603.  So: two consumers from
+        // 96 K tiles of 64 on, when their tiles fill at least one wave of co-resident pairs.
+        int64_t pairs = dev.max_clusters[2];
+        if (o->max_clusters > 0 && o->max_clusters < pairs) pairs = o->max_clusters;
+        const int64_t tiles2 = ((M + 511) / 512) * ((N + 255) / 256);
+        o->consumers = (o->cta_group != 1 && k_tiles >= 96 && tiles2 >= pairs) ? 2 : 1;
+    }
     if (o->cta_group != 0) return;
     if (o->consumers == 2) {
         o->cta_group = 2;
@@ -703,7 +720,7 @@ int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f
     if (st != GEMM_OK) return st;
     Plan plan;
     resolve_config(M, N, K, *info, true, &o);
-    if (o.block_n == 64) return 0;  // narrow tiles never split K
+    if (o.block_n == 64 || o.consumers == 2) return 0;  // narrow tiles and two consumers never split K
     st = o.cta_group == 2 ? make_plan<2, 1, 256>(M, N, K, *info, o, true, &plan)
                           : make_plan<1, 1, 256>(M, N, K, *info, o, true, &plan);
     if (st != GEMM_OK) return st;

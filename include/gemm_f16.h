@@ -70,7 +70,7 @@ typedef enum gemm_status {
  *                 cta_group 2); 0 = as many as are co-resident on the device.
  *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes
  *                 V6, "l2_group_size"); 0 = chosen from the shape: the largest
- *                 group whose A panel (group x 128*cta_group rows x K fp16)
+ *                 group whose A panel (group x the tile's rows x K fp16)
  *                 fits in 32 MiB, between 1 and the number of M-tiles.
  *   debug_flags   test hook, 0 in normal use.  1 starts the producer end of
  *                 the SMEM ring at phase 0 instead of 1 -- the pages' "subtlest
@@ -85,19 +85,29 @@ typedef enum gemm_status {
  *                 tail; the kernel still waits for it to finish, and for its
  *                 writes to be visible, before it reads A or B or writes D.
  *                 -1: an ordinary launch.  Other values: GEMM_ERR_INVALID_ARG.
- *   consumers     0 or 1 (default): one MMA consumer per CTA pair, 256 x 256
- *                 tiles, two accumulator buffers in tensor memory so the
- *                 epilogue overlaps the next tile.  2 (needs cta_group 2):
- *                 two consumers share each staged B tile, 512 x 256 tiles
+ *   consumers     1: one MMA consumer per CTA pair, 256 x 256 tiles, two
+ *                 accumulator buffers in tensor memory so the epilogue
+ *                 overlaps the next tile.  2 (needs cta_group 0 or 2): two
+ *                 consumers share each staged B tile, 512 x 256 tiles
  *                 ("GEMM III", Step 9; TIRx notes V9), one accumulator per
- *                 consumer.  Other values: GEMM_ERR_INVALID_ARG.
+ *                 consumer, registers moved from the producer and MMA warps
+ *                 to the epilogue warps (Step 7, setmaxnreg) so the
+ *                 accumulator goes back to the MMA before D is stored.
+ *                 0 (default): 2 when the K-loop is at least 96 tiles of 64
+ *                 and the 512 x 256 tiles fill at least one wave of
+ *                 co-resident pairs (and cta_group is not 1, block_n not
+ *                 64), else 1: a long K-loop amortises the wait for the
+ *                 epilogue at every tile, and the shared B tile moves a
+ *                 quarter fewer operand bytes, which under the power cap
+ *                 buys clock.  Other values: GEMM_ERR_INVALID_ARG.
  *   block_n       tile width in columns of D.  256: the tiles above.  64
  *                 (needs cta_group 0 or 1 and one consumer): single CTAs
  *                 with 128 x 64 tiles and an 8-stage ring (all of a K up to
  *                 512 in flight after one load latency), D stored by
  *                 coalesced warp stores; for small, latency-bound problems.  Not on
  *                 the pages: they fix the tile at 128 or 256 x 256.  0
- *                 (default): 64 when cta_group is 0, the K-loop is at most 8
+ *                 (default): 64 when cta_group is 0, consumers is not 2, the
+ *                 K-loop is at most 8
  *                 tiles of 64 and the 128 x 64 tiles fit one wave of
  *                 co-resident CTAs, else 256.  Other values:
  *                 GEMM_ERR_INVALID_ARG.

@@ -529,17 +529,45 @@ NO_SPLIT = GB300[:5] + [0] * 6                         # one that cannot co-sche
 
 def test_describe_for_the_five_workloads_on_gb300():
     expect = {
-        (128, 128, 64): dict(cta_group=1, block_n=64, block_m=64, cluster_k=1, clusters=4, work_items=4),
-        (256, 256, 512): dict(cta_group=1, block_n=64, block_m=64, cluster_k=4, clusters=16, work_items=64),
-        (4096, 4096, 4096): dict(cta_group=2, block_n=256, block_m=128, cluster_k=1, clusters=76, work_items=284),
-        (8192, 8192, 8192): dict(cta_group=2, block_n=256, block_m=128, cluster_k=1, clusters=76, work_items=1060),
-        (8192, 28672, 4096): dict(cta_group=2, block_n=256, block_m=128, cluster_k=1, clusters=76,
+        (128, 128, 64): dict(cta_group=1, consumers=1, block_n=64, block_m=64, cluster_k=1, clusters=4,
+                             work_items=4),
+        (256, 256, 512): dict(cta_group=1, consumers=1, block_n=64, block_m=64, cluster_k=4, clusters=16,
+                              work_items=64),
+        (4096, 4096, 4096): dict(cta_group=2, consumers=1, block_n=256, block_m=128, cluster_k=1, clusters=76,
+                                 work_items=284),
+        # K = 8192: two consumers, 512 x 256 tiles (16 x 32 = 512 on 76 pairs; the last wave is
+        # 56 tiles, more than half of 76, so nothing is split)
+        (8192, 8192, 8192): dict(cta_group=2, consumers=2, block_n=256, block_m=128, cluster_k=1, clusters=76,
+                                 work_items=512),
+        (8192, 28672, 4096): dict(cta_group=2, consumers=1, block_n=256, block_m=128, cluster_k=1, clusters=76,
                                   work_items=3596),
     }
     for (M, N, K), want in expect.items():
         got = g.describe_for(M, N, K, GB300)
         assert {k: got[k] for k in want} == want, (M, N, K)
         assert got["split_k"] == 1 and got["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("M,N,K,consumers", [
+    (4096, 4096, 8192, 2), (6144, 6144, 6144, 2), (8192, 8192, 8192, 2), (12288, 12288, 12288, 2),
+    (8192, 8192, 16384, 2), (16384, 8192, 8192, 2),
+    (4096, 4096, 4096, 1), (8192, 8192, 4096, 1), (8192, 28672, 4096, 1), (8192, 8192, 2048, 1),
+    (3072, 3072, 3072, 1),
+    # 96 K tiles but 4 x 8 = 32 two-consumer tiles, fewer than one wave of 76 pairs
+    (2048, 2048, 6144, 1),
+])
+def test_describe_for_the_consumer_count_rule(M, N, K, consumers):
+    """Two MMA consumers from 96 K tiles of 64 on, when their 512 x 256 tiles fill a wave of
+    pairs; given options are kept."""
+    c = g.describe_for(M, N, K, GB300)
+    assert (c["cta_group"], c["consumers"], c["block_n"], c["split_k"]) == (2, consumers, 256, 1)
+    assert c["work_items"] >= -(-M // (256 * consumers)) * -(-N // 256)
+    assert g.describe_for(M, N, K, GB300, g.Options(consumers=1))["consumers"] == 1
+    assert g.describe_for(M, N, K, GB300, g.Options(consumers=2))["consumers"] == 2
+    single = g.describe_for(M, N, K, GB300, g.Options(cta_group=1))
+    assert (single["cta_group"], single["consumers"]) == (1, 1)
+    # a grid capped below the tile count still counts as a full wave
+    assert g.describe_for(M, N, K, GB300, g.Options(max_clusters=8))["consumers"] == (2 if K >= 6144 else 1)
 
 
 @pytest.mark.parametrize("M,N,K,bm,ks", [

@@ -448,14 +448,15 @@ def _assert_close_by_rows(got, ref_bits, what, rows_per_chunk=512):
 @pytest.mark.parametrize("name", ["square_4096", "square_8192", "mlp_proj_8192x28672x4096"])
 def test_full_size_workloads_full(gpu_lib, name):
     # The whole of D against the whole of the oracle's D, for the default options (the launch
-    # configuration the benchmark times: CTA pairs, 256 x 256 tiles, persistent clusters) and
-    # for the two-consumer variant (512 x 256 tiles).  Every 128 x 128 block of D has its owner
+    # configuration the benchmark times: persistent CTA pairs with one MMA consumer and 256 x 256
+    # tiles, or two consumers and 512 x 256 tiles with a long K) and for the other consumer count.  Every 128 x 128 block of D has its owner
     # CTA ("TIRx GEMM detailed technical notes", V8 "Output Ownership"), so a full compare covers
     # every owner, every tile border and the half tiles of the split last wave.
     w = si.WORKLOADS[name]
     A, B = w.operands()
     ref = oracle.gemm_f16_nt(A, B)  # all host threads; about a minute for the largest shape
-    for consumers in (1, 2):
-        D = run(gpu_lib, A, B, None if consumers == 1 else gpu_lib.Options(consumers=2))
+    default = gpu_lib.describe(w.M, w.N, w.K)["consumers"]
+    for options in (None, gpu_lib.Options(consumers=3 - default)):  # the default, then the other count
+        D = run(gpu_lib, A, B, options)
         assert np.isfinite(D.astype(np.float32)).all()
-        _assert_close_by_rows(D, ref, f"{name} consumers={consumers}")
+        _assert_close_by_rows(D, ref, f"{name} consumers={default if options is None else 3 - default}")
