@@ -473,7 +473,9 @@ def measure_sustained(g, dev, A, B, local: int, seconds: float, with_cublas: boo
 
 def kernel_label(cfg: dict) -> str:
     """A short name for the configuration gemm_f16_nt_describe reports."""
-    if cfg["block_n"] == 64:
+    if cfg["block_n"] == 16:
+        kind = "thin 64x16"
+    elif cfg["block_n"] == 64:
         kind = f"{'tiny' if cfg['block_m'] == 64 else 'narrow'} {cfg['block_m']}x64"
         if cfg["cluster_k"] > 1:
             kind += f", K over {cfg['cluster_k']} CTAs"

@@ -114,6 +114,11 @@ int device_setup(int *dev_out, DeviceInfo **info_out) {
             if (d.status == GEMM_OK) d.status = prepare_kernel<2, 2, 256>(&d.max_clusters[2]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64>(&d.max_clusters[3]);
             if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 64, 64>(&d.max_clusters[4]);
+            // thin 64 x 16 tiles use the tiny tiles' co-resident count (their shared
+            // memory is smaller, so at least as many fit; checked here)
+            int thin = 0;
+            if (d.status == GEMM_OK) d.status = prepare_kernel<1, 1, 16, 64>(&thin);
+            if (d.status == GEMM_OK && thin < d.max_clusters[4]) d.status = GEMM_ERR_CUDA;
             // The K splits across clusters are optional: a device that cannot
             // co-schedule clusters of that size (0 co-resident) never takes them.
             if (d.status == GEMM_OK && prepare_kernel<1, 1, 64, 64, 2>(&d.max_clusters[5]) != GEMM_OK) {
@@ -192,7 +197,7 @@ bool shape_ok(int64_t M, int64_t N, int64_t K) {
 struct Opts {
     int32_t cta_group = 0;  // 0: chosen from the shape (resolve_config)
     int32_t consumers = 0;  // MMA consumers 1 or 2; 0: chosen from the shape (resolve_config)
-    int32_t block_n = 0;    // tile width 256 or 64; 0: chosen from the shape (resolve_config)
+    int32_t block_n = 0;    // tile width 256, 64 or 16; 0: chosen from the shape (resolve_config)
     int32_t block_m = 0;    // rows per CTA 128 or 64 (64 only with block_n 64); 0: chosen likewise
     int32_t cluster_k = 0;  // narrow / tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 chosen
                             // likewise
@@ -210,7 +215,9 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
         if (opts->overlap_launch < -1 || opts->overlap_launch > 1) return GEMM_ERR_INVALID_ARG;
         if (opts->overlap_launch == -1) o->overlap = false;
         if (opts->cta_group != 0) o->cta_group = opts->cta_group;
-        if (opts->block_n != 0 && opts->block_n != 64 && opts->block_n != 256) return GEMM_ERR_INVALID_ARG;
+        if (opts->block_n != 0 && opts->block_n != 16 && opts->block_n != 64 && opts->block_n != 256) {
+            return GEMM_ERR_INVALID_ARG;
+        }
         o->block_n = opts->block_n;
         if (opts->block_m != 0 && opts->block_m != 64 && opts->block_m != 128) return GEMM_ERR_INVALID_ARG;
         o->block_m = opts->block_m;
@@ -230,6 +237,15 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     }
     if (o->cta_group != 0 && o->cta_group != 1 && o->cta_group != 2) return GEMM_ERR_INVALID_ARG;
     if (o->consumers == 2 && o->cta_group == 1) return GEMM_ERR_INVALID_ARG;
+    if (o->block_n == 16) {
+        // thin tiles: 64 rows, one CTA, one consumer, no K split
+        if (o->block_m == 128 || o->cluster_k > 1 || o->cta_group == 2 || o->consumers == 2) {
+            return GEMM_ERR_INVALID_ARG;
+        }
+        o->block_m = 64;
+        o->cluster_k = 1;
+        return GEMM_OK;
+    }
     if (o->cluster_k > 1) {
         // the K split runs on 64-wide tiles: tiny ones unless 128 rows are asked for
         if (o->block_n == 256) return GEMM_ERR_INVALID_ARG;
@@ -238,7 +254,7 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
     }
     if (o->block_m == 64) {
         if (o->block_n == 256) return GEMM_ERR_INVALID_ARG;
-        o->block_n = 64;  // 64-row tiles are 64 wide
+        o->block_n = 64;  // 64-row tiles are 64 wide (or 16, the thin tiles above)
     }
     if (o->block_n == 64 && (o->cta_group == 2 || o->consumers == 2)) return GEMM_ERR_INVALID_ARG;
     return GEMM_OK;
@@ -370,6 +386,13 @@ bool cluster_k_applies(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, c
 //   (1024x1024x512 5.21 vs 4.28).
 void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool allow_splitk, Opts *o) {
     const int64_t k_tiles = (K + 63) / 64;
+    // tile shape left to the library entirely (the thin tiles below are only chosen then)
+    const bool auto_tile = o->block_n == 0 && o->block_m == 0 && o->cluster_k == 0;
+    if (o->block_n == 16) {
+        o->cta_group = 1;
+        o->consumers = 1;
+        return;
+    }
     if (o->block_n == 0) {
         bool narrow = false;
         if (o->cta_group == 0 && o->consumers != 2) {
@@ -393,6 +416,21 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
         o->cta_group = 1;
         o->consumers = 1;
         small_tiles(M, N, K, dev, o);
+        // Thin 64 x 16 tiles for the shortest of these problems: where the tiny tiles
+        // apply with a K of at most 512 (8 K tiles) and the thin tiles still fit one
+        // wave, each CTA loads and drains a quarter as much.  Measured on GB300
+        // (graph-timed, us, thin vs the default before them): 128x128x64 1.57 vs 1.76,
+        // 128x256x256 2.05 vs 2.24, 256x256x512 2.78 vs 2.88 (tiny tiles with K over
+        // 4-CTA clusters); with a longer K the cluster K split wins (256x128x1024 3.96
+        // vs 3.22), past one wave the tiny tiles (512x512x512 4.57 vs 2.85).  64 x 8
+        // tiles gained nothing more (1.60 and 2.90), 64 x 32 less (1.74 and 2.83).
+        int64_t ctas = dev.max_clusters[4];
+        if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
+        const int64_t thin_tiles = ((M + 63) / 64) * ((N + 15) / 16);
+        if (auto_tile && o->block_m == 64 && k_tiles <= 8 && thin_tiles <= ctas) {
+            o->block_n = 16;
+            o->cluster_k = 1;
+        }
         return;
     }
     o->cluster_k = 1;
@@ -592,6 +630,7 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (K == 0) return zero_fill(D, M, N, s);
     resolve_config(M, N, K, *info, workspace != nullptr, &o);
+    if (o.block_n == 16) return launch<1, 1, 16, 64>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
     if (o.block_n == 64 && o.block_m == 64) {
         switch (o.cluster_k) {
             case 2: return launch<1, 1, 64, 64, 2>(A, B, D, M, N, K, s, *info, o, nullptr, 0);
@@ -621,7 +660,10 @@ int describe_with(const DeviceInfo &info, Opts o, int64_t M, int64_t N, int64_t 
     resolve_config(M, N, K, info, ws, &o);
     Plan plan;
     int stages = 0;
-    if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 2) {
+    if (o.block_n == 16) {
+        st = make_plan<1, 1, 16, 64>(M, N, K, info, o, false, &plan);
+        stages = Cfg<1, 1, 16, 64>::STAGES;
+    } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 2) {
         st = make_plan<1, 1, 64, 64, 2>(M, N, K, info, o, false, &plan);
         stages = Cfg<1, 1, 64, 64, 2>::STAGES;
     } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 4) {
@@ -720,7 +762,7 @@ int64_t gemm_f16_nt_workspace_size(int64_t M, int64_t N, int64_t K, const gemm_f
     if (st != GEMM_OK) return st;
     Plan plan;
     resolve_config(M, N, K, *info, true, &o);
-    if (o.block_n == 64 || o.consumers == 2) return 0;  // narrow tiles and two consumers never split K
+    if (o.block_n != 256 || o.consumers == 2) return 0;  // narrow, tiny, thin tiles and two consumers never split K
     st = o.cta_group == 2 ? make_plan<2, 1, 256>(M, N, K, *info, o, true, &plan)
                           : make_plan<1, 1, 256>(M, N, K, *info, o, true, &plan);
     if (st != GEMM_OK) return st;
@@ -825,14 +867,14 @@ const char *gemm_f16_status_string(int status) {
 int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int32_t consumers, int32_t block_n,
                          int32_t block_m, int32_t raster_group, int32_t split_k, int64_t num_clusters,
                          int64_t cluster_id, int64_t iter, gemm_f16_work_item *out) {
-    if (block_m == 0) block_m = 128;
+    if (block_m == 0) block_m = block_n == 16 ? 64 : 128;
     if (block_n == 0) block_n = block_m == 64 ? 64 : 256;
-    if (cta_group == 0) cta_group = block_n == 64 ? 1 : 2;
+    if (cta_group == 0) cta_group = block_n == 256 ? 2 : 1;
     if (consumers == 0) consumers = 1;
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
-        (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
-        (block_n == 64 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
-        (block_m == 64 && block_n != 64) || raster_group < 0 ||
+        (consumers == 2 && cta_group != 2) || (block_n != 16 && block_n != 64 && block_n != 256) ||
+        (block_n != 256 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
+        (block_m == 64 && block_n == 256) || (block_n == 16 && block_m != 64) || raster_group < 0 ||
         (split_k != 0 && split_k != 1 && split_k != 2 && split_k != 4 && split_k != 8) ||
         (split_k > 1 && block_n != 64) || K < 0 ||
         K > kDimLimit || M <= 0 || N <= 0 || M > kDimLimit || N > kDimLimit || num_clusters <= 0 ||
@@ -845,7 +887,7 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
     if (tiles > kDimLimit / 16) return GEMM_ERR_INVALID_ARG;
     const int32_t k_tiles = static_cast<int32_t>((K + 63) / 64);
     if (raster_group == 0) raster_group = auto_raster_group(static_cast<int32_t>(num_m), K, static_cast<int32_t>(tile_m));
-    const bool narrow = block_n == 64;
+    const bool narrow = block_n != 256;
     int32_t slices = 1;
     if (split_k > 1) {
         // narrow or tiny tiles with K split across clusters of split_k CTAs (cluster_k)
@@ -881,16 +923,17 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
 int gemm_f16_nt_cta_origin(int32_t cta_group, int32_t consumers, int32_t block_n, int32_t block_m, int64_t m_idx,
                            int64_t n_idx, int64_t n_off, int64_t n_len, int32_t rank, int64_t *a_row, int64_t *b_row,
                            int64_t *d_row, int64_t *d_col) {
-    if (block_m == 0) block_m = 128;
+    if (block_m == 0) block_m = block_n == 16 ? 64 : 128;
     if (block_n == 0) block_n = block_m == 64 ? 64 : 256;
-    if (cta_group == 0) cta_group = block_n == 64 ? 1 : 2;
+    if (cta_group == 0) cta_group = block_n == 256 ? 2 : 1;
     if (consumers == 0) consumers = 1;
-    const bool lens_ok = block_n == 64 ? (n_len == 64 && n_off == 0)
-                                       : ((n_len == 256 && n_off == 0) || (n_len == 128 && (n_off == 0 || n_off == 128)));
+    const bool lens_ok = block_n != 256 ? (n_len == block_n && n_off == 0)
+                                        : ((n_len == 256 && n_off == 0) || (n_len == 128 && (n_off == 0 || n_off == 128)));
     if ((cta_group != 1 && cta_group != 2) || (consumers != 1 && consumers != 2) ||
-        (consumers == 2 && cta_group != 2) || (block_n != 64 && block_n != 256) ||
-        (block_n == 64 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
-        (block_m == 64 && block_n != 64) || rank < 0 || rank >= cta_group || m_idx < 0 || n_idx < 0 ||
+        (consumers == 2 && cta_group != 2) || (block_n != 16 && block_n != 64 && block_n != 256) ||
+        (block_n != 256 && (cta_group != 1 || consumers != 1)) || (block_m != 64 && block_m != 128) ||
+        (block_m == 64 && block_n == 256) || (block_n == 16 && block_m != 64) || rank < 0 || rank >= cta_group ||
+        m_idx < 0 || n_idx < 0 ||
         m_idx * block_m * cta_group * consumers > kDimLimit || n_idx * block_n > kDimLimit || !lens_ok ||
         !a_row || !b_row || !d_row || !d_col) {
         return GEMM_ERR_INVALID_ARG;

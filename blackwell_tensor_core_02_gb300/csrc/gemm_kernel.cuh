@@ -63,6 +63,13 @@
 // quarter of TMEM (row r in lane 32 * (r / 16) + r % 16), so each epilogue
 // warp reads its quarter as usual and stores 16 rows from its lanes 0-15.
 //
+// Thin tiles (BM = 64, BN = 16): the tiny tiles cut four times finer along N
+// for the shortest problems, MMAs of M = 64, N = 16, two 16-column
+// accumulators in the smallest TMEM allocation (32 columns), and an epilogue
+// that stores each row's 32 bytes straight from registers.  Each CTA then
+// loads and drains a quarter as much per tile, which shortens the one pass
+// of the data path such a problem is.
+//
 // K split across a cluster (KS = 2, 4, 8; narrow and tiny tiles): KS CTAs own
 // one tile, CTA s runs K slice s, and the copy engine moves each CTA's fp32
 // sums to the CTA that owns those rows, which adds the KS slices in order,
@@ -120,15 +127,18 @@ template <int CG, int NC, int BN = 256, int BM = 128, int KS = 1>
 struct Cfg {
     static_assert(CG == 1 || CG == 2, "cta_group is 1 or 2");
     static_assert(NC == 1 || (NC == 2 && CG == 2), "two consumers need a CTA pair");
-    static_assert(BN == 256 || (BN == 64 && CG == 1 && NC == 1), "narrow tiles are single-CTA, one consumer");
-    static_assert(BM == 128 || (BM == 64 && BN == 64), "64-row tiles are narrow");
+    static_assert(BN == 256 || ((BN == 64 || BN == 16) && CG == 1 && NC == 1), "narrow tiles are single-CTA, one consumer");
+    static_assert(BM == 128 || (BM == 64 && BN <= 64), "64-row tiles are narrow");
+    static_assert(BN != 16 || (BM == 64 && KS == 1), "thin tiles are 64 x 16, without a K split");
     static_assert(KS == 1 || ((KS == 2 || KS == 4 || KS == 8) && BN == 64), "a K split over 2, 4 or 8 narrow or tiny CTAs");
     static constexpr bool NARROW = BN != 256;
     static constexpr bool TINY = BM == 64;
+    static constexpr bool THIN = BN == 16;
     static constexpr bool KSPLIT = KS > 1;
     static constexpr int CLUSTER = CG * KS;             // CTAs per cluster
     // co-resident cluster count slot of this configuration in the host's
-    // per-device table
+    // per-device table (thin tiles share the tiny tiles' slot: they need less
+    // shared memory, and the host checks that at least as many fit)
     static constexpr int KIND = KSPLIT ? (KS == 2 ? 5 : (KS == 4 ? 6 : 7)) + (TINY ? 0 : 3)
                                        : (TINY ? 4 : (NARROW ? 3 : (CG == 1 ? 0 : NC)));
     static constexpr int BLOCK_M = BM;                  // rows of D per CTA and consumer
@@ -145,8 +155,8 @@ struct Cfg {
     static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
     static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
-    static constexpr int TMEM_COLS = ACC_BUFS * NC * BLOCK_N;           // 512 (all of TMEM) or 128
-    static_assert(TMEM_COLS == 512 || TMEM_COLS == 128, "a power of two of at least 32 columns");
+    static constexpr int TMEM_COLS = ACC_BUFS * NC * BLOCK_N;           // 512 (all of TMEM), 128 or 32
+    static_assert(TMEM_COLS == 512 || TMEM_COLS == 128 || TMEM_COLS == 32, "a power of two of at least 32 columns");
     static constexpr int EPI_WARPS = 4 * NC;
     static constexpr int EPI_WARP0 = NC == 2 ? 4 : 2;   // first epilogue warp (a warpgroup boundary for NC 2)
     static constexpr bool EPI_TMA = !NARROW;            // stage in SMEM, store D (or split-K partials) by TMA
@@ -154,15 +164,15 @@ struct Cfg {
     // so that a warp's store covers whole 128-byte rows of D (coalesced
     // st.global): a row per lane would send 16-byte pieces of 16 or 32
     // different rows per store instruction.
-    static constexpr bool EPI_COALESCED = NARROW;
-    static constexpr int EPI_N = 64;                    // columns per epilogue chunk
+    static constexpr bool EPI_COALESCED = NARROW && !THIN;
+    static constexpr int EPI_N = THIN ? 16 : 64;        // columns per epilogue chunk
     static constexpr int WARP_ROWS = BLOCK_M / 4;       // rows of D per epilogue warp: the first WARP_ROWS
                                                         // lanes of its TMEM quarter
     // staging buffers per epilogue warp: two (one chunk's TMA store reads one while the next
     // chunk fills the other), or one with two consumers, whose operand ring leaves room for
     // no more
     static constexpr int EPI_BUFS = EPI_TMA ? (NC == 2 ? 1 : 2) : (EPI_COALESCED ? 1 : 0);
-    static constexpr int EPI_BUF = 32 * EPI_N * 2;      // one warp's 32 rows x 64 fp16 = 4 KiB
+    static constexpr int EPI_BUF = 32 * 64 * 2;         // one warp's 32 rows x 64 fp16 = 4 KiB
     static constexpr int THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
     // Register split of the two-consumer kernel (setmaxnreg).  A CTA's pool is what it
     // launches with: THREADS x the registers per thread the compiler assigns, at most
@@ -649,118 +659,144 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     continue;
                 }
             }
-#pragma unroll 1
-            for (int c = 0; c < chunks; ++c) {
-                uint32_t lo[32], hi[32];
-                ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N, lo);
-                ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
+            if constexpr (C::THIN) {
+                // Thin tiles: one 16-column chunk.  Lane r of the warp holds row r of
+                // its 16 rows (lanes 0-15 of its TMEM quarter); the 32 bytes of that
+                // row go to D in two 16-byte stores straight from registers.
+                uint32_t v[16];
+                ptx::tmem_ld_32x32b_x16(taddr, v);
                 ptx::tmem_wait_ld();
-                if (c == chunks - 1) release_tmem();
-                if constexpr (C::EPI_TMA) {
-                    // Split-K: this slice's fp32 partial sums go to the
-                    // workspace [slice][M][N] as two 32 x 32 fp32 boxes per
-                    // chunk (128-byte rows, the same swizzled staging as the
-                    // fp16 path; the 3-D map clips each slice at its own M).
+                release_tmem();
+                uint32_t h[8];
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t *v = half ? hi : lo;
-                        if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
-                        __syncwarp();
-                        const uint32_t row_addr = stage_base + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+                for (int j = 0; j < 8; ++j) {
+                    const __half2 t = __floats2half2_rn(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                    h[j] = *reinterpret_cast<const uint32_t *>(&t);
+                }
+                const int32_t row = row0 + lane;
+                if (lane < C::WARP_ROWS && row < p.M) {
+                    uint16_t *dst = p.D + static_cast<int64_t>(row) * p.N + col0;
+                    // N % 8 == 0: a 16-byte unit is all in range or all out
+                    if (col0 < p.N) ptx::st_global_v4(dst, h[0], h[1], h[2], h[3]);
+                    if (col0 + 8 < p.N) ptx::st_global_v4(dst + 8, h[4], h[5], h[6], h[7]);
+                }
+                acc.advance();
+                continue;
+            }
+            if constexpr (!C::THIN) {  // (thin tiles finished their item above)
+#pragma unroll 1
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t lo[32], hi[32];
+                    ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N, lo);
+                    ptx::tmem_ld_32x32b_x32(taddr + c * C::EPI_N + 32, hi);
+                    ptx::tmem_wait_ld();
+                    if (c == chunks - 1) release_tmem();
+                    if constexpr (C::EPI_TMA) {
+                        // Split-K: this slice's fp32 partial sums go to the
+                        // workspace [slice][M][N] as two 32 x 32 fp32 boxes per
+                        // chunk (128-byte rows, the same swizzled staging as the
+                        // fp16 path; the 3-D map clips each slice at its own M).
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
-                            ptx::st_shared_v4(row_addr + unit * 16u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                        }
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int32_t col = col0 + c * C::EPI_N + 32 * half;
-                            if (row0 < p.M && col < p.N) {
-                                ptx::tma_store_3d(&tmP, stage_base + buf * C::EPI_BUF, col, row0, w.slice);
+                        for (int half = 0; half < 2; ++half) {
+                            const uint32_t *v = half ? hi : lo;
+                            if (lane == 0) ptx::bulk_wait_group_read<C::EPI_BUFS - 1>();
+                            __syncwarp();
+                            const uint32_t row_addr = stage_base + buf * C::EPI_BUF + static_cast<uint32_t>(lane) * 128u;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
+                                ptx::st_shared_v4(row_addr + unit * 16u, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                             }
-                            ptx::bulk_commit_group();
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                const int32_t col = col0 + c * C::EPI_N + 32 * half;
+                                if (row0 < p.M && col < p.N) {
+                                    ptx::tma_store_3d(&tmP, stage_base + buf * C::EPI_BUF, col, row0, w.slice);
+                                }
+                                ptx::bulk_commit_group();
+                            }
+                            buf = (buf + 1u) % C::EPI_BUFS;
                         }
-                        buf = (buf + 1u) % C::EPI_BUFS;
-                    }
-                } else if constexpr (C::KSPLIT) {
-                    // K split across the cluster: CTA s adds up and stores
-                    // rows [s * KS_ROWS, (s + 1) * KS_ROWS) of the tile.
-                    // Lane r writes its row R's fp32 sums over this CTA's K
-                    // slice, chunk c at 16-byte units 16c .. 16c + 15, to row
-                    // R of the CTA's source buffer (KS_ROW_BYTES, unit u at
-                    // u ^ (R % 8): no bank conflicts).  After the last chunk
-                    // one lane copies the warp's rows, by the copy engine, to
-                    // slots krank * KS_ROWS + R % KS_ROWS of each owner's
-                    // receive region (the same swizzle, as KS_ROWS is a
-                    // multiple of 8), counted in bytes on its receive barrier.
-                    const uint32_t src = base + C::OFF_SRC;
-                    if (lane < C::WARP_ROWS) {
-                        const uint32_t R = static_cast<uint32_t>(quarter * C::WARP_ROWS + lane);
-                        const uint32_t row_addr = src + R * C::KS_ROW_BYTES;
-                        const uint32_t sw = R & 7u;
-                        const uint32_t u0 = 16u * static_cast<uint32_t>(c);
+                    } else if constexpr (C::KSPLIT) {
+                        // K split across the cluster: CTA s adds up and stores
+                        // rows [s * KS_ROWS, (s + 1) * KS_ROWS) of the tile.
+                        // Lane r writes its row R's fp32 sums over this CTA's K
+                        // slice, chunk c at 16-byte units 16c .. 16c + 15, to row
+                        // R of the CTA's source buffer (KS_ROW_BYTES, unit u at
+                        // u ^ (R % 8): no bank conflicts).  After the last chunk
+                        // one lane copies the warp's rows, by the copy engine, to
+                        // slots krank * KS_ROWS + R % KS_ROWS of each owner's
+                        // receive region (the same swizzle, as KS_ROWS is a
+                        // multiple of 8), counted in bytes on its receive barrier.
+                        const uint32_t src = base + C::OFF_SRC;
+                        if (lane < C::WARP_ROWS) {
+                            const uint32_t R = static_cast<uint32_t>(quarter * C::WARP_ROWS + lane);
+                            const uint32_t row_addr = src + R * C::KS_ROW_BYTES;
+                            const uint32_t sw = R & 7u;
+                            const uint32_t u0 = 16u * static_cast<uint32_t>(c);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            ptx::st_shared_v4(row_addr + (((u0 + j) ^ sw) * 16u), lo[4 * j], lo[4 * j + 1],
-                                              lo[4 * j + 2], lo[4 * j + 3]);
-                            ptx::st_shared_v4(row_addr + (((u0 + 8 + j) ^ sw) * 16u), hi[4 * j], hi[4 * j + 1],
-                                              hi[4 * j + 2], hi[4 * j + 3]);
-                        }
-                    }
-                    if (c == chunks - 1) {
-                        ptx::fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            // rows [r0, r0 + WARP_ROWS) of the tile, cut at owner boundaries
-                            const uint32_t r0 = static_cast<uint32_t>(quarter * C::WARP_ROWS);
-                            for (uint32_t R = r0; R < r0 + C::WARP_ROWS;) {
-                                const uint32_t owner = R / C::KS_ROWS;
-                                uint32_t end = (owner + 1) * C::KS_ROWS;
-                                if (end > r0 + C::WARP_ROWS) end = r0 + C::WARP_ROWS;
-                                const uint32_t slot = krank * C::KS_ROWS + R % C::KS_ROWS;
-                                ptx::bulk_copy_to_cluster(ptx::mapa(sD + slot * C::KS_ROW_BYTES, owner),
-                                                          src + R * C::KS_ROW_BYTES, (end - R) * C::KS_ROW_BYTES,
-                                                          ptx::mapa(bar_recv, owner));
-                                R = end;
+                            for (int j = 0; j < 8; ++j) {
+                                ptx::st_shared_v4(row_addr + (((u0 + j) ^ sw) * 16u), lo[4 * j], lo[4 * j + 1],
+                                                  lo[4 * j + 2], lo[4 * j + 3]);
+                                ptx::st_shared_v4(row_addr + (((u0 + 8 + j) ^ sw) * 16u), hi[4 * j], hi[4 * j + 1],
+                                                  hi[4 * j + 2], hi[4 * j + 3]);
                             }
                         }
-                    }
-                } else if constexpr (C::EPI_COALESCED) {
-                    // Narrow and tiny tiles: lane r holds row r of this warp's
-                    // WARP_ROWS rows.  Each row goes to the warp's staging
-                    // buffer (128 bytes, 16-byte unit j at j ^ (r % 8), which
-                    // keeps both passes free of bank conflicts); the warp then
-                    // reads it back four rows per instruction, lane l taking
-                    // unit l % 8 of row l / 8, so every st.global of the warp
-                    // writes four whole 128-byte rows of D.  N % 8 == 0, so a
-                    // 16-byte unit is all in range or all out.
-                    uint32_t h[32];
-                    to_f16x2(lo, h);
-                    to_f16x2(hi, h + 16);
-                    const uint32_t buf_base = stage_base;
-                    if (lane < C::WARP_ROWS) {
-                        const uint32_t row_addr = buf_base + static_cast<uint32_t>(lane) * 128u;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
-                            ptx::st_shared_v4(row_addr + unit * 16u, h[4 * j], h[4 * j + 1], h[4 * j + 2],
-                                              h[4 * j + 3]);
+                        if (c == chunks - 1) {
+                            ptx::fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                // rows [r0, r0 + WARP_ROWS) of the tile, cut at owner boundaries
+                                const uint32_t r0 = static_cast<uint32_t>(quarter * C::WARP_ROWS);
+                                for (uint32_t R = r0; R < r0 + C::WARP_ROWS;) {
+                                    const uint32_t owner = R / C::KS_ROWS;
+                                    uint32_t end = (owner + 1) * C::KS_ROWS;
+                                    if (end > r0 + C::WARP_ROWS) end = r0 + C::WARP_ROWS;
+                                    const uint32_t slot = krank * C::KS_ROWS + R % C::KS_ROWS;
+                                    ptx::bulk_copy_to_cluster(ptx::mapa(sD + slot * C::KS_ROW_BYTES, owner),
+                                                              src + R * C::KS_ROW_BYTES, (end - R) * C::KS_ROW_BYTES,
+                                                              ptx::mapa(bar_recv, owner));
+                                    R = end;
+                                }
+                            }
                         }
-                    }
-                    __syncwarp();
-                    const int32_t col = col0 + c * C::EPI_N + 8 * (lane & 7);
+                    } else if constexpr (C::EPI_COALESCED) {
+                        // Narrow and tiny tiles: lane r holds row r of this warp's
+                        // WARP_ROWS rows.  Each row goes to the warp's staging
+                        // buffer (128 bytes, 16-byte unit j at j ^ (r % 8), which
+                        // keeps both passes free of bank conflicts); the warp then
+                        // reads it back four rows per instruction, lane l taking
+                        // unit l % 8 of row l / 8, so every st.global of the warp
+                        // writes four whole 128-byte rows of D.  N % 8 == 0, so a
+                        // 16-byte unit is all in range or all out.
+                        uint32_t h[32];
+                        to_f16x2(lo, h);
+                        to_f16x2(hi, h + 16);
+                        const uint32_t buf_base = stage_base;
+                        if (lane < C::WARP_ROWS) {
+                            const uint32_t row_addr = buf_base + static_cast<uint32_t>(lane) * 128u;
 #pragma unroll
-                    for (int i = 0; i < C::WARP_ROWS / 4; ++i) {
-                        const int32_t r = 4 * i + (lane >> 3);
-                        const uint32_t unit = static_cast<uint32_t>(lane & 7) ^ static_cast<uint32_t>(r & 7);
-                        const uint4 v = ptx::ld_shared_v4(buf_base + static_cast<uint32_t>(r) * 128u + unit * 16u);
-                        const int32_t row = row0 + r;
-                        if (row < p.M && col < p.N) {
-                            ptx::st_global_v4(p.D + static_cast<int64_t>(row) * p.N + col, v.x, v.y, v.z, v.w);
+                            for (int j = 0; j < 8; ++j) {
+                                const uint32_t unit = static_cast<uint32_t>(j) ^ (static_cast<uint32_t>(lane) & 7u);
+                                ptx::st_shared_v4(row_addr + unit * 16u, h[4 * j], h[4 * j + 1], h[4 * j + 2],
+                                                  h[4 * j + 3]);
+                            }
                         }
+                        __syncwarp();
+                        const int32_t col = col0 + c * C::EPI_N + 8 * (lane & 7);
+#pragma unroll
+                        for (int i = 0; i < C::WARP_ROWS / 4; ++i) {
+                            const int32_t r = 4 * i + (lane >> 3);
+                            const uint32_t unit = static_cast<uint32_t>(lane & 7) ^ static_cast<uint32_t>(r & 7);
+                            const uint4 v = ptx::ld_shared_v4(buf_base + static_cast<uint32_t>(r) * 128u + unit * 16u);
+                            const int32_t row = row0 + r;
+                            if (row < p.M && col < p.N) {
+                                ptx::st_global_v4(p.D + static_cast<int64_t>(row) * p.N + col, v.x, v.y, v.z, v.w);
+                            }
+                        }
+                        __syncwarp();  // the buffer is rewritten by the next chunk or work item
                     }
-                    __syncwarp();  // the buffer is rewritten by the next chunk or work item
                 }
             }
             acc.advance();

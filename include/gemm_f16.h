@@ -104,12 +104,18 @@ typedef enum gemm_status {
  *                 (needs cta_group 0 or 1 and one consumer): single CTAs
  *                 with 128 x 64 tiles and an 8-stage ring (all of a K up to
  *                 512 in flight after one load latency), D stored by
- *                 coalesced warp stores; for small, latency-bound problems.  Not on
- *                 the pages: they fix the tile at 128 or 256 x 256.  0
+ *                 coalesced warp stores; for small, latency-bound problems.
+ *                 16 (needs cta_group 0 or 1, one consumer, block_m 0 or 64,
+ *                 cluster_k 0 or 1): thin single-CTA 64 x 16 tiles, MMAs of
+ *                 M = 64, N = 16, 32 columns of tensor memory, each row of D
+ *                 stored straight from registers; for the shortest problems.
+ *                 Not on the pages: they fix the tile at 128 or 256 x 256.  0
  *                 (default): 64 when cta_group is 0, consumers is not 2, the
- *                 K-loop is at most 8
- *                 tiles of 64 and the 128 x 64 tiles fit one wave of
- *                 co-resident CTAs, else 256.  Other values:
+ *                 K-loop is at most 8 tiles of 64 and the 128 x 64 tiles fit
+ *                 one wave of co-resident CTAs, else 256; and with block_m
+ *                 and cluster_k at 0 too, 16 where the tiny tiles of block_m
+ *                 64 would run a K-loop of at most 8 tiles of 64 and the
+ *                 64 x 16 tiles fit one wave.  Other values:
  *                 GEMM_ERR_INVALID_ARG.
  *   block_m       rows of D per CTA.  128: the tiles above.  64 (needs
  *                 block_n 0 or 64, which then means 64): single CTAs with
@@ -255,7 +261,7 @@ int gemm_f16_nt_static_ws(const void *A, const void *B, void *D, int64_t M, int6
 typedef struct gemm_f16_launch_info {
     int32_t cta_group;        /* 1 or 2 */
     int32_t consumers;        /* 1 or 2 */
-    int32_t block_n;          /* tile width: 256 or 64 */
+    int32_t block_n;          /* tile width: 256, 64 or 16 */
     int32_t split_k;          /* K slices S (1 = no split-K; > 1 adds the reduction kernel) */
     int32_t block_m;          /* rows of D per CTA and consumer: 128 or 64 */
     int32_t stages;           /* depth of the shared-memory operand ring */
@@ -340,10 +346,11 @@ typedef struct gemm_f16_work_item {
 /*
  * The persistent scheduler, as a pure host query (no CUDA call); the kernel
  * runs the same code.  D is cut into tiles of (block_m * cta_group *
- * consumers) rows x block_n columns (consumers 0 means 1; block_m 0 means 128,
- * and 64, the tiny tiles of gemm_f16_options, needs block_n 0 or 64; block_n 0
- * means 64 with block_m 64, else 256; block_n 64, the narrow tiles, needs
- * cta_group 0 or 1, which then means 1, and one consumer), ordered in groups of
+ * consumers) rows x block_n columns (consumers 0 means 1; block_m 0 means 64
+ * with block_n 16, else 128, and 64, the tiny tiles of gemm_f16_options, needs
+ * block_n 0, 16 or 64; block_n 0 means 64 with block_m 64, else 256; block_n
+ * 64 or 16, the narrow and thin tiles, needs cta_group 0 or 1, which then
+ * means 1, and one consumer, and 16 needs block_m 64), ordered in groups of
  * `raster_group` M-tiles (0 = the shape-derived default described under
  * gemm_f16_options): M fastest inside a group, then N, then the next group
  * (TIRx notes V6, "Better L2 Locality").  With T tiles and P = num_clusters
@@ -353,7 +360,7 @@ typedef struct gemm_f16_work_item {
  * 148 CTAs leave 6.9 tiles per CTA, i.e. a partly idle last wave).  With
  * split_k = 1 (what gemm_f16_nt_ws() does given enough workspace) and few
  * tiles, K is instead cut into slices: item t*S + s is slice s of tile t.
- * Narrow and tiny tiles are never split along N, nor along K this way.
+ * Narrow, tiny and thin tiles are never split along N, nor along K this way.
  * split_k 2, 4 or 8 (narrow or tiny tiles) is the K split across a cluster
  * (cluster_k of gemm_f16_options): S = split_k, reduced to at most the
  * number of 64-wide K tiles, with the same item numbering; that kernel runs
@@ -370,7 +377,8 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
 /*
  * Where CTA `rank` of a work item reads and writes, as a pure host query (no
  * CUDA call); the kernel uses the same function.  TIRx notes V8, "Operand
- * Partition" and "Output Ownership": with bm = block_m (0 meaning 128), m_base =
+ * Partition" and "Output Ownership": with bm = block_m (0 meaning 64 with
+ * block_n 16, else 128), m_base =
  * m_idx * bm * cta_group * consumers and n_base = n_idx * block_n + n_off, the
  * CTA loads A rows a_row = m_base + bm * rank (bm rows; consumer c's block
  * lies c * bm * cta_group rows further, TIRx notes V9) and B rows b_row =
@@ -379,10 +387,12 @@ int gemm_f16_nt_schedule(int64_t M, int64_t N, int64_t K, int32_t cta_group, int
  * n_len columns starting at d_col = n_base ("Epilogue Column Address": no rank
  * term).  block_n is 0 (meaning 256, or 64 with block_m 64) or 256: n_len is
  * 256 (whole tile, n_off 0) or 128 (half tile, n_off 0 or 128); or 64 (narrow
- * tiles, cta_group 0 or 1, one consumer): n_len 64, n_off 0.  block_m 64
- * needs block_n 64.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not
- * 0/1/2, consumers not 0/1/2 or 2 without a pair, block_n not 0/64/256 or 64
- * with a pair or two consumers, block_m not 0/64/128 or 64 with block_n 256,
+ * tiles, cta_group 0 or 1, one consumer): n_len 64, n_off 0; or 16 (thin
+ * tiles, also block_m 64): n_len 16, n_off 0.  block_m 64 needs block_n 0, 16
+ * or 64.  Returns GEMM_OK, or GEMM_ERR_INVALID_ARG (cta_group not
+ * 0/1/2, consumers not 0/1/2 or 2 without a pair, block_n not 0/16/64/256 or
+ * 16 or 64 with a pair or two consumers, block_m not 0/64/128, 64 with
+ * block_n 256 or 128 with block_n 16,
  * rank out of range, bad n_off/n_len, negative or too large indices, null
  * outputs).
  */

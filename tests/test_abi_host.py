@@ -128,7 +128,9 @@ def test_argument_errors_are_returned_before_any_launch():
                 g.Options(block_m=64, cta_group=2), g.Options(block_m=64, consumers=2),
                 g.Options(cluster_k=3), g.Options(cluster_k=16), g.Options(cluster_k=-1),
                 g.Options(cluster_k=4, block_n=256),
-                g.Options(cluster_k=8, cta_group=2), g.Options(cluster_k=2, consumers=2)):
+                g.Options(cluster_k=8, cta_group=2), g.Options(cluster_k=2, consumers=2),
+                g.Options(block_n=16, block_m=128), g.Options(block_n=16, cluster_k=2), g.Options(block_n=16, cta_group=2),
+                g.Options(block_n=16, consumers=2), g.Options(block_n=8)):
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
 
@@ -529,9 +531,10 @@ NO_SPLIT = GB300[:5] + [0] * 6                         # one that cannot co-sche
 
 def test_describe_for_the_five_workloads_on_gb300():
     expect = {
-        (128, 128, 64): dict(cta_group=1, consumers=1, block_n=64, block_m=64, cluster_k=1, clusters=4,
-                             work_items=4),
-        (256, 256, 512): dict(cta_group=1, consumers=1, block_n=64, block_m=64, cluster_k=4, clusters=16,
+        # thin 64 x 16 tiles: 2 x 8 and 4 x 16 of them, one per CTA, no K split
+        (128, 128, 64): dict(cta_group=1, consumers=1, block_n=16, block_m=64, cluster_k=1, clusters=16,
+                             work_items=16),
+        (256, 256, 512): dict(cta_group=1, consumers=1, block_n=16, block_m=64, cluster_k=1, clusters=64,
                               work_items=64),
         (4096, 4096, 4096): dict(cta_group=2, consumers=1, block_n=256, block_m=128, cluster_k=1, clusters=76,
                                  work_items=284),
@@ -572,8 +575,7 @@ def test_describe_for_the_consumer_count_rule(M, N, K, consumers):
 
 @pytest.mark.parametrize("M,N,K,bm,ks", [
     (256, 256, 4096, 64, 4), (128, 128, 4096, 64, 8), (256, 256, 1024, 64, 4), (128, 1024, 1024, 64, 2),
-    (512, 512, 4096, 128, 4), (256, 256, 512, 64, 4), (128, 128, 512, 64, 4),
-    (256, 256, 448, 64, 1), (512, 512, 512, 64, 1), (512, 512, 1024, 64, 1), (576, 576, 1024, 64, 1),
+    (512, 512, 4096, 128, 4), (512, 512, 512, 64, 1), (512, 512, 1024, 64, 1), (576, 576, 1024, 64, 1),
     (640, 640, 4096, 128, 2), (768, 512, 4096, 128, 2), (512, 1024, 4096, 128, 2), (768, 768, 4096, 128, 2),
     (768, 768, 2048, 128, 1), (384, 384, 2048, 128, 4), (512, 512, 2048, 128, 2),
 ])
@@ -585,6 +587,32 @@ def test_describe_for_the_cluster_k_split_rule(M, N, K, bm, ks):
     # with a workspace the split still wins; without the device's clusters it is off
     assert g.describe_for(M, N, K, GB300, with_workspace=True)["workspace_bytes"] == 0
     assert g.describe_for(M, N, K, NO_SPLIT)["cluster_k"] == 1
+
+
+@pytest.mark.parametrize("M,N,K,thin", [
+    (128, 128, 64, True), (256, 256, 512, True), (128, 128, 512, True), (256, 256, 448, True),
+    (128, 256, 256, True), (1, 8, 8, True), (384, 384, 256, True),  # 6 x 24 = 144 thin tiles: one wave
+    (256, 256, 576, False),   # 9 K tiles: the cluster K split instead
+    (512, 512, 512, False),   # 8 x 32 = 256 thin tiles: more than a wave, tiny tiles
+    (1024, 1024, 512, False),  # narrow tiles
+])
+def test_describe_for_the_thin_tile_rule(M, N, K, thin):
+    """Thin 64 x 16 tiles where the tiny tiles would run a K-loop of at most 8 tiles of 64 and
+    the thin tiles fit one wave; only when block_n, block_m and cluster_k are all left open."""
+    c = g.describe_for(M, N, K, GB300)
+    if thin:
+        tiles = -(-M // 64) * -(-N // 16)
+        assert (c["cta_group"], c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (1, 16, 64, 1, 1)
+        assert (c["clusters"], c["work_items"], c["workspace_bytes"], c["stages"]) == (tiles, tiles, 0, 12)
+        # any tile option given by the caller keeps the earlier rules
+        for o in (g.Options(block_m=64), g.Options(block_n=64), g.Options(cluster_k=1)):
+            assert g.describe_for(M, N, K, GB300, o)["block_n"] == 64
+        # a grid capped below the thin tile count keeps the tiny tiles
+        assert g.describe_for(M, N, K, GB300, g.Options(max_clusters=tiles - 1))["block_n"] in (64, 16 if tiles == 1 else 64)
+    else:
+        assert c["block_n"] != 16
+    forced = g.describe_for(512, 512, 4096, GB300, g.Options(block_n=16))
+    assert (forced["block_n"], forced["block_m"], forced["cluster_k"], forced["work_items"]) == (16, 64, 1, 256)
 
 
 def test_describe_for_the_workspace_split_k_choice():
@@ -631,6 +659,10 @@ def test_describe_for_random_shapes_keep_the_launch_rules(device):
         if c["block_n"] == 64:
             assert c["cta_group"] == 1 and c["block_m"] in (64, 128) and c["workspace_bytes"] == 0
             tiles = -(-M // c["block_m"]) * -(-N // 64)
+        if c["block_n"] == 16:  # thin tiles: short K, one wave, no split
+            tiles = -(-M // 64) * -(-N // 16)
+            assert (c["cta_group"], c["block_m"], c["cluster_k"], c["split_k"], c["workspace_bytes"]) == (1, 64, 1, 1, 0)
+            assert k_tiles <= 8 and tiles <= device[4] and c["work_items"] == tiles == c["clusters"]
         if c["cluster_k"] > 1:
             assert c["block_n"] == 64 and c["split_k"] == 1
             assert c["clusters"] == tiles and c["work_items"] == tiles * c["cluster_k"]

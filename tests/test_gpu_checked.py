@@ -25,8 +25,10 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     # (M, N, K, cta_group, consumers, block_n, max_clusters, workspace[, block_m[, cluster_k]])
-    (128, 128, 64, 0, 0, 0, 0, False),       # default: tiny tiles
-    (256, 256, 512, 0, 0, 0, 0, False),      # default: tiny tiles, K split across clusters
+    (128, 128, 64, 0, 0, 0, 0, False),       # default: thin 64 x 16 tiles
+    (256, 256, 512, 0, 0, 0, 0, False),      # default: thin tiles, a K-loop of 8 tiles
+    (256, 256, 512, 0, 0, 64, 0, False, 64, 4),  # tiny tiles, K split across clusters of 4
+    (700, 600, 1000, 1, 1, 16, 9, False, 64),  # thin tiles, many per CTA, K beyond the ring, ragged
     (200, 136, 520, 1, 1, 64, 0, False, 64, 8),   # K split over 8 CTAs, ragged M, N and K
     (520, 264, 1000, 1, 1, 64, 0, False, 64, 2),  # K split over 2 CTAs, K beyond the ring
     (300, 200, 1000, 1, 1, 64, 0, False, 128, 4),  # narrow tiles, K split over 4 CTAs, ragged

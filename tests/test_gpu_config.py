@@ -18,18 +18,18 @@ def _resident_tiny_ctas(gpu_lib):
     return gpu_lib.describe(4096, 4096, 64, gpu_lib.Options(block_m=64))["clusters"]
 
 
-def test_smallest_problems_take_tiny_tiles(gpu_lib):
+def test_smallest_problems_take_thin_or_tiny_tiles(gpu_lib):
+    # the two small workloads: thin 64 x 16 tiles, one per CTA (K at most 512, one wave)
     c1 = gpu_lib.describe(128, 128, 64)
-    assert (c1["cta_group"], c1["block_n"], c1["block_m"], c1["split_k"], c1["clusters"], c1["work_items"],
-            c1["stages"]) == (1, 64, 64, 1, 4, 4, 12)
-    c2 = gpu_lib.describe(256, 256, 512)  # sixteen tiles, K split across clusters of 4
+    assert (c1["cta_group"], c1["block_n"], c1["block_m"], c1["split_k"], c1["cluster_k"], c1["clusters"],
+            c1["work_items"], c1["stages"]) == (1, 16, 64, 1, 1, 16, 16, 12)
+    c2 = gpu_lib.describe(256, 256, 512)
     assert (c2["cta_group"], c2["block_n"], c2["block_m"], c2["split_k"], c2["cluster_k"], c2["clusters"],
-            c2["work_items"]) == (1, 64, 64, 1, 4, 16, 64)
+            c2["work_items"]) == (1, 16, 64, 1, 1, 64, 64)
     # 64 x 64 tiles up to two thirds of the co-resident CTAs, any K, without a workspace
     P = _resident_tiny_ctas(gpu_lib)
     assert P >= 140  # GB300: 152 SMs, one tiny-tile CTA each
-    for M, N, K in ((256, 256, 448), (512, 512, 512), (64 * (2 * P // 3), 64, 1024), (576, 576, 1024),
-                    (200, 1000, 72)):
+    for M, N, K in ((512, 512, 512), (64 * (2 * P // 3), 64, 1024), (576, 576, 1024), (200, 1000, 72)):
         c = gpu_lib.describe(M, N, K)
         tiles = -(-M // 64) * -(-N // 64)
         assert (c["block_n"], c["block_m"], c["cluster_k"], c["work_items"], c["clusters"]) == \

@@ -41,9 +41,9 @@ def _cases(n=36, seed=2026, per_series=12):
     # make sure split-K (few tiles, long K) shows up with each workspace entry point
     out.append((n, 256, 264, 2600, (2, 1), 0, "ws"))  # the default would take narrow tiles here
     out.append((n + 1, 500, 512, 2048, (1, 1), 0, "static"))
-    # narrow and tiny tiles, forced, with the K-loop both inside and beyond
+    # narrow, tiny and thin tiles, forced, with the K-loop both inside and beyond
     # the 8- and 12-stage rings
-    for series, variant in ((1, (1, 1, 64, 128)), (2, (1, 1, 64, 64)), (3, None)):
+    for series, variant in ((1, (1, 1, 64, 128)), (2, (1, 1, 64, 64)), (3, None), (4, (1, 1, 16, 64))):
         rng = np.random.default_rng(seed + series)
         first = n + 2 + per_series * (series - 1)
         for i in range(first, first + per_series):

@@ -52,11 +52,12 @@ def assert_close(gpu_f16, ref_bits, what=""):
 # sharing each B stage, the narrow 128 x 64 single-CTA tiles of small problems
 # and the tiny 64 x 64 tiles (MMAs of M = 64) of the smallest, each without a K
 # split and with K split across clusters of 2, 4 and 8 CTAs (fewer where K has
-# fewer 64-wide tiles).
+# fewer 64-wide tiles), and the thin 64 x 16 tiles (MMAs of M = 64, N = 16).
 VARIANTS = [(2, 1, 256), (1, 1, 256), (2, 2, 256), (1, 1, 64, 128, 1), (1, 1, 64, 128, 2), (1, 1, 64, 128, 4),
-            (1, 1, 64, 128, 8), (1, 1, 64, 64, 1), (1, 1, 64, 64, 2), (1, 1, 64, 64, 4), (1, 1, 64, 64, 8)]
+            (1, 1, 64, 128, 8), (1, 1, 64, 64, 1), (1, 1, 64, 64, 2), (1, 1, 64, 64, 4), (1, 1, 64, 64, 8),
+            (1, 1, 16, 64, 1)]
 VIDS = ["pair", "single", "pair-2consumers", "narrow", "narrow-k2", "narrow-k4", "narrow-k8", "tiny", "tiny-k2",
-        "tiny-k4", "tiny-k8"]
+        "tiny-k4", "tiny-k8", "thin"]
 
 
 def opts(g, variant=(0, 0), max_clusters=0):
@@ -162,11 +163,11 @@ def test_ragged_shapes_full(gpu_lib, M, N, K, v):
 
 @pytest.mark.parametrize("v,clusters", [((2, 1), 1), ((2, 1), 3), ((1, 1), 1), ((1, 1), 5), ((2, 2), 1), ((2, 2), 3),
                                         ((1, 1, 64), 1), ((1, 1, 64), 6), ((1, 1, 64, 64), 1),
-                                        ((1, 1, 64, 64), 7)])
+                                        ((1, 1, 64, 64), 7), ((1, 1, 16, 64), 1), ((1, 1, 16, 64), 9)])
 def test_few_persistent_clusters_run_many_tiles(gpu_lib, v, clusters):
     # 1024 x 1024 x 320: 16 (pair), 32 (single CTA), 8 (two consumers), 128
-    # (narrow) or 256 (tiny) tiles, so each persistent CTA runs several tiles
-    # and both rings wrap many times across tiles.
+    # (narrow), 256 (tiny) or 1024 (thin) tiles, so each persistent CTA runs
+    # several tiles and both rings wrap many times across tiles.
     w = si.custom(1024, 1024, 320, seed=77)
     A, B = w.operands()
     assert_close(run(gpu_lib, A, B, opts(gpu_lib, v, clusters)), oracle.gemm_f16_nt(A, B),

@@ -21,15 +21,15 @@ TIMEOUT = -7
 
 
 # (cta_group, consumers, block_n, block_m, cluster_k): the CTA pair, a single CTA, two
-# consumers, narrow and tiny tiles, and narrow and tiny tiles with K split across clusters of
-# 2, 4 and 8 CTAs (there every CTA still reaches the cluster barrier after its roles gave up)
+# consumers, narrow, tiny and thin tiles, and narrow and tiny tiles with K split across clusters
+# of 2, 4 and 8 CTAs (there every CTA still reaches the cluster barrier after its roles gave up)
 VARIANTS = [(2, 1, 0, 0, 0), (1, 1, 0, 0, 0), (2, 2, 0, 0, 0), (1, 1, 64, 128, 1), (1, 1, 64, 128, 2),
-            (1, 1, 64, 64, 1), (1, 1, 64, 64, 4), (1, 1, 64, 64, 8)]
+            (1, 1, 64, 64, 1), (1, 1, 64, 64, 4), (1, 1, 64, 64, 8), (1, 1, 16, 64, 1)]
 
 
 @pytest.mark.parametrize("cg,consumers,bn,bm,ks", VARIANTS,
                          ids=["pair", "single", "pair-2consumers", "narrow", "narrow-k2", "tiny", "tiny-k4",
-                              "tiny-k8"])
+                              "tiny-k8", "thin"])
 def test_deadlocked_ring_times_out_and_context_survives(gpu_lib, cg, consumers, bn, bm, ks):
     w = si.WORKLOADS["ktile_grid_256x256x512"]
     A, B = w.operands()
