@@ -26,6 +26,11 @@ def test_smallest_problems_take_thin_or_tiny_tiles(gpu_lib):
     c2 = gpu_lib.describe(256, 256, 512)
     assert (c2["cta_group"], c2["block_n"], c2["block_m"], c2["split_k"], c2["cluster_k"], c2["clusters"],
             c2["work_items"]) == (1, 16, 64, 1, 1, 64, 64)
+    for M, N, K in ((128, 128, 512), (256, 256, 448), (128, 256, 256)):  # K <= 512: thin tiles as well
+        c = gpu_lib.describe(M, N, K)
+        tiles = -(-M // 64) * -(-N // 16)
+        assert (c["block_n"], c["block_m"], c["cluster_k"], c["work_items"], c["clusters"]) == \
+            (16, 64, 1, tiles, tiles), (M, N, K)
     # 64 x 64 tiles up to two thirds of the co-resident CTAs, any K, without a workspace
     P = _resident_tiny_ctas(gpu_lib)
     assert P >= 140  # GB300: 152 SMs, one tiny-tile CTA each
@@ -45,7 +50,6 @@ def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
     # or where the tiny ones split in 2 and the narrow ones can split in 4 with at least 8
     for (M, N, K), bm, ks in (((256, 256, 4096), 64, 4), ((128, 128, 4096), 64, 8), ((256, 256, 1024), 64, 4),
                               ((128, 1024, 1024), 64, 2), ((384, 384, 2048), 128, 4), ((512, 512, 4096), 128, 4),
-                              ((256, 256, 512), 64, 4), ((128, 128, 512), 64, 4), ((256, 256, 448), 64, 1),
                               ((512, 512, 512), 64, 1), ((512, 512, 1024), 64, 1), ((576, 576, 1024), 64, 1),
                               ((640, 640, 4096), 128, 2), ((768, 512, 4096), 128, 2), ((512, 1024, 4096), 128, 2),
                               ((768, 768, 4096), 128, 2), ((768, 768, 2048), 128, 1), ((512, 512, 2048), 128, 2)):
