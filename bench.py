@@ -675,8 +675,9 @@ def run_ours(args) -> None:
                          "algorithmic_bytes_per_launch": w.min_bytes},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": 2 * (w.M * w.K + w.N * w.K),
                     "d2h_bytes_per_step": 2 * w.M * w.N, "steps": e2e_steps, "wall_ms": e2e_wall_ms,
-                    "what": "HostPipeline: per step, pinned host A, B -> device, GEMM, D -> pinned host; "
-                            "copies of neighbouring steps overlap the GEMM on separate streams"},
+                    "what": "HostPipeline: per step one gemm_f16_nt_host call (C ABI: pinned host A, B -> "
+                            "device, GEMM, D -> pinned host, enqueued on one stream); three slots on three "
+                            "streams overlap neighbouring steps' copies with the GEMM"},
             "gpu_launches": args.steps,
             "clocks": clocks,
             "cublas_reference": cublas,

@@ -79,6 +79,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.gemm_f16_nt_schedule.restype = ctypes.c_int
     lib.gemm_f16_nt_cta_origin.argtypes = [i32, i32, i32, i32, i64, i64, i64, i64, i32, i64p, i64p, i64p, i64p]
     lib.gemm_f16_nt_cta_origin.restype = ctypes.c_int
+    lib.gemm_f16_nt_host.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp, ctypes.POINTER(Options)]
+    lib.gemm_f16_nt_host.restype = ctypes.c_int
     lib.gemm_f16_nt_ws.argtypes = [vp, vp, vp, i64, i64, i64, vp, i64, vp, ctypes.POINTER(Options)]
     lib.gemm_f16_nt_ws.restype = ctypes.c_int
     lib.gemm_f16_nt_workspace_size.argtypes = [i64, i64, i64, ctypes.POINTER(Options)]
@@ -219,11 +221,11 @@ def gemm_f16_nt(A, B, D=None, *, stream=None, options: Options | None = None, wo
 
 
 def gemm_f16_nt_host(A_host, B_host, D_host=None, *, device=None, stream=None, A_dev=None, B_dev=None,
-                     D_dev=None):
-    """End-to-end call on HOST fp16 tensors: copy A, B in, run the GEMM, copy D out.
-
-    Pass pinned host tensors for asynchronous copies and (optionally) reusable
-    device buffers. Returns the host D after the stream has finished.
+                     D_dev=None, options: Options | None = None):
+    """End-to-end call on HOST fp16 tensors through the C entry point ``gemm_f16_nt_host``: the
+    copy of A and B into device buffers, the GEMM and the copy of D back, all enqueued on one
+    stream.  Pass pinned host tensors for asynchronous copies and (optionally) reusable device
+    buffers. Returns the host D after the stream has finished.
     """
     import torch
 
@@ -235,91 +237,86 @@ def gemm_f16_nt_host(A_host, B_host, D_host=None, *, device=None, stream=None, A
         A_dev = A_dev if A_dev is not None else torch.empty((M, K), dtype=torch.float16, device=dev)
         B_dev = B_dev if B_dev is not None else torch.empty((N, K), dtype=torch.float16, device=dev)
         D_dev = D_dev if D_dev is not None else torch.empty((M, N), dtype=torch.float16, device=dev)
-        if D_host is None:
-            D_host = torch.empty((M, N), dtype=torch.float16, pin_memory=True)
-        A_dev.copy_(A_host, non_blocking=True)
-        B_dev.copy_(B_host, non_blocking=True)
-        gemm_f16_nt(A_dev, B_dev, D_dev, stream=s)
-        D_host.copy_(D_dev, non_blocking=True)
+    if D_host is None:
+        D_host = torch.empty((M, N), dtype=torch.float16, pin_memory=True)
+    _host_call(A_host, B_host, D_host, A_dev, B_dev, D_dev, s, options)
     s.synchronize()
     return D_host
+
+
+def _host_call(A_host, B_host, D_host, A_dev, B_dev, D_dev, stream, options=None) -> None:
+    """One ``gemm_f16_nt_host`` call (checks dtypes, shapes and contiguity; raises on a status)."""
+    import torch
+
+    M, K = A_host.shape
+    N = B_host.shape[0]
+    for t, shape, host in ((A_host, (M, K), True), (B_host, (N, K), True), (D_host, (M, N), True),
+                           (A_dev, (M, K), False), (B_dev, (N, K), False), (D_dev, (M, N), False)):
+        if t.dtype != torch.float16 or tuple(t.shape) != shape or not t.is_contiguous() or t.is_cuda == host:
+            raise ValueError("host and device operands must be contiguous fp16 tensors of matching shapes")
+    rc = load().gemm_f16_nt_host(A_host.data_ptr(), B_host.data_ptr(), D_host.data_ptr(), M, N, K,
+                                 A_dev.data_ptr(), B_dev.data_ptr(), D_dev.data_ptr(), stream.cuda_stream,
+                                 ctypes.byref(options) if options is not None else None)
+    if rc != 0:
+        raise GemmError(rc, "gemm_f16_nt_host")
 
 
 class HostPipeline:
     """GEMMs on HOST fp16 tensors with the copies overlapped: D_i = A_i·B_iᵀ.
 
-    Three streams: copy-in, compute, copy-out.  Device buffers come in
-    `depth` slots; step i uses slot i % depth, so step i+1's copy-in and step
-    i-1's copy-out run while step i's GEMM does.  Events keep each slot's
-    buffers from being overwritten before they are consumed.  Pass pinned host
-    tensors, and read a D_host only after synchronize().  Copy-outs run in
-    submission order on one stream, so reusing a D_host is ordered.
+    Each step is one ``gemm_f16_nt_host`` call (copy-in, GEMM, copy-out enqueued on one
+    stream).  Device buffers and streams come in `depth` slots; step i uses slot i % depth,
+    so step i+1's copy-in and step i-1's copy-out run while step i's GEMM does.  A slot's
+    stream orders its own steps, so a slot's buffers are reused only after its previous
+    copy-out.  Pass pinned host tensors, and read a D_host only after synchronize().
     """
 
-    def __init__(self, M: int, N: int, K: int, *, device=None, depth: int = 2):
+    def __init__(self, M: int, N: int, K: int, *, device=None, depth: int = 3):
         import torch
 
         self.dev = torch.device(device or "cuda")
         self.M, self.N, self.K = M, N, K
         self.depth = depth
-        self.h2d = torch.cuda.Stream(self.dev)
-        self.comp = torch.cuda.Stream(self.dev)
-        self.d2h = torch.cuda.Stream(self.dev)
+        self.streams = [torch.cuda.Stream(self.dev) for _ in range(depth)]
         mk = lambda *shape: torch.empty(shape, dtype=torch.float16, device=self.dev)  # noqa: E731
         self.A = [mk(M, K) for _ in range(depth)]
         self.B = [mk(N, K) for _ in range(depth)]
         self.D = [mk(M, N) for _ in range(depth)]
-        ev = lambda: [torch.cuda.Event() for _ in range(depth)]  # noqa: E731
-        self.loaded, self.computed, self.stored = ev(), ev(), ev()
-        self.used = [False] * depth
         self.i = 0
 
     def submit(self, A_host, B_host, D_host) -> None:
         """Queue one step: copy A_host, B_host in, compute, copy D out into D_host."""
         j = self.i % self.depth
         self.i += 1
-        if self.used[j]:
-            self.h2d.wait_event(self.computed[j])   # slot j's A, B consumed by its last GEMM
-            self.comp.wait_event(self.stored[j])    # slot j's D copied out
-        with torch_stream(self.h2d):
-            self.A[j].copy_(A_host, non_blocking=True)
-            self.B[j].copy_(B_host, non_blocking=True)
-            self.loaded[j].record(self.h2d)
-        self.comp.wait_event(self.loaded[j])
-        gemm_f16_nt(self.A[j], self.B[j], self.D[j], stream=self.comp)
-        self.computed[j].record(self.comp)
-        self.d2h.wait_event(self.computed[j])
-        with torch_stream(self.d2h):
-            D_host.copy_(self.D[j], non_blocking=True)
-            self.stored[j].record(self.d2h)
-        self.used[j] = True
+        _host_call(A_host, B_host, D_host, self.A[j], self.B[j], self.D[j], self.streams[j])
 
     def record_start(self):
-        """An event on the copy-in stream before the next submit (for timing)."""
+        """An event, on every slot's stream, before the next submit (for timing): the first slot's."""
         import torch
 
         e = torch.cuda.Event(enable_timing=True)
-        e.record(self.h2d)
+        e.record(self.streams[self.i % self.depth])
+        for k in range(1, self.depth):
+            self.streams[(self.i + k) % self.depth].wait_event(e)
         return e
 
     def record_end(self):
-        """An event on the copy-out stream after everything submitted so far (for timing)."""
+        """An event after everything submitted so far (for timing): all slots joined on one stream."""
         import torch
 
+        last = self.streams[(self.i - 1) % self.depth]
+        for s in self.streams:
+            if s is not last:
+                ev = torch.cuda.Event()
+                ev.record(s)
+                last.wait_event(ev)
         e = torch.cuda.Event(enable_timing=True)
-        e.record(self.d2h)
+        e.record(last)
         return e
 
     def synchronize(self) -> None:
-        self.h2d.synchronize()
-        self.comp.synchronize()
-        self.d2h.synchronize()
-
-
-def torch_stream(s):
-    import torch
-
-    return torch.cuda.stream(s)
+        for s in self.streams:
+            s.synchronize()
 
 
 def last_device_status(stream=None) -> tuple[int, int]:

@@ -606,12 +606,13 @@ int launch(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t 
 
 int zero_fill(void *D, int64_t M, int64_t N, cudaStream_t stream);
 
-int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
-        const gemm_f16_options *opts, void *workspace, int64_t workspace_bytes) {
-    Opts o;
-    int st = parse_options(opts, &o);
+// The argument checks every compute entry point makes before anything is enqueued (A, B, D
+// are the device operands).  GEMM_OK also for an empty product, which then launches nothing.
+int check_args(const void *A, const void *B, const void *D, int64_t M, int64_t N, int64_t K,
+               const gemm_f16_options *opts, Opts *o) {
+    int st = parse_options(opts, o);
     if (st != GEMM_OK) return st;
-    if (M < 0 || N < 0 || K < 0 || workspace_bytes < 0) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (!shape_ok(M, N, K)) return GEMM_ERR_UNSUPPORTED_SHAPE;
     if (M == 0 || N == 0) return GEMM_OK;  // empty product: nothing to write
     if (!D || (K > 0 && (!A || !B))) return GEMM_ERR_INVALID_ARG;
@@ -623,6 +624,15 @@ int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, 
     if (K > 0 && (overlaps(D, M * N * 2, A, M * K * 2) || overlaps(D, M * N * 2, B, N * K * 2))) {
         return GEMM_ERR_INVALID_ARG;
     }
+    return GEMM_OK;
+}
+
+int run(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream,
+        const gemm_f16_options *opts, void *workspace, int64_t workspace_bytes) {
+    Opts o;
+    if (workspace_bytes < 0) return GEMM_ERR_INVALID_ARG;
+    int st = check_args(A, B, D, M, N, K, opts, &o);
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
     int dev = -1;
     DeviceInfo *info = nullptr;
     st = device_setup(&dev, &info);
@@ -741,6 +751,33 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
 
 int gemm_f16_nt(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *stream) {
     return run(A, B, D, M, N, K, stream, nullptr, nullptr, 0);
+}
+
+int gemm_f16_nt_host(const void *A_host, const void *B_host, void *D_host, int64_t M, int64_t N, int64_t K,
+                     void *A_dev, void *B_dev, void *D_dev, void *stream, const gemm_f16_options *opts) {
+    Opts o;
+    int st = check_args(A_dev, B_dev, D_dev, M, N, K, opts, &o);
+    if (st != GEMM_OK || M == 0 || N == 0) return st;
+    if (!D_host || (K > 0 && (!A_host || !B_host))) return GEMM_ERR_INVALID_ARG;
+    int dev = -1;
+    DeviceInfo *info = nullptr;
+    st = device_setup(&dev, &info);  // a usable GB300 before any copy is enqueued
+    if (st != GEMM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (K > 0 && (cudaMemcpyAsync(A_dev, A_host, static_cast<size_t>(M * K * 2), cudaMemcpyHostToDevice, s) !=
+                      cudaSuccess ||
+                  cudaMemcpyAsync(B_dev, B_host, static_cast<size_t>(N * K * 2), cudaMemcpyHostToDevice, s) !=
+                      cudaSuccess)) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    st = run(A_dev, B_dev, D_dev, M, N, K, stream, opts, nullptr, 0);
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpyAsync(D_host, D_dev, static_cast<size_t>(M * N * 2), cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
 }
 
 int gemm_f16_nt_ws(const void *A, const void *B, void *D, int64_t M, int64_t N, int64_t K, void *workspace,

@@ -191,6 +191,30 @@ int gemm_f16_nt_ex(const void *A, const void *B, void *D, int64_t M, int64_t N, 
                    const gemm_f16_options *opts);
 
 /*
+ * End to end from host memory: enqueues on `stream`, in order, the copies of the
+ * host operands A_host (M x K) and B_host (N x K) into the caller's device
+ * buffers A_dev and B_dev, the GEMM D_dev = A_dev * B_dev^T of gemm_f16_nt_ex()
+ * with `opts` (NULL = defaults), and the copy of D_dev into the host buffer
+ * D_host (M x N); returns once all four are enqueued.  D_host is complete when
+ * the stream reaches that point (synchronise the stream, or an event recorded
+ * after the call, before reading it).  Layouts as above, all fp16 row-major.
+ * The device buffers are owned by the caller and the library allocates
+ * nothing: D_dev must not overlap A_dev or B_dev; they must stay alive, and
+ * not be written by other work, until the stream has passed the copy-out.
+ * With page-locked (pinned) host buffers the copies are asynchronous and
+ * overlap work on other streams: calls on two or three streams, each with its
+ * own device buffers, overlap one step's copy-in, another's GEMM and a third's
+ * copy-out, which is how a stream of host-resident problems is best run.
+ * With pageable host buffers the copy-in returns only when the host data has
+ * been taken.  Errors: those of gemm_f16_nt_ex() for the device buffers (all
+ * checked before anything is enqueued), GEMM_ERR_INVALID_ARG for a null host
+ * buffer of a non-empty product, GEMM_ERR_CUDA when a copy cannot be
+ * enqueued.  Not on the pages, which start from operands in device memory.
+ */
+int gemm_f16_nt_host(const void *A_host, const void *B_host, void *D_host, int64_t M, int64_t N, int64_t K,
+                     void *A_dev, void *B_dev, void *D_dev, void *stream, const gemm_f16_options *opts);
+
+/*
  * As gemm_f16_nt_ex(), with a caller-owned device workspace that lets the
  * library split the K-loop across CTA pairs when the output has few tiles
  * (split-K: at most a quarter as many 256x256 tiles as co-resident pairs, and

@@ -134,6 +134,26 @@ def test_argument_errors_are_returned_before_any_launch():
         assert g.gemm_f16_nt_ptr(a, b, d, 128, 128, 64, None, bad) == INVALID
 
 
+def test_host_buffer_entry_checks_its_arguments_first():
+    """gemm_f16_nt_host checks the device buffers as every compute entry point does, and the
+    host buffers for null, before it enqueues anything (no GPU needed: every case fails
+    validation, and valid arguments then meet the missing device)."""
+    lib = g.load()
+    h, a, b, d = 0x50000, 0x10000, 0x20000, 0x30000  # never dereferenced
+    call = lambda *args: lib.gemm_f16_nt_host(*args, None, None)  # noqa: E731
+    assert call(h, h, h, 128, 128, 64, a, b, None) == INVALID          # no device D
+    assert call(h, h, h, 128, 128, 64, None, b, d) == INVALID          # no device A
+    assert call(h, h, None, 128, 128, 64, a, b, d) == INVALID          # no host D
+    assert call(None, h, h, 128, 128, 64, a, b, d) == INVALID          # no host A
+    assert call(h, h, h, 128, 128, 64, a + 2, b, d) == MISALIGNED
+    assert call(h, h, h, 128, 12, 64, a, b, d) == UNSUPPORTED
+    assert call(h, h, h, 128, 128, 64, a, b, a + 0x1000) == INVALID    # device D overlaps device A
+    assert call(None, None, None, 0, 128, 64, None, None, None) == OK  # empty product
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        assert call(h, h, h, 128, 128, 64, a, b, d) == NO_DEVICE
+
+
 def test_no_device_reported_without_gpu():
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():

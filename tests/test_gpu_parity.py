@@ -410,6 +410,34 @@ def test_host_pipeline_end_to_end(gpu_lib):
     assert_close(single.numpy(), oracle.gemm_f16_nt(A, B), "single host call")
 
 
+def test_host_buffer_entry_point(gpu_lib):
+    # gemm_f16_nt_host through the C ABI: pinned and pageable host operands, the caller's device
+    # buffers, copy-in, GEMM and copy-out enqueued on one side stream; D_host must equal the
+    # oracle once the stream is done, including the thin, pair and K = 0 paths.
+    lib = gpu_lib.load()
+    s = torch.cuda.Stream()
+    for (M, N, K), pinned in (((128, 128, 64), True), ((300, 520, 200), True), ((1000, 264, 1000), False),
+                              ((64, 64, 0), True)):
+        A, B = si.custom(M, N, K, seed=M + 2 * N + 3 * K).operands()
+        Ah, Bh = torch.from_numpy(A), torch.from_numpy(B)
+        Dh = torch.full((M, N), float("nan"), dtype=torch.float16)
+        if pinned:
+            Ah, Bh, Dh = Ah.pin_memory(), Bh.pin_memory(), Dh.pin_memory()
+        dA = torch.empty((M, K), dtype=torch.float16, device="cuda")
+        dB = torch.empty((N, K), dtype=torch.float16, device="cuda")
+        dD = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        rc = lib.gemm_f16_nt_host(Ah.data_ptr() if K else None, Bh.data_ptr() if K else None, Dh.data_ptr(),
+                                  M, N, K, dA.data_ptr() if K else None, dB.data_ptr() if K else None,
+                                  dD.data_ptr(), s.cuda_stream, None)
+        assert rc == 0, gpu_lib.status_string(rc)
+        s.synchronize()
+        assert gpu_lib.last_device_status(s)[0] == 0
+        if K == 0:
+            assert not Dh.float().abs().sum().item()
+        else:
+            assert_close(Dh.numpy(), oracle.gemm_f16_nt(A, B), f"host entry {M}x{N}x{K} pinned={pinned}")
+
+
 def test_cuda_graph_capture_and_replay(gpu_lib):
     # Launches captured in a CUDA graph (after a first eager call has done the
     # per-device set-up) replay correctly, including a GEMM that reads the
