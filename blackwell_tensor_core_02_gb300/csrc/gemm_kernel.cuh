@@ -227,7 +227,7 @@ struct Params {
     int32_t raster_group;
     uint32_t debug_flags;
     uint64_t timeout_ns;
-    uint16_t *D;       // for the direct-store epilogue (row-major, ldd = N)
+    uint16_t *D;       // for the epilogues that store with st.global (row-major, ldd = N)
     float *partial;    // split-K workspace [slices][M][N] fp32, when slices > 1
 };
 
