@@ -672,40 +672,40 @@ int describe_with(const DeviceInfo &info, Opts o, int64_t M, int64_t N, int64_t 
     int stages = 0;
     if (o.block_n == 16) {
         st = make_plan<1, 1, 16, 64>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 16, 64>::STAGES;
+        stages = Cfg<1, 1, 16, 64>::STAGES * Cfg<1, 1, 16, 64>::KPS;
     } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 2) {
         st = make_plan<1, 1, 64, 64, 2>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64, 2>::STAGES;
+        stages = Cfg<1, 1, 64, 64, 2>::STAGES * Cfg<1, 1, 64, 64, 2>::KPS;
     } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 4) {
         st = make_plan<1, 1, 64, 64, 4>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64, 4>::STAGES;
+        stages = Cfg<1, 1, 64, 64, 4>::STAGES * Cfg<1, 1, 64, 64, 4>::KPS;
     } else if (o.block_n == 64 && o.block_m == 64 && o.cluster_k == 8) {
         st = make_plan<1, 1, 64, 64, 8>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64, 8>::STAGES;
+        stages = Cfg<1, 1, 64, 64, 8>::STAGES * Cfg<1, 1, 64, 64, 8>::KPS;
     } else if (o.block_n == 64 && o.block_m == 64) {
         st = make_plan<1, 1, 64, 64>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 64>::STAGES;
+        stages = Cfg<1, 1, 64, 64>::STAGES * Cfg<1, 1, 64, 64>::KPS;
     } else if (o.block_n == 64 && o.cluster_k == 2) {
         st = make_plan<1, 1, 64, 128, 2>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 128, 2>::STAGES;
+        stages = Cfg<1, 1, 64, 128, 2>::STAGES * Cfg<1, 1, 64, 128, 2>::KPS;
     } else if (o.block_n == 64 && o.cluster_k == 4) {
         st = make_plan<1, 1, 64, 128, 4>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 128, 4>::STAGES;
+        stages = Cfg<1, 1, 64, 128, 4>::STAGES * Cfg<1, 1, 64, 128, 4>::KPS;
     } else if (o.block_n == 64 && o.cluster_k == 8) {
         st = make_plan<1, 1, 64, 128, 8>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64, 128, 8>::STAGES;
+        stages = Cfg<1, 1, 64, 128, 8>::STAGES * Cfg<1, 1, 64, 128, 8>::KPS;
     } else if (o.block_n == 64) {
         st = make_plan<1, 1, 64>(M, N, K, info, o, false, &plan);
-        stages = Cfg<1, 1, 64>::STAGES;
+        stages = Cfg<1, 1, 64>::STAGES * Cfg<1, 1, 64>::KPS;
     } else if (o.cta_group == 2 && o.consumers == 2) {
         st = make_plan<2, 2, 256>(M, N, K, info, o, false, &plan);
-        stages = Cfg<2, 2, 256>::STAGES;
+        stages = Cfg<2, 2, 256>::STAGES * Cfg<2, 2, 256>::KPS;
     } else if (o.cta_group == 2) {
         st = make_plan<2, 1, 256>(M, N, K, info, o, ws, &plan);
-        stages = Cfg<2, 1, 256>::STAGES;
+        stages = Cfg<2, 1, 256>::STAGES * Cfg<2, 1, 256>::KPS;
     } else {
         st = make_plan<1, 1, 256>(M, N, K, info, o, ws, &plan);
-        stages = Cfg<1, 1, 256>::STAGES;
+        stages = Cfg<1, 1, 256>::STAGES * Cfg<1, 1, 256>::KPS;
     }
     if (st != GEMM_OK) return st;
     out->cta_group = o.cta_group;

@@ -148,12 +148,23 @@ struct Cfg {
     static constexpr int TILE_M = MMA_M * NC;           // rows of D per tile
     static constexpr int UMMA_K = 16;                   // K of one tcgen05.mma kind::f16
     static constexpr int B_ROWS = BLOCK_N / CG;         // rows of B each CTA loads
+    // K tiles of 64 per ring stage.  The MMAs of one K tile of a 64-row tile (tiny or thin) are
+    // so short that the per-stage hand-off (full wait, fence, commit to empty, the producer's
+    // turn) bounds the K-loop, so those tiles move two K tiles per stage (half as many stages
+    // of twice the size; the last stage of a work item may hold one).  Measured on GB300
+    // (graph-timed, us, one vs two K tiles per stage): 256x256x512 (thin) 2.70 vs 2.43,
+    // 512x256x256 2.60 vs 2.46, 256x256x4096 (tiny, K over 4 CTAs) 4.81 vs 4.19, 128x128x64
+    // (one K tile) 1.58 either way; CTA pairs lose with 3 stages of 2 (4096^3 +13 %, 1536^3
+    // +6 %), and narrow tiles 1-3 %.
+    static constexpr int KPS = TINY ? 2 : 1;
     static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
-    static constexpr int A_STAGE = A_BLOCK * NC;
-    static constexpr int B_STAGE = B_ROWS * BLOCK_K * 2;
-    static constexpr int STAGES = TINY ? 12 : (NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)));
-    static constexpr uint32_t TX_BYTES = (A_STAGE + B_STAGE) * CG;      // per stage, on the leader
-    static constexpr uint32_t TX_HALF = (A_STAGE + B_STAGE / 2) * CG;   // the same for a half tile
+    static constexpr int A_KT = A_BLOCK * NC;           // one K tile of A (every consumer's block)
+    static constexpr int A_STAGE = A_KT * KPS;
+    static constexpr int B_KT = B_ROWS * BLOCK_K * 2;   // one K tile of B
+    static constexpr int B_STAGE = B_KT * KPS;
+    static constexpr int STAGES = (TINY ? 12 : (NARROW ? 8 : (NC == 2 ? 4 : (CG == 2 ? 6 : 4)))) / KPS;
+    static constexpr uint32_t TX_BYTES = (A_KT + B_KT) * CG;      // per K tile, on the leader
+    static constexpr uint32_t TX_HALF = (A_KT + B_KT / 2) * CG;   // the same for a half tile
     static constexpr int ACC_BUFS = NC == 2 ? 1 : 2;
     static constexpr int TMEM_COLS = ACC_BUFS * NC * BLOCK_N;           // 512 (all of TMEM), 128 or 32
     static_assert(TMEM_COLS == 512 || TMEM_COLS == 128 || TMEM_COLS == 32, "a power of two of at least 32 columns");
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     // tail.
                     const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
                     const CUtensorMap *mapB = w.n_len < C::BLOCK_N ? &tmBh : &tmB;
-                    const int kt_end = w.kt_begin + C::STAGES < w.kt_end ? w.kt_begin + C::STAGES : w.kt_end;
+                    const int kt_end = w.kt_begin + C::STAGES * C::KPS < w.kt_end ? w.kt_begin + C::STAGES * C::KPS : w.kt_end;
                     for (int kt = w.kt_begin; kt < kt_end; ++kt) {
 #pragma unroll
                         for (int c = 0; c < NC; ++c) {
@@ -438,7 +449,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     const CtaOrigin o = cta_origin(w, CG, static_cast<int32_t>(rank), NC, C::BLOCK_N, C::BLOCK_M);
                     const bool half = w.n_len < C::BLOCK_N;
                     const CUtensorMap *mapB = half ? &tmBh : &tmB;
-                    for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
+                    for (int kt = w.kt_begin; kt < w.kt_end; kt += C::KPS) {
+                        const int nkt = w.kt_end - kt < C::KPS ? w.kt_end - kt : C::KPS;  // K tiles in this stage
                         if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleProducer, kCheckStage,
                                        seq) ||
                             !wait_bounded(bar_empty + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns,
@@ -447,25 +459,31 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                             break;
                         }
                         const uint32_t full = bar_full + 8 * ring.stage;
-                        if (leader) ptx::mbar_arrive_expect_tx(full, half ? C::TX_HALF : C::TX_BYTES);
+                        if (leader) ptx::mbar_arrive_expect_tx(full, (half ? C::TX_HALF : C::TX_BYTES) * nkt);
                         if (!dependency_met) {
                             // the first load of A or B: the previous kernel of
                             // the stream must be complete and its writes visible
                             ptx::griddep_wait();
                             dependency_met = true;
                         }
-                        const int32_t k0 = kt * C::BLOCK_K;
-                        if constexpr (CG == 2) {
-                            const uint32_t full_leader = ptx::mapa(full, 0);
 #pragma unroll
-                            for (int c = 0; c < NC; ++c) {  // consumer c's A rows lie c * MMA_M below
-                                ptx::tma_load_2d_pair(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK, &tmA, full_leader,
-                                                      k0, o.a_row + c * C::MMA_M);
+                        for (int j = 0; j < C::KPS; ++j) {
+                            if (j >= nkt) break;
+                            const int32_t k0 = (kt + j) * C::BLOCK_K;
+                            const uint32_t sa = sA + ring.stage * C::A_STAGE + j * C::A_KT;
+                            const uint32_t sb = sB + ring.stage * C::B_STAGE + j * C::B_KT;
+                            if constexpr (CG == 2) {
+                                const uint32_t full_leader = ptx::mapa(full, 0);
+#pragma unroll
+                                for (int c = 0; c < NC; ++c) {  // consumer c's A rows lie c * MMA_M below
+                                    ptx::tma_load_2d_pair(sa + c * C::A_BLOCK, &tmA, full_leader, k0,
+                                                          o.a_row + c * C::MMA_M);
+                                }
+                                ptx::tma_load_2d_pair(sb, mapB, full_leader, k0, o.b_row);
+                            } else {
+                                ptx::tma_load_2d(sa, &tmA, full, k0, o.a_row);
+                                ptx::tma_load_2d(sb, mapB, full, k0, o.b_row);
                             }
-                            ptx::tma_load_2d_pair(sB + ring.stage * C::B_STAGE, mapB, full_leader, k0, o.b_row);
-                        } else {
-                            ptx::tma_load_2d(sA + ring.stage * C::A_STAGE, &tmA, full, k0, o.a_row);
-                            ptx::tma_load_2d(sB + ring.stage * C::B_STAGE, mapB, full, k0, o.b_row);
                         }
                         ring.advance();
                     }
@@ -502,7 +520,8 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                     }
                     ptx::tcgen05_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc.stage * NC * C::BLOCK_N);
-                    for (int kt = w.kt_begin; kt < w.kt_end; ++kt) {
+                    for (int kt = w.kt_begin; kt < w.kt_end; kt += C::KPS) {
+                        const int nkt = w.kt_end - kt < C::KPS ? w.kt_end - kt : C::KPS;  // K tiles in this stage
                         if (!in_bounds(ring.stage >= 0 && ring.stage < C::STAGES, abort_flag, kRoleMma, kCheckStage, seq) ||
                             !wait_bounded(bar_full + 8 * ring.stage, ring.phase, abort_flag, p.timeout_ns, kRoleMma,
                                           seq)) {
@@ -510,17 +529,21 @@ __global__ void __launch_bounds__(Cfg<CG, NC, BN, BM, KS>::THREADS, 1)
                             break;
                         }
                         ptx::tcgen05_fence_after();
-                        const uint64_t b_desc = ptx::smem_desc_k_sw128(sB + ring.stage * C::B_STAGE);
 #pragma unroll
-                        for (int c = 0; c < NC; ++c) {  // both consumers read the same B stage
-                            const uint64_t a_desc =
-                                ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE + c * C::A_BLOCK);
+                        for (int j = 0; j < C::KPS; ++j) {
+                            if (j >= nkt) break;
+                            const uint64_t b_desc = ptx::smem_desc_k_sw128(sB + ring.stage * C::B_STAGE + j * C::B_KT);
 #pragma unroll
-                            for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
-                                // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
-                                const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
-                                ptx::mma_f16<CG>(d_tmem + c * C::BLOCK_N, a_desc + koff, b_desc + koff, idesc,
-                                                 (kt != w.kt_begin || k != 0) ? 1u : 0u);
+                            for (int c = 0; c < NC; ++c) {  // both consumers read the same B stage
+                                const uint64_t a_desc = ptx::smem_desc_k_sw128(sA + ring.stage * C::A_STAGE +
+                                                                               j * C::A_KT + c * C::A_BLOCK);
+#pragma unroll
+                                for (int k = 0; k < C::BLOCK_K / C::UMMA_K; ++k) {
+                                    // +32 bytes along K inside the 128-byte swizzle row: +2 in units of 16 B.
+                                    const uint64_t koff = static_cast<uint64_t>(k * C::UMMA_K * 2 / 16);
+                                    ptx::mma_f16<CG>(d_tmem + c * C::BLOCK_N, a_desc + koff, b_desc + koff, idesc,
+                                                     (kt + j != w.kt_begin || k != 0) ? 1u : 0u);
+                                }
                             }
                         }
                         ptx::mma_commit<CG>(bar_empty + 8 * ring.stage, pair_mask);  // stage free, both CTAs

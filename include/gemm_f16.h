@@ -288,7 +288,8 @@ typedef struct gemm_f16_launch_info {
     int32_t block_n;          /* tile width: 256, 64 or 16 */
     int32_t split_k;          /* K slices S (1 = no split-K; > 1 adds the reduction kernel) */
     int32_t block_m;          /* rows of D per CTA and consumer: 128 or 64 */
-    int32_t stages;           /* depth of the shared-memory operand ring */
+    int32_t stages;           /* K tiles of 64 the shared-memory operand ring holds (64-row tiles
+                                 move two per ring slot: 6 slots of 2) */
     int64_t clusters;         /* clusters in the grid (CTAs = clusters * cta_group * cluster_k); persistent
                                  unless cluster_k > 1, which runs one cluster per tile */
     int64_t work_items;       /* tiles, half tiles or K slices dealt to the clusters (to the CTAs with
