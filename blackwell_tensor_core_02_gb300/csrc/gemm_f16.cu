@@ -275,8 +275,16 @@ int parse_options(const gemm_f16_options *opts, Opts *o) {
 // So the split pays from 8 K tiles of 64 on, with at least 2 per CTA, while
 // the grid leaves half of the SMs to the next kernel's set-up (tiles * KS at
 // most half the co-resident CTAs); with at least 24 K tiles per CTA a whole
-// wave of clusters still pays.  Automatic: the largest KS of 8, 4, 2 that
-// meets this; a grid capped by max_clusters keeps the persistent tiles.
+// wave of clusters still pays.  Tiny tiles, which stage two K tiles at a time,
+// run a short K faster unsplit, so for them the split starts at 12 K tiles,
+// and clusters of 8 pay only while they fill at most a quarter of the
+// co-resident CTAs (graph-timed, us, KS = 1 / 2 / 4 / 8): 256x256x512 2.68 /
+// 3.06 / 2.83, 256x256x640 2.79 / 3.19 / 2.86, 256x256x896 3.23 / 3.40 / 2.96,
+// 128x256x1024 3.45 / 3.44 / 2.92 / 3.23, 192x192x1024 3.37 / 3.44 / 2.90 /
+// 3.31, 256x128x1536 4.13 / 3.88 / 3.09 / 3.37, 128x128x1024 3.43 / 3.44 / 2.89
+// / 2.85, 128x128x2048 4.84 / 4.30 / 3.19 / 3.03.  Automatic: the largest KS
+// of 8, 4, 2 that meets this; a grid capped by max_clusters keeps the
+// persistent tiles.
 // Forced: at most the number of K tiles, and halved until the device can
 // co-schedule clusters of that size.
 int32_t cluster_k_slot(int32_t ks, int32_t block_m) {
@@ -289,12 +297,14 @@ int32_t cluster_k_for(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, co
     const int64_t ctas = dev.max_clusters[block_m == 64 ? 4 : 3];  // co-resident single CTAs of these tiles
     int32_t ks = o.cluster_k;
     if (ks == 0) {
-        if (o.max_clusters > 0 || k_tiles < 8) return 1;
+        const bool tiny = block_m == 64;
+        if (o.max_clusters > 0 || k_tiles < (tiny ? 12 : 8)) return 1;
         const int32_t options[3] = {8, 4, 2};
         for (int i = 0; i < 3; ++i) {
             const int64_t per_cta = k_tiles / options[i];
             if (per_cta < 2 || tiles > dev.max_clusters[cluster_k_slot(options[i], block_m)]) continue;
-            if (2 * tiles * options[i] <= ctas || per_cta >= 24) return options[i];
+            const int64_t share = tiny && options[i] == 8 ? 4 : 2;  // at most 1/share of the CTAs
+            if (share * tiles * options[i] <= ctas || per_cta >= 24) return options[i];
         }
         return 1;
     }
@@ -417,17 +427,21 @@ void resolve_config(int64_t M, int64_t N, int64_t K, const DeviceInfo &dev, bool
         o->consumers = 1;
         small_tiles(M, N, K, dev, o);
         // Thin 64 x 16 tiles for the shortest of these problems: where the tiny tiles
-        // apply with a K of at most 512 (8 K tiles) and the thin tiles still fit one
-        // wave, each CTA loads and drains a quarter as much.  Measured on GB300
-        // (graph-timed, us, thin vs the default before them): 128x128x64 1.57 vs 1.76,
-        // 128x256x256 2.05 vs 2.24, 256x256x512 2.78 vs 2.88 (tiny tiles with K over
-        // 4-CTA clusters); with a longer K the cluster K split wins (256x128x1024 3.96
-        // vs 3.22), past one wave the tiny tiles (512x512x512 4.57 vs 2.85).  64 x 8
-        // tiles gained nothing more (1.60 and 2.90), 64 x 32 less (1.74 and 2.83).
+        // apply with a K of at most 768 (12 K tiles) and the thin tiles fill at most
+        // half of the co-resident CTAs, each CTA loads and drains a quarter as much.
+        // Measured on GB300 (graph-timed, us, thin vs the best other tiles): 128x128x64
+        // 1.57 vs 1.76, 256x256x512 2.48 vs 2.68, 256x256x640 2.63 vs 2.79, 256x256x768
+        // 2.81 vs 2.94, 128x256x768 2.83 vs 2.91; with a longer K the cluster K split
+        // wins (256x256x896 3.09 vs 2.96, 128x128x1024 3.25 vs 2.85), and with more thin
+        // tiles the tiny ones unsplit, whose operands cross L2 a quarter as often
+        // (thin tiles in brackets: 320x256x512 2.64 vs 2.64 (80), 384x256x512 2.73 vs
+        // 2.63 (96), 512x256x512 2.91 vs 2.65 (128), 384x384x256 2.55 vs 2.33 (144),
+        // 384x384x64 2.11 vs 1.98 (144)).  64 x 8 tiles gained nothing more (1.60 and
+        // 2.90 at 128x128x64 and 256x256x512), 64 x 32 less (1.74 and 2.83).
         int64_t ctas = dev.max_clusters[4];
         if (o->max_clusters > 0 && o->max_clusters < ctas) ctas = o->max_clusters;
         const int64_t thin_tiles = ((M + 63) / 64) * ((N + 15) / 16);
-        if (auto_tile && o->block_m == 64 && k_tiles <= 8 && thin_tiles <= ctas) {
+        if (auto_tile && o->block_m == 64 && k_tiles <= 12 && 2 * thin_tiles <= ctas) {
             o->block_n = 16;
             o->cluster_k = 1;
         }

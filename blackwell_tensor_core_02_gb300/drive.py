@@ -44,7 +44,7 @@ def main(argv=None) -> None:
     ap.add_argument("--cta-group", type=int, default=0)
     ap.add_argument("--consumers", type=int, nargs="+", default=[0],
                     help="MMA consumers 1 or 2, 0 for the shape's default; several: each in turn")
-    ap.add_argument("--block-n", type=int, default=0, help="tile width: 64, 256, or 0 for the shape's default")
+    ap.add_argument("--block-n", type=int, default=0, help="tile width: 16 (thin 64 x 16 tiles), 64, 256, or 0 for the shape's default")
     ap.add_argument("--block-m", type=int, default=0, help="rows per CTA: 64 (with 64-wide tiles), 128, or 0")
     ap.add_argument("--cluster-k", type=int, default=0,
                     help="tiny tiles: K split across clusters of 2, 4 or 8 CTAs; 1 none; 0 the shape's default")

@@ -114,12 +114,14 @@ typedef enum gemm_status {
  *                 K-loop is at most 8 tiles of 64 and the 128 x 64 tiles fit
  *                 one wave of co-resident CTAs, else 256; and with block_m
  *                 and cluster_k at 0 too, 16 where the tiny tiles of block_m
- *                 64 would run a K-loop of at most 8 tiles of 64 and the
- *                 64 x 16 tiles fit one wave.  Other values:
+ *                 64 would run a K-loop of at most 12 tiles of 64 and the
+ *                 64 x 16 tiles fill at most half of the co-resident CTAs.
+ *                 Other values:
  *                 GEMM_ERR_INVALID_ARG.
  *   block_m       rows of D per CTA.  128: the tiles above.  64 (needs
  *                 block_n 0 or 64, which then means 64): single CTAs with
- *                 64 x 64 tiles, MMAs of M = 64 and a 12-stage ring; for the
+ *                 64 x 64 tiles, MMAs of M = 64 and a ring of 6 stages of
+ *                 two K tiles each (as for the thin tiles); for the
  *                 smallest problems.  Not on the pages.  0 (default): with
  *                 block_n resolved to 64, 64 when the 64 x 64 tiles number at
  *                 most two thirds of the co-resident CTAs, else 128.  Other
@@ -139,9 +141,10 @@ typedef enum gemm_status {
  *                 1/cluster_k of the tile's operands, which is what bounds
  *                 small problems.  Not on the pages.  1: no K split.
  *                 0 (default): with max_clusters 0 and at least 8 K tiles
- *                 of 64, the largest of 8, 4, 2 that leaves each CTA at
- *                 least 2 K tiles, lets all the clusters run at once and
- *                 keeps the grid within half the co-resident CTAs (within
+ *                 of 64 (12 for tiny tiles), the largest of 8, 4, 2 that
+ *                 leaves each CTA at least 2 K tiles, lets all the clusters
+ *                 run at once and keeps the grid within half the co-resident
+ *                 CTAs (a quarter for tiny tiles in clusters of 8; within
  *                 all of them from 24 K tiles per CTA), else 1.  With
  *                 block_m 0 as well, a long K can turn tiny tiles into
  *                 narrow ones: where the tiny tiles get no split but the

@@ -598,6 +598,9 @@ def test_describe_for_the_consumer_count_rule(M, N, K, consumers):
     (512, 512, 4096, 128, 4), (512, 512, 512, 64, 1), (512, 512, 1024, 64, 1), (576, 576, 1024, 64, 1),
     (640, 640, 4096, 128, 2), (768, 512, 4096, 128, 2), (512, 1024, 4096, 128, 2), (768, 768, 4096, 128, 2),
     (768, 768, 2048, 128, 1), (384, 384, 2048, 128, 4), (512, 512, 2048, 128, 2),
+    # tiny tiles: no split below 12 K tiles; clusters of 8 only within a quarter of the CTAs
+    (384, 384, 640, 64, 1), (256, 256, 896, 64, 4), (128, 128, 1024, 64, 8), (128, 256, 1024, 64, 4),
+    (192, 192, 1024, 64, 4),
 ])
 def test_describe_for_the_cluster_k_split_rule(M, N, K, bm, ks):
     c = g.describe_for(M, N, K, GB300)
@@ -611,14 +614,17 @@ def test_describe_for_the_cluster_k_split_rule(M, N, K, bm, ks):
 
 @pytest.mark.parametrize("M,N,K,thin", [
     (128, 128, 64, True), (256, 256, 512, True), (128, 128, 512, True), (256, 256, 448, True),
-    (128, 256, 256, True), (1, 8, 8, True), (384, 384, 256, True),  # 6 x 24 = 144 thin tiles: one wave
-    (256, 256, 576, False),   # 9 K tiles: the cluster K split instead
-    (512, 512, 512, False),   # 8 x 32 = 256 thin tiles: more than a wave, tiny tiles
+    (128, 256, 256, True), (1, 8, 8, True), (256, 256, 576, True), (256, 256, 768, True),  # up to 12 K tiles
+    (256, 256, 832, False),   # 13 K tiles: the cluster K split instead
+    (320, 256, 512, False),   # 5 x 16 = 80 thin tiles: more than half a wave, tiny tiles
+    (384, 384, 256, False),   # 6 x 24 = 144 thin tiles
+    (512, 512, 512, False),   # 8 x 32 = 256 thin tiles: more than a wave
     (1024, 1024, 512, False),  # narrow tiles
 ])
 def test_describe_for_the_thin_tile_rule(M, N, K, thin):
-    """Thin 64 x 16 tiles where the tiny tiles would run a K-loop of at most 8 tiles of 64 and
-    the thin tiles fit one wave; only when block_n, block_m and cluster_k are all left open."""
+    """Thin 64 x 16 tiles where the tiny tiles would run a K-loop of at most 12 tiles of 64 and
+    the thin tiles fill at most half of the co-resident CTAs; only when block_n, block_m and
+    cluster_k are all left open."""
     c = g.describe_for(M, N, K, GB300)
     if thin:
         tiles = -(-M // 64) * -(-N // 16)
@@ -682,12 +688,12 @@ def test_describe_for_random_shapes_keep_the_launch_rules(device):
         if c["block_n"] == 16:  # thin tiles: short K, one wave, no split
             tiles = -(-M // 64) * -(-N // 16)
             assert (c["cta_group"], c["block_m"], c["cluster_k"], c["split_k"], c["workspace_bytes"]) == (1, 64, 1, 1, 0)
-            assert k_tiles <= 8 and tiles <= device[4] and c["work_items"] == tiles == c["clusters"]
+            assert k_tiles <= 12 and 2 * tiles <= device[4] and c["work_items"] == tiles == c["clusters"]
         if c["cluster_k"] > 1:
             assert c["block_n"] == 64 and c["split_k"] == 1
             assert c["clusters"] == tiles and c["work_items"] == tiles * c["cluster_k"]
             assert c["clusters"] <= device[slots[(c["block_m"], c["cluster_k"])]]
-            assert c["cluster_k"] <= k_tiles and k_tiles >= 8
+            assert c["cluster_k"] <= k_tiles and k_tiles >= (12 if c["block_m"] == 64 else 8)
         elif c["block_n"] == 64:
             assert c["work_items"] == tiles
         if c["split_k"] > 1:

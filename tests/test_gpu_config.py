@@ -19,14 +19,14 @@ def _resident_tiny_ctas(gpu_lib):
 
 
 def test_smallest_problems_take_thin_or_tiny_tiles(gpu_lib):
-    # the two small workloads: thin 64 x 16 tiles, one per CTA (K at most 512, one wave)
+    # the two small workloads: thin 64 x 16 tiles, one per CTA (K at most 768, half a wave)
     c1 = gpu_lib.describe(128, 128, 64)
     assert (c1["cta_group"], c1["block_n"], c1["block_m"], c1["split_k"], c1["cluster_k"], c1["clusters"],
             c1["work_items"], c1["stages"]) == (1, 16, 64, 1, 1, 16, 16, 12)
     c2 = gpu_lib.describe(256, 256, 512)
     assert (c2["cta_group"], c2["block_n"], c2["block_m"], c2["split_k"], c2["cluster_k"], c2["clusters"],
             c2["work_items"]) == (1, 16, 64, 1, 1, 64, 64)
-    for M, N, K in ((128, 128, 512), (256, 256, 448), (128, 256, 256)):  # K <= 512: thin tiles as well
+    for M, N, K in ((128, 128, 512), (256, 256, 448), (128, 256, 256), (256, 256, 768)):  # thin tiles as well
         c = gpu_lib.describe(M, N, K)
         tiles = -(-M // 64) * -(-N // 16)
         assert (c["block_n"], c["block_m"], c["cluster_k"], c["work_items"], c["clusters"]) == \
@@ -43,16 +43,18 @@ def test_smallest_problems_take_thin_or_tiny_tiles(gpu_lib):
 
 
 def test_long_k_on_few_tiles_splits_k_across_clusters(gpu_lib):
-    # from 8 K tiles of 64 on, 64-wide tiles split K across a cluster: the largest of 8, 4, 2 CTAs
-    # that leaves each at least 2 K tiles, with tiles * cluster_k at most half the co-resident
-    # CTAs (a whole wave with at least 24 K tiles per CTA); narrow tiles instead of tiny ones
+    # from 8 K tiles of 64 on (12 for tiny tiles), 64-wide tiles split K across a cluster: the
+    # largest of 8, 4, 2 CTAs that leaves each at least 2 K tiles, with tiles * cluster_k at most
+    # half the co-resident CTAs (a quarter for tiny tiles in clusters of 8; a whole wave with at
+    # least 24 K tiles per CTA); narrow tiles instead of tiny ones
     # where the tiny ones get no split but the narrow ones do with at least 16 K tiles per CTA,
     # or where the tiny ones split in 2 and the narrow ones can split in 4 with at least 8
     for (M, N, K), bm, ks in (((256, 256, 4096), 64, 4), ((128, 128, 4096), 64, 8), ((256, 256, 1024), 64, 4),
                               ((128, 1024, 1024), 64, 2), ((384, 384, 2048), 128, 4), ((512, 512, 4096), 128, 4),
                               ((512, 512, 512), 64, 1), ((512, 512, 1024), 64, 1), ((576, 576, 1024), 64, 1),
                               ((640, 640, 4096), 128, 2), ((768, 512, 4096), 128, 2), ((512, 1024, 4096), 128, 2),
-                              ((768, 768, 4096), 128, 2), ((768, 768, 2048), 128, 1), ((512, 512, 2048), 128, 2)):
+                              ((768, 768, 4096), 128, 2), ((768, 768, 2048), 128, 1), ((512, 512, 2048), 128, 2),
+                              ((384, 384, 640), 64, 1), ((256, 256, 896), 64, 4), ((128, 256, 1024), 64, 4)):
         c = gpu_lib.describe(M, N, K)
         tiles = -(-M // bm) * -(-N // 64)
         assert (c["block_n"], c["block_m"], c["cluster_k"], c["split_k"]) == (64, bm, ks, 1), (M, N, K)
