@@ -150,13 +150,15 @@ struct Cfg {
     static constexpr int B_ROWS = BLOCK_N / CG;         // rows of B each CTA loads
     // K tiles of 64 per ring stage.  The MMAs of one K tile of a 64-row tile (tiny or thin) are
     // so short that the per-stage hand-off (full wait, fence, commit to empty, the producer's
-    // turn) bounds the K-loop, so those tiles move two K tiles per stage (half as many stages
-    // of twice the size; the last stage of a work item may hold one).  Measured on GB300
+    // turn) bounds the K-loop, so tiny tiles move two K tiles per stage and thin ones four
+    // (fewer, larger stages; the last stage of a work item may hold fewer).  Measured on GB300
     // (graph-timed, us, one vs two K tiles per stage): 256x256x512 (thin) 2.70 vs 2.43,
     // 512x256x256 2.60 vs 2.46, 256x256x4096 (tiny, K over 4 CTAs) 4.81 vs 4.19, 128x128x64
-    // (one K tile) 1.58 either way; CTA pairs lose with 3 stages of 2 (4096^3 +13 %, 1536^3
-    // +6 %), and narrow tiles 1-3 %.
-    static constexpr int KPS = TINY ? 2 : 1;
+    // (one K tile) 1.58 either way; thin tiles, two vs four: 256x256x512 2.43 vs 2.40,
+    // 256x256x768 2.80 vs 2.72, 128x256x768 2.77 vs 2.69 (three: 2.44, 2.76, 2.74); tiny tiles
+    // lose with four (256x256x4096 4.21 vs 4.45); CTA pairs lose with 3 stages of 2 (4096^3
+    // +13 %, 1536^3 +6 %), and narrow tiles 1-3 %.
+    static constexpr int KPS = THIN ? 4 : (TINY ? 2 : 1);
     static constexpr int A_BLOCK = BLOCK_M * BLOCK_K * 2;
     static constexpr int A_KT = A_BLOCK * NC;           // one K tile of A (every consumer's block)
     static constexpr int A_STAGE = A_KT * KPS;

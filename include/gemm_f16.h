@@ -107,8 +107,9 @@ typedef enum gemm_status {
  *                 coalesced warp stores; for small, latency-bound problems.
  *                 16 (needs cta_group 0 or 1, one consumer, block_m 0 or 64,
  *                 cluster_k 0 or 1): thin single-CTA 64 x 16 tiles, MMAs of
- *                 M = 64, N = 16, 32 columns of tensor memory, each row of D
- *                 stored straight from registers; for the shortest problems.
+ *                 M = 64, N = 16, 32 columns of tensor memory, a ring of 3
+ *                 stages of four K tiles, each row of D stored straight from
+ *                 registers; for the shortest problems.
  *                 Not on the pages: they fix the tile at 128 or 256 x 256.  0
  *                 (default): 64 when cta_group is 0, consumers is not 2, the
  *                 K-loop is at most 8 tiles of 64 and the 128 x 64 tiles fit
@@ -121,7 +122,7 @@ typedef enum gemm_status {
  *   block_m       rows of D per CTA.  128: the tiles above.  64 (needs
  *                 block_n 0 or 64, which then means 64): single CTAs with
  *                 64 x 64 tiles, MMAs of M = 64 and a ring of 6 stages of
- *                 two K tiles each (as for the thin tiles); for the
+ *                 two K tiles each; for the
  *                 smallest problems.  Not on the pages.  0 (default): with
  *                 block_n resolved to 64, 64 when the 64 x 64 tiles number at
  *                 most two thirds of the co-resident CTAs, else 128.  Other
@@ -291,8 +292,8 @@ typedef struct gemm_f16_launch_info {
     int32_t block_n;          /* tile width: 256, 64 or 16 */
     int32_t split_k;          /* K slices S (1 = no split-K; > 1 adds the reduction kernel) */
     int32_t block_m;          /* rows of D per CTA and consumer: 128 or 64 */
-    int32_t stages;           /* K tiles of 64 the shared-memory operand ring holds (64-row tiles
-                                 move two per ring slot: 6 slots of 2) */
+    int32_t stages;           /* K tiles of 64 the shared-memory operand ring holds (tiny tiles
+                                 move two per ring slot, thin tiles four) */
     int64_t clusters;         /* clusters in the grid (CTAs = clusters * cta_group * cluster_k); persistent
                                  unless cluster_k > 1, which runs one cluster per tile */
     int64_t work_items;       /* tiles, half tiles or K slices dealt to the clusters (to the CTAs with
