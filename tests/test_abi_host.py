@@ -244,10 +244,16 @@ def test_default_raster_group_keeps_a_32mib_a_panel():
 
 
 def test_schedule_grouped_order():
-    # 16 x 16 tiles, groups of 8 M-tiles: M fastest inside a group, then N.
+    # 16 x 16 tiles, groups of 8 M-tiles: M fastest inside a group, then N; the second
+    # group walks N backwards, starting on the B panels the first one ended on.
     order = [g.schedule(4096, 4096, 2, 8, 1, 0, i)[:2] for i in range(256)]
     assert order[:9] == [(m, 0) for m in range(8)] + [(0, 1)]
-    assert order[127] == (7, 15) and order[128] == (8, 0) and order[255] == (15, 15)
+    assert order[127] == (7, 15) and order[128] == (8, 15) and order[136] == (8, 14)
+    assert order[255] == (15, 0)
+    # a ragged last group (5 of 3 + 2 M-tiles) also turns, and every tile comes once
+    order = [g.schedule(1280, 1024, 2, 3, 1, 0, i)[:2] for i in range(20)]
+    assert order[12:] == [(3, 3), (4, 3), (3, 2), (4, 2), (3, 1), (4, 1), (3, 0), (4, 0)]
+    assert sorted(order) == [(m, n) for m in range(5) for n in range(4)]
 
 
 @pytest.mark.parametrize("M,N,K,cg,clusters,slices", [
