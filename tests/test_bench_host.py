@@ -94,3 +94,14 @@ def test_reference_budget_must_be_positive():
     out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--ref-seconds", "0"],
                          cwd=ROOT, capture_output=True, text=True, timeout=120)
     assert out.returncode != 0 and "--ref-seconds" in out.stderr
+
+
+def test_roofline_peak_follows_the_length_of_the_timed_region():
+    """A long back-to-back region runs under the power cap and is set against the measured
+    sustained peak; a short burst against the burst peak; with no sustained figure, burst."""
+    peak, regime, src = bench.roofline_peak(0.86, 1912.4, 1724.7, "burst source")
+    assert (peak, regime) == (1724.7, "sustained") and "sustained" in src and "0.86 s" in src
+    assert bench.roofline_peak(0.0017, 1912.4, 1724.7, "burst source") == (1912.4, "burst", "burst source")
+    assert bench.roofline_peak(5.0, 1912.4, None, "burst source") == (1912.4, "burst", "burst source")
+    assert bench.roofline_peak(bench.SUSTAINED_REGION_S, 1912.4, 1724.7, "b")[1] == "sustained"
+

@@ -40,6 +40,10 @@ def test_main_arm_prints_the_contract_line():
     r = d["roofline"]
     assert (r["bound"], r["unit"]) == ("tensor", "TFLOP/s") and r["peak"] > 0
     assert r["frac"] == pytest.approx(r["achieved"] / r["peak"], rel=1e-9)
+    # 50 launches of ~80 us are a burst: set against the measured burst peak
+    timed_s = steps * d["ms_per_step"] / 1e3
+    assert r["peak_regime"] == ("sustained" if timed_s >= bench.SUSTAINED_REGION_S else "burst")
+    assert r["frac_of_burst"] == pytest.approx(r["achieved"] / bench.measured_peak()[0], rel=1e-9)
     assert r["traffic"] is None or r["traffic"] > 0
     e = d["e2e"]
     assert e["unit"] == d["unit"] and 0 < e["value"] < d["value"]
