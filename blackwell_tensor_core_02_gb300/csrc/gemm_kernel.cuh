@@ -58,15 +58,16 @@
 // coalesced warp stores.  Not on the pages, which fix the tile.
 //
 // Tiny tiles (BM = 64, BN = 64): for problems whose 64 x 64 tiles fill at most
-// two thirds of a wave, the same again with MMAs of M = 64 and a 12-stage ring of
-// 16 KiB stages.  An M = 64 accumulator takes lanes 0-15 of each 32-lane
+// two thirds of a wave, the same again with MMAs of M = 64 and a ring of 6
+// stages of two 16 KiB K tiles.  An M = 64 accumulator takes lanes 0-15 of each 32-lane
 // quarter of TMEM (row r in lane 32 * (r / 16) + r % 16), so each epilogue
 // warp reads its quarter as usual and stores 16 rows from its lanes 0-15.
 //
 // Thin tiles (BM = 64, BN = 16): the tiny tiles cut four times finer along N
 // for the shortest problems, MMAs of M = 64, N = 16, two 16-column
-// accumulators in the smallest TMEM allocation (32 columns), and an epilogue
-// that stores each row's 32 bytes straight from registers.  Each CTA then
+// accumulators in the smallest TMEM allocation (32 columns), a ring of 3 stages
+// of four 10 KiB K tiles, and an epilogue that stores each row's 32 bytes
+// straight from registers.  Each CTA then
 // loads and drains a quarter as much per tile, which shortens the one pass
 // of the data path such a problem is.
 //

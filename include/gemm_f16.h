@@ -111,9 +111,11 @@ typedef enum gemm_status {
  *                 stages of four K tiles, each row of D stored straight from
  *                 registers; for the shortest problems.
  *                 Not on the pages: they fix the tile at 128 or 256 x 256.  0
- *                 (default): 64 when cta_group is 0, consumers is not 2, the
- *                 K-loop is at most 8 tiles of 64 and the 128 x 64 tiles fit
- *                 one wave of co-resident CTAs, else 256; and with block_m
+ *                 (default): 64 when cta_group is 0, consumers is not 2 and
+ *                 the 128 x 64 tiles fit one wave of co-resident CTAs (with
+ *                 a workspace, unless no cluster K split applies and split-K
+ *                 over 256-wide tiles would take 8 slices or more), else
+ *                 256; and with block_m
  *                 and cluster_k at 0 too, 16 where the tiny tiles of block_m
  *                 64 would run a K-loop of at most 12 tiles of 64 and the
  *                 64 x 16 tiles fill at most half of the co-resident CTAs.
