@@ -69,9 +69,12 @@ typedef enum gemm_status {
  *   max_clusters  cap on the persistent grid, in clusters (CTA pairs for
  *                 cta_group 2); 0 = as many as are co-resident on the device.
  *   raster_group  L2 grouping of the tile scheduler, in M-tiles (TIRx notes
- *                 V6, "l2_group_size"); 0 = chosen from the shape: the largest
- *                 group whose A panel (group x the tile's rows x K fp16)
- *                 fits in 32 MiB, between 1 and the number of M-tiles.
+ *                 V6, "l2_group_size"); inside a group M varies fastest, and
+ *                 odd groups walk N backwards (a serpentine, so a group starts
+ *                 on the B panels the previous one ended on).  0 = chosen from
+ *                 the shape: the largest group whose A panel (group x the
+ *                 tile's rows x K fp16) fits in 32 MiB, between 1 and the
+ *                 number of M-tiles.
  *   debug_flags   test hook, 0 in normal use.  1 starts the producer end of
  *                 the SMEM ring at phase 0 instead of 1 -- the pages' "subtlest
  *                 bug" ("GEMM III", "opposite initial phases") -- so that every
