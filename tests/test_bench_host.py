@@ -105,3 +105,27 @@ def test_roofline_peak_follows_the_length_of_the_timed_region():
     assert bench.roofline_peak(5.0, 1912.4, None, "burst source") == (1912.4, "burst", "burst source")
     assert bench.roofline_peak(bench.SUSTAINED_REGION_S, 1912.4, 1724.7, "b")[1] == "sustained"
 
+
+
+def test_kernel_labels_name_each_configuration():
+    """The compact workload list names the kernel from gemm_f16_nt_describe's fields."""
+    base = dict(cta_group=1, consumers=1, block_n=64, block_m=64, cluster_k=1, clusters=16)
+    assert bench.kernel_label({**base, "block_n": 16}) == "thin 64x16, 16 clusters"
+    assert bench.kernel_label(base) == "tiny 64x64, 16 clusters"
+    assert bench.kernel_label({**base, "cluster_k": 4}) == "tiny 64x64, K over 4 CTAs, 16 clusters"
+    assert bench.kernel_label({**base, "block_m": 128, "cluster_k": 2}) == "narrow 128x64, K over 2 CTAs, 16 clusters"
+    pair = dict(cta_group=2, consumers=1, block_n=256, block_m=128, cluster_k=1, clusters=76)
+    assert bench.kernel_label(pair) == "pair 256x256, 76 clusters"
+    assert bench.kernel_label({**pair, "consumers": 2}) == "pair 512x256, 2 consumers, 76 clusters"
+    assert bench.kernel_label({**pair, "cta_group": 1, "clusters": 152}) == "single 128x256, 152 clusters"
+
+
+def test_workloads_summary_keeps_one_short_entry_per_workload():
+    w = {"workload": "square_4096", "ms_median": 0.0812345, "tflops": 1692.04, "cublas_ms_median": 0.0833,
+         "hbm_gbs_compulsory": 1239.11, "parity_vs_oracle": {"pass": True},
+         "kernel": dict(cta_group=2, consumers=1, block_n=256, block_m=128, cluster_k=1, clusters=76)}
+    [s] = bench.workloads_summary([w])
+    assert s == {"workload": "square_4096", "kernel": "pair 256x256, 76 clusters", "us": 81.23, "tflops": 1692.0,
+                 "cublas_us": 83.3, "hbm_gbs": 1239.1, "parity": True}
+    [s] = bench.workloads_summary([{**w, "cublas_ms_median": None, "parity_vs_oracle": None}])
+    assert s["cublas_us"] is None and s["parity"] is None
